@@ -1,0 +1,253 @@
+"""Python binding of libpath_attn (PaTH attention on GB300, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpath_attn.so``; PyTorch supplies device memory and streams.
+The functions carry the names of the C entry points in ``include/path_attn.h``.
+There is no fallback: if the library is missing or a call fails, a
+``PathAttnError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "PathAttnError", "load_library", "path_attn_prefill_fwd", "path_attn_decode_step",
+    "path_attn_build_kcache", "path_attn_prefill_workspace_size",
+    "path_attn_decode_workspace_size", "path_attn_build_kcache_workspace_size",
+    "path_attn_device_status", "path_attn_selftest_bounded_wait", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpath_attn.so")
+
+PATH_OK, PATH_ERR_INVALID_ARG, PATH_ERR_UNSUPPORTED, PATH_ERR_CUDA, PATH_ERR_TIMEOUT = range(5)
+PATH_F32, PATH_BF16 = 0, 1
+
+EXPORTED_SYMBOLS = (
+    "path_attn_prefill_workspace_size", "path_attn_prefill_fwd",
+    "path_attn_decode_workspace_size", "path_attn_decode_step",
+    "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
+    "path_attn_device_status", "path_attn_selftest_bounded_wait",
+    "path_attn_status_string", "path_attn_last_error", "path_attn_version",
+)
+
+
+class PathAttnError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (_STATUS.get(status, status), message))
+        self.status = status
+
+
+_STATUS = {PATH_OK: "PATH_OK", PATH_ERR_INVALID_ARG: "PATH_ERR_INVALID_ARG",
+           PATH_ERR_UNSUPPORTED: "PATH_ERR_UNSUPPORTED", PATH_ERR_CUDA: "PATH_ERR_CUDA",
+           PATH_ERR_TIMEOUT: "PATH_ERR_TIMEOUT"}
+
+
+class PrefillDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("seq_len", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("chunk", ctypes.c_int32)]
+
+
+class DecodeDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("cache_capacity", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_lib = None
+_lock = threading.Lock()
+_VP = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+
+
+def load_library(path: str | None = None):
+    """Load libpath_attn.so (built by ``build.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise PathAttnError(PATH_ERR_CUDA, "libpath_attn.so not built (%s); run "
+                                "dependent_positional_attention_gb300.build.build()" % p)
+        lib = ctypes.CDLL(p)
+        pd, dd = ctypes.POINTER(PrefillDesc), ctypes.POINTER(DecodeDesc)
+        lib.path_attn_prefill_workspace_size.argtypes = [pd]
+        lib.path_attn_prefill_workspace_size.restype = _SZ
+        lib.path_attn_prefill_fwd.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                              _VP, _SZ, _VP]
+        lib.path_attn_decode_workspace_size.argtypes = [dd]
+        lib.path_attn_decode_workspace_size.restype = _SZ
+        lib.path_attn_decode_step.argtypes = [dd, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
+                                              _VP, _VP, _VP, _VP, _SZ, _VP]
+        lib.path_attn_build_kcache_workspace_size.argtypes = [pd]
+        lib.path_attn_build_kcache_workspace_size.restype = _SZ
+        lib.path_attn_build_kcache.argtypes = [pd, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP,
+                                               _SZ, _VP]
+        lib.path_attn_device_status.argtypes = [ctypes.c_int32]
+        lib.path_attn_selftest_bounded_wait.argtypes = [ctypes.c_uint32, _VP]
+        lib.path_attn_status_string.restype = ctypes.c_char_p
+        lib.path_attn_last_error.restype = ctypes.c_char_p
+        lib.path_attn_version.restype = ctypes.c_int32
+        for f in ("path_attn_prefill_fwd", "path_attn_decode_step", "path_attn_build_kcache",
+                  "path_attn_device_status", "path_attn_selftest_bounded_wait"):
+            getattr(lib, f).restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status):
+    if status != PATH_OK:
+        raise PathAttnError(status, load_library().path_attn_last_error().decode())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return PATH_F32
+    if t.dtype == torch.bfloat16:
+        return PATH_BF16
+    raise PathAttnError(PATH_ERR_UNSUPPORTED, "dtype %s not supported" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, shape=None, dtype=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise PathAttnError(PATH_ERR_INVALID_ARG, "%s must be a contiguous CUDA tensor" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise PathAttnError(PATH_ERR_INVALID_ARG, "%s has shape %s, expected %s"
+                            % (name, tuple(t.shape), tuple(shape)))
+    if dtype is not None and t.dtype != dtype:
+        raise PathAttnError(PATH_ERR_INVALID_ARG, "%s has dtype %s, expected %s"
+                            % (name, t.dtype, dtype))
+
+
+def _prefill_desc(q, scale, chunk):
+    B, H, L, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    return PrefillDesc(B, H, L, d, _dtype_code(q), float(scale), int(chunk))
+
+
+def path_attn_prefill_workspace_size(desc: PrefillDesc) -> int:
+    return int(load_library().path_attn_prefill_workspace_size(ctypes.byref(desc)))
+
+
+def path_attn_prefill_fwd(q, k, v, w, beta, log_f=None, out=None, lse=None, scale=None,
+                          chunk=0, workspace=None, stream=None, want_lse=True):
+    """Causal PaTH / PaTH-FoX attention forward (see path_attn_prefill_fwd in
+    include/path_attn.h).  q, k, v, w: [B, H, L, d] CUDA tensors (float32 or
+    bfloat16); beta, log_f: float32 [B, H, L].  Returns (out, lse)."""
+    import torch
+    lib = load_library()
+    B, H, L, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (w, "w")):
+        _need(t, n, (B, H, L, d), q.dtype)
+    _need(beta, "beta", (B, H, L), torch.float32)
+    if log_f is not None:
+        _need(log_f, "log_f", (B, H, L), torch.float32)
+    desc = _prefill_desc(q, scale, chunk)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (B, H, L, d), q.dtype)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, L), device=q.device, dtype=torch.float32)
+    if lse is not None:
+        _need(lse, "lse", (B, H, L), torch.float32)
+    ws_bytes = path_attn_prefill_workspace_size(desc)
+    if ws_bytes == 0:
+        _check(lib.path_attn_prefill_fwd(ctypes.byref(desc), *([None] * 9), 0, None))
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    _check(lib.path_attn_prefill_fwd(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out, lse
+
+
+def path_attn_decode_workspace_size(desc: DecodeDesc) -> int:
+    return int(load_library().path_attn_decode_workspace_size(ctypes.byref(desc)))
+
+
+def decode_desc(k_cache, scale=None):
+    B, H, cap, d = k_cache.shape
+    if scale is None:
+        scale = d ** -0.5
+    return DecodeDesc(B, H, d, cap, _dtype_code(k_cache), float(scale))
+
+
+def path_attn_decode_step(k_cache, v_cache, cache_len, q_t, k_t, v_t, w_t, beta_t, out=None,
+                          scale=None, workspace=None, stream=None):
+    """One PaTH decode step (see path_attn_decode_step in include/path_attn.h).
+    k_cache, v_cache: [B, H, capacity, d]; q_t .. w_t: [B, H, d]; beta_t:
+    float32 [B, H].  Updates k_cache in place, writes slot cache_len of both
+    caches, returns out [B, H, d]."""
+    import torch
+    lib = load_library()
+    B, H, cap, d = k_cache.shape
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", (B, H, cap, d), k_cache.dtype)
+    for t, n in ((q_t, "q_t"), (k_t, "k_t"), (v_t, "v_t"), (w_t, "w_t")):
+        _need(t, n, (B, H, d), k_cache.dtype)
+    _need(beta_t, "beta_t", (B, H), torch.float32)
+    desc = decode_desc(k_cache, scale)
+    if out is None:
+        out = torch.empty_like(q_t)
+    _need(out, "out", (B, H, d), k_cache.dtype)
+    if workspace is None:
+        n = path_attn_decode_workspace_size(desc)
+        workspace = torch.empty(max(n, 16), device=k_cache.device, dtype=torch.uint8)
+    _check(lib.path_attn_decode_step(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), int(cache_len), _ptr(q_t), _ptr(k_t),
+        _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def path_attn_build_kcache_workspace_size(desc: PrefillDesc) -> int:
+    return int(load_library().path_attn_build_kcache_workspace_size(ctypes.byref(desc)))
+
+
+def path_attn_build_kcache(k, w, beta, k_cache, workspace=None, stream=None):
+    """Write k_cache[:, :, j] = H_{L-1} ... H_{j+1} k_j for j < L (see
+    path_attn_build_kcache in include/path_attn.h)."""
+    import torch
+    lib = load_library()
+    B, H, L, d = k.shape
+    _need(k, "k")
+    _need(w, "w", (B, H, L, d), k.dtype)
+    _need(beta, "beta", (B, H, L), torch.float32)
+    _need(k_cache, "k_cache")
+    desc = _prefill_desc(k, None, 0)
+    if workspace is None:
+        n = path_attn_build_kcache_workspace_size(desc)
+        workspace = torch.empty(max(n, 16), device=k.device, dtype=torch.uint8)
+    _check(lib.path_attn_build_kcache(
+        ctypes.byref(desc), _ptr(k), _ptr(w), _ptr(beta), _ptr(k_cache), k_cache.shape[2],
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return k_cache
+
+
+def path_attn_device_status(clear=True):
+    """Synchronise and return the device error status code (PATH_OK or
+    PATH_ERR_TIMEOUT); clears the flag by default."""
+    return int(load_library().path_attn_device_status(1 if clear else 0))
+
+
+def path_attn_selftest_bounded_wait(limit_us=1000, stream=None):
+    _check(load_library().path_attn_selftest_bounded_wait(int(limit_us), _stream(stream)))

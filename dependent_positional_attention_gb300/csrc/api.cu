@@ -1,0 +1,267 @@
+// C ABI of libpath_attn: argument validation, workspace layout, dispatch.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/path_attn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace path {
+
+// The library's only device-resident state: the error flag set by kernels
+// whose bounded waits ran out.
+__device__ uint32_t g_error_flag;
+
+namespace {
+
+thread_local char g_msg[512];
+
+path_status_t fail(path_status_t s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+path_status_t ok() {
+    g_msg[0] = 0;
+    return PATH_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Per-device address of g_error_flag (looked up once per device).
+uint32_t *error_flag_ptr() {
+    static uint32_t *ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_flag) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<uint32_t *>(p);
+    }
+    return ptrs[dev];
+}
+
+struct PrefillPlan {
+    int BH, L, Lp, N, C, d;
+    bool bf16;
+    size_t esize;
+    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, total;
+};
+
+path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
+    if (!desc) return fail(PATH_ERR_INVALID_ARG, "desc is NULL");
+    if (desc->batch < 1 || desc->heads < 1 || desc->seq_len < 1 || desc->head_dim < 1)
+        return fail(PATH_ERR_INVALID_ARG, "batch, heads, seq_len, head_dim must be >= 1");
+    if (desc->dtype != PATH_F32 && desc->dtype != PATH_BF16)
+        return fail(PATH_ERR_INVALID_ARG, "dtype must be PATH_F32 or PATH_BF16");
+    if (!(desc->scale == desc->scale) || isinf(desc->scale))
+        return fail(PATH_ERR_INVALID_ARG, "scale must be finite");
+    const long long BH = (long long)desc->batch * desc->heads;
+    if (BH > 65535) return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
+    p->bf16 = desc->dtype == PATH_BF16;
+    p->d = desc->head_dim;
+    if (p->bf16) {
+        if (p->d != 128) return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 needs head_dim == 128");
+        if (desc->chunk != 0 && desc->chunk != 128)
+            return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 needs chunk 0 or 128");
+        p->C = 128;
+    } else {
+        if (p->d > 128 || p->d % 4)
+            return fail(PATH_ERR_UNSUPPORTED, "PATH_F32 needs head_dim <= 128, multiple of 4");
+        int C = desc->chunk ? desc->chunk : 64;
+        if (C != 16 && C != 32 && C != 64 && C != 128)
+            return fail(PATH_ERR_UNSUPPORTED, "PATH_F32 chunk must be 16, 32, 64 or 128");
+        p->C = C;
+    }
+    p->BH = (int)BH;
+    p->L = desc->seq_len;
+    p->N = (p->L + p->C - 1) / p->C;
+    if ((long long)p->N * p->C > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
+    p->Lp = p->N * p->C;
+    p->esize = p->bf16 ? 2 : 4;
+    const size_t rows = (size_t)p->BH * p->Lp;
+    const size_t cc = (size_t)p->BH * p->N * p->C * p->C;
+    size_t off = 0;
+    p->off_Qh = off; off = align_up(off + rows * p->d * p->esize, 256);
+    p->off_Kh = off; off = align_up(off + rows * p->d * p->esize, 256);
+    p->off_Wt = off; off = align_up(off + rows * p->d * p->esize, 256);
+    p->off_Sd = off; off = align_up(off + cc * 4, 256);
+    p->off_F = off; off = align_up(off + rows * 4, 256);
+    p->off_scratch = off; off = align_up(off + cc * 5 * 4, 256);
+    p->total = off;
+    return ok();
+}
+
+template <class T> T *at(void *base, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(base) + off);
+}
+
+path_status_t cuda_status(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(PATH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+}  // namespace
+}  // namespace path
+
+using namespace path;
+
+extern "C" {
+
+size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc) {
+    PrefillPlan p;
+    if (plan_prefill(desc, &p) != PATH_OK) return 0;
+    return p.total;
+}
+
+path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void *q,
+                                    const void *k, const void *v, const void *w,
+                                    const float *beta, const float *log_f, void *out,
+                                    float *lse, void *workspace, size_t workspace_bytes,
+                                    path_stream_t stream) {
+    PrefillPlan p;
+    path_status_t s = plan_prefill(desc, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {q, k, v, w, beta, out, workspace};
+    const char *names[] = {"q", "k", "v", "w", "beta", "out", "workspace"};
+    for (int i = 0; i < 7; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (log_f && !aligned16(log_f)) return fail(PATH_ERR_INVALID_ARG, "log_f is not 16-byte aligned");
+    if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+    if (workspace_bytes < p.total)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.total);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
+    if (log_f) {
+        s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
+        if (s != PATH_OK) return s;
+    }
+    PrepSimtArgs pa;
+    pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
+    pa.Qh = at<char>(workspace, p.off_Qh);
+    pa.Kh = at<char>(workspace, p.off_Kh);
+    pa.Wt = at<char>(workspace, p.off_Wt);
+    pa.Sd = at<float>(workspace, p.off_Sd);
+    pa.scratch = at<float>(workspace, p.off_scratch);
+    pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
+    pa.keys_only = 0;
+    s = cuda_status(launch_prep_simt(pa, p.bf16, p.bf16, st), "prep launch");
+    if (s != PATH_OK) return s;
+
+    if (p.bf16) return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 scan not built yet");
+    FlashSimtArgs fa;
+    fa.Qh = pa.Qh; fa.Kh = pa.Kh; fa.Wt = pa.Wt; fa.w = w; fa.v = v;
+    fa.Sd = pa.Sd; fa.F = F; fa.out = out; fa.lse = lse; fa.scale = desc->scale;
+    fa.BH = p.BH; fa.L = p.L; fa.Lp = p.Lp; fa.N = p.N; fa.C = p.C; fa.d = p.d;
+    return cuda_status(launch_flash_simt(fa, st), "scan launch");
+}
+
+size_t path_attn_decode_workspace_size(const path_decode_desc_t *desc) {
+    (void)desc;
+    return 0;
+}
+
+path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cache,
+                                    void *v_cache, int32_t cache_len, const void *q_t,
+                                    const void *k_t, const void *v_t, const void *w_t,
+                                    const float *beta_t, void *out, void *workspace,
+                                    size_t workspace_bytes, path_stream_t stream) {
+    (void)desc; (void)k_cache; (void)v_cache; (void)cache_len; (void)q_t; (void)k_t;
+    (void)v_t; (void)w_t; (void)beta_t; (void)out; (void)workspace; (void)workspace_bytes;
+    (void)stream;
+    return fail(PATH_ERR_UNSUPPORTED, "decode not built yet");
+}
+
+size_t path_attn_build_kcache_workspace_size(const path_prefill_desc_t *desc) {
+    (void)desc;
+    return 0;
+}
+
+path_status_t path_attn_build_kcache(const path_prefill_desc_t *desc, const void *k,
+                                     const void *w, const float *beta, void *k_cache,
+                                     int32_t cache_capacity, void *workspace,
+                                     size_t workspace_bytes, path_stream_t stream) {
+    (void)desc; (void)k; (void)w; (void)beta; (void)k_cache; (void)cache_capacity;
+    (void)workspace; (void)workspace_bytes; (void)stream;
+    return fail(PATH_ERR_UNSUPPORTED, "kcache build not built yet");
+}
+
+path_status_t path_attn_device_status(int32_t clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(PATH_ERR_CUDA, "synchronize: %s", cudaGetErrorString(e));
+    uint32_t *fp = error_flag_ptr();
+    if (!fp) return fail(PATH_ERR_CUDA, "error flag lookup failed");
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, fp, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(PATH_ERR_CUDA, "flag read: %s", cudaGetErrorString(e));
+    if (clear) {
+        uint32_t z = 0;
+        e = cudaMemcpy(fp, &z, sizeof z, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(PATH_ERR_CUDA, "flag clear: %s", cudaGetErrorString(e));
+    }
+    if (v & kErrTimeout) return fail(PATH_ERR_TIMEOUT, "a device-side wait ran out");
+    return ok();
+}
+
+path_status_t path_attn_selftest_bounded_wait(uint32_t limit_us, path_stream_t stream) {
+    if (limit_us == 0 || limit_us > 10000000u)
+        return fail(PATH_ERR_INVALID_ARG, "limit_us must be in 1..10000000");
+    uint32_t *fp = error_flag_ptr();
+    if (!fp) return fail(PATH_ERR_CUDA, "error flag lookup failed");
+    return cuda_status(launch_selftest_wait(fp, (uint64_t)limit_us * 1000ull,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                       "selftest launch");
+}
+
+const char *path_attn_status_string(path_status_t status) {
+    switch (status) {
+    case PATH_OK: return "PATH_OK";
+    case PATH_ERR_INVALID_ARG: return "PATH_ERR_INVALID_ARG";
+    case PATH_ERR_UNSUPPORTED: return "PATH_ERR_UNSUPPORTED";
+    case PATH_ERR_CUDA: return "PATH_ERR_CUDA";
+    case PATH_ERR_TIMEOUT: return "PATH_ERR_TIMEOUT";
+    }
+    return "PATH_ERR_UNKNOWN";
+}
+
+const char *path_attn_last_error(void) { return g_msg; }
+
+int32_t path_attn_version(void) { return 100; }
+
+}  // extern "C"
+
+// ------------------------------------------------------------ selftest kernel
+
+namespace path {
+namespace {
+// One thread waits on an mbarrier that expects an arrival nobody makes.
+__global__ void selftest_wait_kernel(uint32_t *err_flag, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        abort_word = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err_flag, &abort_word, limit_ns);
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(uint32_t *err_flag, uint64_t limit_ns, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(err_flag, limit_ns);
+    return cudaGetLastError();
+}
+}  // namespace path

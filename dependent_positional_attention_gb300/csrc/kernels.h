@@ -1,0 +1,43 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace path {
+
+// Prefill workspace, per (batch*head) and padded length Lp = N * C:
+//   Qh, Kh, Wt : [BH][Lp][d]    element type of the call
+//   Sd         : [BH][N][C][C]  fp32 within-chunk logits (unscaled)
+//   F          : [BH][Lp]       fp32 FoX prefix sums (PaTH-FoX calls only)
+//   scratch    : [BH][N][5][C][C] fp32 (SIMT prep only)
+struct PrepSimtArgs {
+    const void *q, *k, *w;
+    const float *beta;
+    void *Qh, *Kh, *Wt;
+    float *Sd, *scratch;
+    int BH, L, Lp, N, C, d;
+    int keys_only;  // 1: only Kh and Wt (q, Qh, Sd unused)
+};
+
+struct FlashSimtArgs {
+    const void *Qh, *Kh, *Wt, *w, *v;
+    const float *Sd, *F;
+    void *out;
+    float *lse;
+    float scale;
+    int BH, L, Lp, N, C, d;
+};
+
+size_t prep_simt_smem(int C);
+size_t flash_simt_smem(int C, int d);
+cudaError_t launch_prep_simt(const PrepSimtArgs &a, bool bf16_in, bool bf16_out,
+                             cudaStream_t st);
+cudaError_t launch_fox_prefix(const float *log_f, float *F, int L, int Lp, int BH,
+                              cudaStream_t st);
+cudaError_t launch_flash_simt(const FlashSimtArgs &a, cudaStream_t st);
+
+cudaError_t launch_selftest_wait(uint32_t *err_flag, uint64_t limit_ns, cudaStream_t st);
+
+}  // namespace path

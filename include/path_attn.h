@@ -1,0 +1,178 @@
+/*
+ * libpath_attn — PaTH attention on one NVIDIA GB300 (sm_103a).
+ *
+ * PaTH attention (PaTH Attention summary, gist.science/ko/paper/2505.16381,
+ * section "2. 방법론 / 핵심 메커니즘", attention-logit equation) is causal
+ * softmax attention whose logit between query i and key j <= i is
+ *
+ *     scale * k_j^T (H_{j+1} H_{j+2} ... H_i) q_i,    H_s = I - beta_s w_s w_s^T,
+ *
+ * with one unit direction w_s and one coefficient beta_s in [0, 2] per token
+ * and head.  The product is ordered so that H_i acts on q_i first; for
+ * j == i it is the identity.  PaTH-FoX (section "확장: PaTH-FoX") adds the
+ * forgetting-transformer bias sum_{s=j+1}^{i} log f_s, unscaled.
+ *
+ * Conventions shared by every call:
+ *   - Tensors are dense, row-major, on the current CUDA device.  Activations
+ *     q, k, v, w, out are [batch][heads][seq_len][head_dim]; beta, log_f and
+ *     lse are float32 [batch][heads][seq_len].  The element type of q, k, v,
+ *     w, out and the caches is the descriptor's dtype.
+ *   - Every device pointer must be 16-byte aligned.
+ *   - The caller owns every buffer, the workspace included.  The library
+ *     allocates no memory and keeps no state between calls (besides a
+ *     one-word device error flag, see path_attn_device_status).
+ *   - Calls are asynchronous on `stream`.  Argument errors are returned
+ *     before anything is launched.  A launch failure returns PATH_ERR_CUDA.
+ *   - Preconditions the library does not check or enforce: w rows have unit
+ *     norm and beta lies in [0, 2]; nothing is normalised or clipped.
+ *   - Calls that overlap in time on the GPU must not share a workspace.
+ */
+#ifndef PATH_ATTN_H
+#define PATH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t.  NULL selects the legacy default stream. */
+typedef struct CUstream_st *path_stream_t;
+
+typedef enum {
+    PATH_OK = 0,
+    PATH_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or workspace   */
+    PATH_ERR_UNSUPPORTED = 2, /* valid but not implemented (dtype, head_dim) */
+    PATH_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed        */
+    PATH_ERR_TIMEOUT = 4      /* a device-side wait hit its iteration limit  */
+} path_status_t;
+
+typedef enum { PATH_F32 = 0, PATH_BF16 = 1 } path_dtype_t;
+
+/* ------------------------------------------------------------------ prefill */
+
+typedef struct {
+    int32_t batch, heads, seq_len, head_dim;
+    int32_t dtype;  /* path_dtype_t */
+    float scale;    /* multiplies k^T(...)q; usually 1/sqrt(head_dim) */
+    int32_t chunk;  /* 0 = default. PATH_F32: 16, 32, 64 or 128 (default 64).
+                       PATH_BF16: 128 only. */
+} path_prefill_desc_t;
+
+/*
+ * Bytes of device workspace path_attn_prefill_fwd needs for `desc` (0 if the
+ * descriptor is invalid).  The workspace holds, per head, the
+ * boundary-adjusted query and key rows, the chunk products in compact form
+ * and the within-chunk logits (section "3. 효율적인 학습 및 추론",
+ * FlashAttention-style algorithm); its contents are unspecified between
+ * calls.
+ */
+size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc);
+
+/*
+ * Causal PaTH (or PaTH-FoX) attention forward.
+ *   q, k, v, w : [B][H][L][d], desc->dtype.
+ *   beta       : float32 [B][H][L].
+ *   log_f      : float32 [B][H][L] log forget gate (PaTH-FoX), or NULL.
+ *   out        : [B][H][L][d], desc->dtype, written.
+ *   lse        : float32 [B][H][L], natural log of the sum of exp(logit) over
+ *                the causal row (logits include scale and FoX bias), or NULL.
+ *   workspace  : device buffer of at least
+ *                path_attn_prefill_workspace_size(desc) bytes.
+ * Supported: PATH_F32 with head_dim <= 128 (multiple of 4); PATH_BF16 with
+ * head_dim == 128.  seq_len may be any value >= 1 (the last chunk may be
+ * partial).  Method: section 3 of the PaTH summary — a per-chunk UT
+ * transform builds boundary-adjusted rows and the compact chunk product,
+ * then a blockwise scan visits key chunks right to left, carrying the
+ * accumulated product on the query side, with an online softmax.
+ */
+path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void *q,
+                                    const void *k, const void *v, const void *w,
+                                    const float *beta, const float *log_f, void *out,
+                                    float *lse, void *workspace, size_t workspace_bytes,
+                                    path_stream_t stream);
+
+/* ------------------------------------------------------------------- decode */
+
+typedef struct {
+    int32_t batch, heads, head_dim;
+    int32_t cache_capacity; /* slots per (batch, head) in the caches */
+    int32_t dtype;          /* path_dtype_t; PATH_BF16 only */
+    float scale;
+} path_decode_desc_t;
+
+/* Bytes of device workspace path_attn_decode_step needs for any cache_len
+ * up to the capacity (split-KV partial results); 0 if desc is invalid. */
+size_t path_attn_decode_workspace_size(const path_decode_desc_t *desc);
+
+/*
+ * One PaTH decode step (section "3. 효율적인 학습 및 추론", inference
+ * bullet): every cached key j < cache_len is updated in place with the new
+ * token's transition, k_j <- k_j - beta_t w_t (w_t^T k_j), so the cache never
+ * stores w; then (k_t, v_t) is written to slot cache_len untransformed and
+ *     out = softmax_j(scale * q_t . k_j) v_j   over j <= cache_len.
+ *   k_cache, v_cache : [B][H][cache_capacity][d], desc->dtype; k_cache
+ *                      slots < cache_len are rewritten, slot cache_len of
+ *                      both caches receives k_t / v_t.
+ *   q_t, k_t, v_t, w_t : [B][H][d]; beta_t : float32 [B][H]; out : [B][H][d].
+ *   cache_len        : tokens already cached, 0 <= cache_len < capacity.
+ * The caller advances cache_len by one after the call.  Keys are re-rounded
+ * to the cache dtype after every update.
+ */
+path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cache,
+                                    void *v_cache, int32_t cache_len, const void *q_t,
+                                    const void *k_t, const void *v_t, const void *w_t,
+                                    const float *beta_t, void *out, void *workspace,
+                                    size_t workspace_bytes, path_stream_t stream);
+
+/*
+ * Key cache after a prefill of seq_len tokens, as the decode step expects it:
+ *     k_cache[j] = H_{L-1} ... H_{j+1} k_j    (j < L = desc->seq_len),
+ * i.e. every key transformed by all later transitions (inference bullet of
+ * section 3).  The PaTH pages only describe the in-place update one step at
+ * a time; this call produces the same state in O(L d^2) per head by a
+ * right-to-left sweep over chunk products.  k, w: [B][H][L][d]; beta:
+ * float32 [B][H][L]; k_cache: [B][H][cache_capacity][d] (slots < L written).
+ * desc->dtype must equal the cache dtype (PATH_BF16).  The workspace must
+ * hold path_attn_build_kcache_workspace_size(desc) bytes.
+ */
+size_t path_attn_build_kcache_workspace_size(const path_prefill_desc_t *desc);
+path_status_t path_attn_build_kcache(const path_prefill_desc_t *desc, const void *k,
+                                     const void *w, const float *beta, void *k_cache,
+                                     int32_t cache_capacity, void *workspace,
+                                     size_t workspace_bytes, path_stream_t stream);
+
+/* -------------------------------------------------------------- diagnostics */
+
+/*
+ * Synchronises the current device, then reports the device error flag that
+ * kernels set when a bounded wait (mbarrier or flag) runs out: PATH_OK,
+ * PATH_ERR_TIMEOUT, or PATH_ERR_CUDA if the synchronisation itself failed.
+ * clear != 0 resets the flag.
+ */
+path_status_t path_attn_device_status(int32_t clear);
+
+/*
+ * Launches one tiny kernel whose mbarrier wait can never complete, bounded by
+ * limit_us microseconds of device time; the kernel then sets the device
+ * error flag and exits cleanly.  Exists so tests can check the bounded-wait
+ * path without hanging a GPU.
+ */
+path_status_t path_attn_selftest_bounded_wait(uint32_t limit_us, path_stream_t stream);
+
+/* Static text for a status code. */
+const char *path_attn_status_string(path_status_t status);
+
+/* Detail message of the last failing call on this host thread ("" if none). */
+const char *path_attn_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t path_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PATH_ATTN_H */

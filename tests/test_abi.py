@@ -1,0 +1,87 @@
+"""C-ABI checks that need no GPU: the library builds, loads on a host
+without a driver, exports every entry point include/path_attn.h declares,
+and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dependent_positional_attention_gb300 as pa
+from dependent_positional_attention_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return pa.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "path_attn.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(path_attn_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), "missing export %s" % n
+    assert sorted(pa.EXPORTED_SYMBOLS) == names
+
+
+def test_status_strings(lib):
+    assert lib.path_attn_status_string(0) == b"PATH_OK"
+    assert lib.path_attn_status_string(4) == b"PATH_ERR_TIMEOUT"
+    assert lib.path_attn_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)       # 8-byte aligned only
+
+
+def prefill(lib, desc, ws_bytes=1 << 40, ptrs=None, log_f=None):
+    p = ptrs or [FAKE] * 5
+    return lib.path_attn_prefill_fwd(ctypes.byref(desc), p[0], p[1], p[2], p[3], p[4], log_f,
+                                     FAKE, None, FAKE, ws_bytes, None)
+
+
+def test_prefill_rejects_bad_descriptors(lib):
+    D = pa.PrefillDesc
+    assert prefill(lib, D(0, 1, 16, 64, 0, 0.1, 0)) == pa.PATH_ERR_INVALID_ARG
+    assert prefill(lib, D(1, 1, 0, 64, 0, 0.1, 0)) == pa.PATH_ERR_INVALID_ARG
+    assert prefill(lib, D(1, 1, 16, 64, 7, 0.1, 0)) == pa.PATH_ERR_INVALID_ARG
+    assert prefill(lib, D(1, 1, 16, 64, 0, float("nan"), 0)) == pa.PATH_ERR_INVALID_ARG
+    assert prefill(lib, D(1, 1, 16, 64, 1, 0.1, 0)) == pa.PATH_ERR_UNSUPPORTED  # bf16 d=64
+    assert prefill(lib, D(1, 1, 16, 130, 0, 0.1, 0)) == pa.PATH_ERR_UNSUPPORTED
+    assert prefill(lib, D(1, 1, 16, 64, 0, 0.1, 48)) == pa.PATH_ERR_UNSUPPORTED
+    assert prefill(lib, D(1, 1, 16, 128, 1, 0.1, 64)) == pa.PATH_ERR_UNSUPPORTED
+    assert lib.path_attn_prefill_workspace_size(ctypes.byref(D(0, 1, 16, 64, 0, 0.1, 0))) == 0
+    assert b"batch" in lib.path_attn_last_error()
+
+
+def test_prefill_rejects_bad_pointers_and_workspace(lib):
+    D = pa.PrefillDesc
+    desc = D(2, 3, 100, 64, 0, 0.125, 32)
+    need = lib.path_attn_prefill_workspace_size(ctypes.byref(desc))
+    assert need > 0
+    assert prefill(lib, desc, ws_bytes=need - 1) == pa.PATH_ERR_INVALID_ARG
+    assert b"workspace" in lib.path_attn_last_error()
+    for i in range(5):
+        p = [FAKE] * 5
+        p[i] = None
+        assert prefill(lib, desc, ptrs=p) == pa.PATH_ERR_INVALID_ARG
+        p[i] = ODD
+        assert prefill(lib, desc, ptrs=p) == pa.PATH_ERR_INVALID_ARG
+    assert prefill(lib, desc, log_f=ODD) == pa.PATH_ERR_INVALID_ARG
+
+
+def test_workspace_grows_with_problem(lib):
+    D = pa.PrefillDesc
+    a = lib.path_attn_prefill_workspace_size(ctypes.byref(D(1, 1, 128, 128, 1, 0.1, 0)))
+    b = lib.path_attn_prefill_workspace_size(ctypes.byref(D(2, 1, 128, 128, 1, 0.1, 0)))
+    c = lib.path_attn_prefill_workspace_size(ctypes.byref(D(1, 1, 129, 128, 1, 0.1, 0)))
+    assert 0 < a < b and a < c
