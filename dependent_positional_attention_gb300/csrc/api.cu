@@ -99,6 +99,65 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     return ok();
 }
 
+struct DecodePlan {
+    int BH, keys_per_split, max_splits;
+    size_t ws_bytes;
+};
+
+path_status_t plan_decode(const path_decode_desc_t *desc, DecodePlan *p) {
+    if (!desc) return fail(PATH_ERR_INVALID_ARG, "desc is NULL");
+    if (desc->batch < 1 || desc->heads < 1 || desc->head_dim < 1 || desc->cache_capacity < 1)
+        return fail(PATH_ERR_INVALID_ARG, "batch, heads, head_dim, cache_capacity must be >= 1");
+    if (desc->dtype != PATH_F32 && desc->dtype != PATH_BF16)
+        return fail(PATH_ERR_INVALID_ARG, "dtype must be PATH_F32 or PATH_BF16");
+    if (!(desc->scale == desc->scale) || isinf(desc->scale))
+        return fail(PATH_ERR_INVALID_ARG, "scale must be finite");
+    if (desc->dtype != PATH_BF16) return fail(PATH_ERR_UNSUPPORTED, "decode needs PATH_BF16");
+    if (desc->head_dim != 64 && desc->head_dim != 128)
+        return fail(PATH_ERR_UNSUPPORTED, "decode needs head_dim 64 or 128");
+    const long long BH = (long long)desc->batch * desc->heads;
+    if (BH > 65535) return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
+    p->BH = (int)BH;
+    p->keys_per_split = decode_keys_per_split();
+    p->max_splits = (desc->cache_capacity + p->keys_per_split - 1) / p->keys_per_split;
+    p->ws_bytes = align_up((size_t)p->BH * p->max_splits * (desc->head_dim + 2) * 4, 256);
+    return ok();
+}
+
+struct KcachePlan {
+    int BH, HB, L, Lp, N, C, d, G, S;
+    size_t off_Kh, off_Wt, off_scratch, off_Pi, off_Mout, total;
+};
+
+path_status_t plan_kcache(const path_prefill_desc_t *desc, KcachePlan *p) {
+    if (!desc) return fail(PATH_ERR_INVALID_ARG, "desc is NULL");
+    if (desc->batch < 1 || desc->heads < 1 || desc->seq_len < 1 || desc->head_dim < 1)
+        return fail(PATH_ERR_INVALID_ARG, "batch, heads, seq_len, head_dim must be >= 1");
+    if (desc->dtype != PATH_BF16) return fail(PATH_ERR_UNSUPPORTED, "kcache build needs PATH_BF16");
+    if (desc->head_dim > 128 || desc->head_dim % 8)
+        return fail(PATH_ERR_UNSUPPORTED, "kcache build needs head_dim <= 128, multiple of 8");
+    const long long BH = (long long)desc->batch * desc->heads;
+    if (BH > 65535) return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
+    p->BH = (int)BH;
+    p->HB = p->BH < 16 ? p->BH : 16;
+    p->d = desc->head_dim;
+    p->C = 128;
+    p->G = 16;
+    p->L = desc->seq_len;
+    p->N = (p->L + p->C - 1) / p->C;
+    p->Lp = p->N * p->C;
+    p->S = (p->N + p->G - 1) / p->G;
+    const size_t rows = (size_t)p->HB * p->Lp;
+    size_t off = 0;
+    p->off_Kh = off; off = align_up(off + rows * p->d * 4, 256);
+    p->off_Wt = off; off = align_up(off + rows * p->d * 4, 256);
+    p->off_scratch = off; off = align_up(off + (size_t)p->HB * p->N * 5 * p->C * p->C * 4, 256);
+    p->off_Pi = off; off = align_up(off + (size_t)p->HB * p->S * p->d * p->d * 4, 256);
+    p->off_Mout = off; off = align_up(off + (size_t)p->HB * p->S * p->d * p->d * 4, 256);
+    p->total = off;
+    return ok();
+}
+
 template <class T> T *at(void *base, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(base) + off);
 }
@@ -169,8 +228,9 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
 }
 
 size_t path_attn_decode_workspace_size(const path_decode_desc_t *desc) {
-    (void)desc;
-    return 0;
+    DecodePlan p;
+    if (plan_decode(desc, &p) != PATH_OK) return 0;
+    return p.ws_bytes;
 }
 
 path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cache,
@@ -178,24 +238,91 @@ path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cach
                                     const void *k_t, const void *v_t, const void *w_t,
                                     const float *beta_t, void *out, void *workspace,
                                     size_t workspace_bytes, path_stream_t stream) {
-    (void)desc; (void)k_cache; (void)v_cache; (void)cache_len; (void)q_t; (void)k_t;
-    (void)v_t; (void)w_t; (void)beta_t; (void)out; (void)workspace; (void)workspace_bytes;
-    (void)stream;
-    return fail(PATH_ERR_UNSUPPORTED, "decode not built yet");
+    DecodePlan p;
+    path_status_t s = plan_decode(desc, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {k_cache, v_cache, q_t, k_t, v_t, w_t, beta_t, out, workspace};
+    const char *names[] = {"k_cache", "v_cache", "q_t", "k_t", "v_t", "w_t", "beta_t", "out",
+                           "workspace"};
+    for (int i = 0; i < 9; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (cache_len < 0 || cache_len >= desc->cache_capacity)
+        return fail(PATH_ERR_INVALID_ARG, "cache_len %d outside [0, capacity %d)", cache_len,
+                    desc->cache_capacity);
+    if (workspace_bytes < p.ws_bytes)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.ws_bytes);
+    DecodeArgs a;
+    a.k_cache = k_cache; a.v_cache = v_cache; a.q_t = q_t; a.k_t = k_t; a.v_t = v_t;
+    a.w_t = w_t; a.beta_t = beta_t; a.out = out;
+    a.partials = static_cast<float *>(workspace);
+    a.scale = desc->scale;
+    a.BH = p.BH; a.d = desc->head_dim; a.cap = desc->cache_capacity; a.cache_len = cache_len;
+    a.keys_per_split = p.keys_per_split; a.max_splits = p.max_splits;
+    return cuda_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)), "decode launch");
 }
 
 size_t path_attn_build_kcache_workspace_size(const path_prefill_desc_t *desc) {
-    (void)desc;
-    return 0;
+    KcachePlan p;
+    if (plan_kcache(desc, &p) != PATH_OK) return 0;
+    return p.total;
 }
 
 path_status_t path_attn_build_kcache(const path_prefill_desc_t *desc, const void *k,
                                      const void *w, const float *beta, void *k_cache,
                                      int32_t cache_capacity, void *workspace,
                                      size_t workspace_bytes, path_stream_t stream) {
-    (void)desc; (void)k; (void)w; (void)beta; (void)k_cache; (void)cache_capacity;
-    (void)workspace; (void)workspace_bytes; (void)stream;
-    return fail(PATH_ERR_UNSUPPORTED, "kcache build not built yet");
+    KcachePlan p;
+    path_status_t s = plan_kcache(desc, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {k, w, beta, k_cache, workspace};
+    const char *names[] = {"k", "w", "beta", "k_cache", "workspace"};
+    for (int i = 0; i < 5; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (cache_capacity < desc->seq_len)
+        return fail(PATH_ERR_INVALID_ARG, "cache_capacity %d < seq_len %d", cache_capacity,
+                    desc->seq_len);
+    if (workspace_bytes < p.total)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.total);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int d = p.d;
+    for (int h0 = 0; h0 < p.BH; h0 += p.HB) {
+        const int hb = (p.BH - h0 < p.HB) ? p.BH - h0 : p.HB;
+        const size_t in_off = (size_t)h0 * p.L * d;
+        PrepSimtArgs pa;
+        pa.q = static_cast<const __nv_bfloat16 *>(k) + in_off;
+        pa.k = static_cast<const __nv_bfloat16 *>(k) + in_off;
+        pa.w = static_cast<const __nv_bfloat16 *>(w) + in_off;
+        pa.beta = beta + (size_t)h0 * p.L;
+        pa.Qh = at<float>(workspace, p.off_Kh);  // unused in keys-only mode
+        pa.Kh = at<float>(workspace, p.off_Kh);
+        pa.Wt = at<float>(workspace, p.off_Wt);
+        pa.Sd = at<float>(workspace, p.off_scratch);  // unused in keys-only mode
+        pa.scratch = at<float>(workspace, p.off_scratch);
+        pa.BH = hb; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = d;
+        pa.keys_only = 1;
+        s = cuda_status(launch_prep_simt(pa, true, false, st), "kcache prep launch");
+        if (s != PATH_OK) return s;
+        KcacheArgs ka;
+        ka.w = static_cast<const __nv_bfloat16 *>(w) + in_off;
+        ka.Kh = at<float>(workspace, p.off_Kh);
+        ka.Wt = at<float>(workspace, p.off_Wt);
+        ka.Pi = at<float>(workspace, p.off_Pi);
+        ka.Mout = at<float>(workspace, p.off_Mout);
+        ka.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+        ka.h0 = h0; ka.HB = hb; ka.cap = cache_capacity; ka.L = p.L; ka.Lp = p.Lp;
+        ka.N = p.N; ka.C = p.C; ka.d = d; ka.G = p.G; ka.S = p.S;
+        s = cuda_status(launch_kcache_sweep(ka, st), "kcache sweep launch");
+        if (s != PATH_OK) return s;
+    }
+    return ok();
 }
 
 path_status_t path_attn_device_status(int32_t clear) {

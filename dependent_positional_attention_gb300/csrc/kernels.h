@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -37,6 +38,31 @@ cudaError_t launch_prep_simt(const PrepSimtArgs &a, bool bf16_in, bool bf16_out,
 cudaError_t launch_fox_prefix(const float *log_f, float *F, int L, int Lp, int BH,
                               cudaStream_t st);
 cudaError_t launch_flash_simt(const FlashSimtArgs &a, cudaStream_t st);
+
+struct DecodeArgs {
+    void *k_cache, *v_cache;
+    const void *q_t, *k_t, *v_t, *w_t;
+    const float *beta_t;
+    void *out;
+    float *partials;  // [BH][max_splits][d + 2]: m (log2 units), l, o[d]
+    float scale;
+    int BH, d, cap, cache_len, keys_per_split, max_splits;
+};
+
+int decode_keys_per_split();
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+
+// Key-cache build for a group of HB heads starting at global head h0.
+struct KcacheArgs {
+    const __nv_bfloat16 *w;  // raw w of the group, [HB][L][d]
+    const float *Kh, *Wt;    // fp32 boundary-adjusted keys and T W, [HB][Lp][d]
+    float *Pi, *Mout;        // [HB][S][d][d]
+    __nv_bfloat16 *k_cache;  // full cache, [BH][cap][d]
+    int h0, HB, cap, L, Lp, N, C, d, G, S;
+};
+
+size_t kcache_smem(int d, int C);
+cudaError_t launch_kcache_sweep(const KcacheArgs &a, cudaStream_t st);
 
 cudaError_t launch_selftest_wait(uint32_t *err_flag, uint64_t limit_ns, cudaStream_t st);
 
