@@ -7,6 +7,7 @@
 #include "../../include/path_attn.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace path {
 
@@ -46,6 +47,18 @@ uint32_t *error_flag_ptr() {
         ptrs[dev] = static_cast<uint32_t *>(p);
     }
     return ptrs[dev];
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cache[dev] = n;
+    }
+    return cache[dev];
 }
 
 struct PrefillPlan {
@@ -219,7 +232,23 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
     s = cuda_status(launch_prep_simt(pa, p.bf16, p.bf16, st), "prep launch");
     if (s != PATH_OK) return s;
 
-    if (p.bf16) return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 scan not built yet");
+    if (p.bf16) {
+        FlashTcMaps maps;
+        const bool enc =
+            encode_tmap_bf16_3d(&maps.qh, pa.Qh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.kh, pa.Kh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.wt, pa.Wt, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
+        if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+        FlashTcArgs ta;
+        ta.Sd = pa.Sd; ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
+        ta.scale = desc->scale; ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        ta.err = error_flag_ptr();
+        const int sms = num_sms();
+        if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+        return cuda_status(launch_flash_tc(maps, ta, sms, st), "tensor-core scan launch");
+    }
     FlashSimtArgs fa;
     fa.Qh = pa.Qh; fa.Kh = pa.Kh; fa.Wt = pa.Wt; fa.w = w; fa.v = v;
     fa.Sd = pa.Sd; fa.F = F; fa.out = out; fa.lse = lse; fa.scale = desc->scale;

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -63,6 +64,25 @@ struct KcacheArgs {
 
 size_t kcache_smem(int d, int C);
 cudaError_t launch_kcache_sweep(const KcacheArgs &a, cudaStream_t st);
+
+// Tensor-core scan (bf16, head_dim 128, chunk 128).  Maps: 3-D bf16 tensors
+// [BH][rows][128] in 64 x 128 boxes with 128-byte swizzle.
+struct __align__(64) FlashTcMaps {
+    CUtensorMap qh, kh, wt;  // workspace, rows = Lp
+    CUtensorMap w, v;        // inputs, rows = L
+};
+
+struct FlashTcArgs {
+    const float *Sd, *F;
+    __nv_bfloat16 *out;
+    float *lse;
+    float scale;
+    int BH, L, Lp, N;
+    uint32_t *err;
+};
+
+cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
+                            cudaStream_t st);
 
 cudaError_t launch_selftest_wait(uint32_t *err_flag, uint64_t limit_ns, cudaStream_t st);
 

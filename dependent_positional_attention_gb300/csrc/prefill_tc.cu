@@ -1,0 +1,561 @@
+// PaTH prefill scan on 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Blockwise algorithm of the PaTH Attention summary (section "3. 효율적인
+// 학습 및 추론", FlashAttention-style algorithm): per query chunk b (128 rows)
+// the key chunks are visited right to left.  The diagonal chunk uses the
+// within-chunk logits Sd from the prep kernel; for every earlier chunk c the
+// carried query rows Qt (which start as the boundary-adjusted rows Qh_b) give
+//     S_c = Qt Kh_c^T            (logits against boundary-adjusted keys)
+//     X_c = Qt W_c^T,  Qt <- Qt - X_c Wt_c     (apply the chunk product)
+//     O  += softmax-weights(S_c) V_c           (online softmax)
+// All four contractions are 128 x 128 x 128 bf16 MMAs with fp32 accumulation
+// in tensor memory.  Qt keeps an fp32 master copy in TMEM (the accumulator of
+// the update MMA); only its bf16 shadow in shared memory feeds the next MMAs.
+//
+// One CTA per SM (persistent), tiles ordered by decreasing work.  Warp roles:
+//   warp 0      TMA producer: Qh_b, then a 4-slot ring of W_c, Kh_c, Wt_c, V
+//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warps 2-5   carried-query warpgroup: X -> -X bf16 (A operand of the
+//               update), Qt fp32 -> bf16 shadow, Qt initialisation
+//   warps 6-9   softmax warpgroup: logits, online softmax with lazy rescale
+//               of O, P -> bf16, epilogue (out, lse)
+// MMA issue order per step c: X_c, S_c, update_c, PV_{c+1}; the PV of a chunk
+// runs one step late so the softmax has a full step of slack.
+// TMEM columns: [0,128) Qt fp32, [128,256) X, [256,384) S, [384,512) O.
+// Every wait is bounded; on timeout the kernel sets the device error flag,
+// drains its outstanding copies and MMAs, frees TMEM and exits.
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace path {
+namespace {
+
+constexpr int kD = 128, kC = 128;
+constexpr int kSlots = 4;
+constexpr int kTileBytes = kC * kD * 2;  // 32 KB bf16 tile
+constexpr int kThreadsTC = 320;
+constexpr uint32_t kColQ = 0, kColX = 128, kColS = 256, kColO = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// dynamic shared memory layout (offsets from a 1024-aligned base)
+constexpr int kOffQb = 0;
+constexpr int kOffXb = kOffQb + kTileBytes;
+constexpr int kOffPb = kOffXb + kTileBytes;
+constexpr int kOffRing = kOffPb + kTileBytes;
+constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+
+struct Bars {
+    uint64_t full[kSlots], empty[kSlots];
+    uint64_t qb_tma_full, qb_empty, x_full, xb_full, q_done, qb_conv_full;
+    uint64_t s_full, s_empty, p_full, o_done, drain;
+    uint32_t tmem_base;
+    int abort_word;
+    float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
+};
+// barriers/misc after the ring, plus slack to align the dynamic base to 1024
+constexpr int kSmemBytes = kOffBar + (int)((sizeof(Bars) + 127) / 128 * 128) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier over a warpgroup that also ANDs `ok` across its threads, so that a
+// wait that gave up in one thread makes the whole group leave together.
+__device__ __forceinline__ bool group_all(int id, int n, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Writes 32 fp32 values (columns 32*cc .. 32*cc+31 of row r), optionally
+// negated, as bf16 into a swizzled 128-column operand tile.
+__device__ __forceinline__ void store_row_chunk_bf16(uint32_t tile, int r, int cc,
+                                                     const uint32_t (&v)[32], float sign) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int j = cc * 4 + q;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(sign * __uint_as_float(v[q * 8 + 2 * e]),
+                             sign * __uint_as_float(v[q * 8 + 2 * e + 1]));
+        st_shared_v4(tile + tc::swz_off(r, j, kC), w[0], w[1], w[2], w[3]);
+    }
+}
+
+struct Tile {
+    int b, bh;
+};
+
+__device__ __forceinline__ Tile tile_of(int t, int BH, int N) {
+    Tile x;
+    x.b = N - 1 - t / BH;
+    x.bh = t % BH;
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    flash_tc_kernel(const __grid_constant__ FlashTcMaps maps, FlashTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBar);
+    const uint32_t sQb = smem_u32(smem + kOffQb);
+    const uint32_t sXb = smem_u32(smem + kOffXb);
+    const uint32_t sPb = smem_u32(smem + kOffPb);
+    const uint32_t sRing = smem_u32(smem + kOffRing);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = a.N * a.BH;
+    volatile int *abort_word = &bars.abort_word;
+    const uint64_t lim = kWaitLimitNs;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+        }
+        mbar_init(&bars.qb_tma_full, 1);
+        mbar_init(&bars.qb_empty, 2);  // MMA commit + carried-query group
+        mbar_init(&bars.x_full, 1);
+        mbar_init(&bars.xb_full, 1);
+        mbar_init(&bars.q_done, 1);
+        mbar_init(&bars.qb_conv_full, 1);
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.s_empty, 1);
+        mbar_init(&bars.p_full, 1);
+        mbar_init(&bars.o_done, 1);
+        mbar_init(&bars.drain, 1);
+        bars.abort_word = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&bars.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&maps.qh);
+            tc::prefetch_tmap(&maps.kh);
+            tc::prefetch_tmap(&maps.wt);
+            tc::prefetch_tmap(&maps.w);
+            tc::prefetch_tmap(&maps.v);
+            int slot = 0;
+            uint32_t ph = 0, qe_ph = 0;
+            int last_par[kSlots] = {-1, -1, -1, -1};
+            int q_last_par = -1;
+            uint32_t q_loads = 0;
+            bool ok = true;
+            auto load = [&](const CUtensorMap *m, int y, int z) -> bool {
+                if (!mbar_wait(&bars.empty[slot], ph ^ 1, a.err, abort_word, lim)) return false;
+                uint8_t *dst = smem + kOffRing + slot * kTileBytes;
+                mbar_arrive_expect_tx(&bars.full[slot], kTileBytes);
+                tc::tma_load_3d(dst, m, 0, y, z, &bars.full[slot]);
+                tc::tma_load_3d(dst + kTileBytes / 2, m, 64, y, z, &bars.full[slot]);
+                last_par[slot] = (int)ph;
+                if (++slot == kSlots) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+                return true;
+            };
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+                const Tile tl = tile_of(t, a.BH, a.N);
+                const int b = tl.b, bh = tl.bh;
+                if (b >= 1) {
+                    ok = mbar_wait(&bars.qb_empty, qe_ph ^ 1, a.err, abort_word, lim);
+                    qe_ph ^= 1;
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&bars.qb_tma_full, kTileBytes);
+                    tc::tma_load_3d(smem + kOffQb, &maps.qh, 0, b * kC, bh, &bars.qb_tma_full);
+                    tc::tma_load_3d(smem + kOffQb + kTileBytes / 2, &maps.qh, 64, b * kC, bh,
+                                    &bars.qb_tma_full);
+                    q_last_par = (int)(q_loads++ & 1);
+                }
+                for (int c = b - 1; c >= 0 && ok; --c) {
+                    if (c >= 1) ok = ok && load(&maps.w, c * kC, bh);
+                    ok = ok && load(&maps.kh, c * kC, bh);
+                    if (c >= 1) ok = ok && load(&maps.wt, c * kC, bh);
+                    ok = ok && load(&maps.v, (c + 1) * kC, bh);
+                }
+                ok = ok && load(&maps.v, 0, bh);
+            }
+            if (*abort_word) {
+                // let every copy this thread issued land before the CTA exits
+                for (int s = 0; s < kSlots; ++s)
+                    if (last_par[s] >= 0) mbar_wait(&bars.full[s], last_par[s], a.err, nullptr, lim);
+                if (q_last_par >= 0) mbar_wait(&bars.qb_tma_full, q_last_par, a.err, nullptr, lim);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t ph = 0, qt_ph = 0, qc_ph = 0, xb_ph = 0, se_ph = 0, pf_ph = 0;
+            bool ok = true;
+            auto take = [&](uint32_t &addr) -> bool {
+                if (!mbar_wait(&bars.full[slot], ph, a.err, abort_word, lim)) return false;
+                addr = sRing + slot * kTileBytes;
+                return true;
+            };
+            auto release = [&]() {
+                tc::mma_commit(&bars.empty[slot]);
+                if (++slot == kSlots) {
+                    slot = 0;
+                    ph ^= 1;
+                }
+            };
+            auto pv = [&](bool accumulate) -> bool {
+                uint32_t vaddr;
+                if (!take(vaddr)) return false;
+                if (!mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim)) return false;
+                pf_ph ^= 1;
+                tc::fence_after_sync();
+                tc::gemm_128x128x128(tmem + kColO, sPb, vaddr, true, accumulate);
+                release();
+                tc::mma_commit(&bars.o_done);
+                return true;
+            };
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+                const int b = tile_of(t, a.BH, a.N).b;
+                for (int c = b - 1; c >= 0 && ok; --c) {
+                    if (c == b - 1) {
+                        ok = mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim);
+                        qt_ph ^= 1;
+                    } else {
+                        ok = mbar_wait(&bars.qb_conv_full, qc_ph, a.err, abort_word, lim);
+                        qc_ph ^= 1;
+                    }
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    uint32_t addr;
+                    if (c >= 1) {
+                        if (!(ok = take(addr))) break;
+                        tc::gemm_128x128x128(tmem + kColX, sQb, addr, false, false);
+                        release();
+                        tc::mma_commit(&bars.x_full);
+                    }
+                    if (!(ok = take(addr))) break;
+                    if (!(ok = mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim))) break;
+                    se_ph ^= 1;
+                    tc::fence_after_sync();
+                    tc::gemm_128x128x128(tmem + kColS, sQb, addr, false, false);
+                    release();
+                    tc::mma_commit(&bars.s_full);
+                    if (c == 0) tc::mma_commit(&bars.qb_empty);
+                    if (c >= 1) {
+                        if (!(ok = take(addr))) break;
+                        if (!(ok = mbar_wait(&bars.xb_full, xb_ph, a.err, abort_word, lim))) break;
+                        xb_ph ^= 1;
+                        tc::fence_after_sync();
+                        tc::gemm_128x128x128(tmem + kColQ, sXb, addr, true, true);
+                        release();
+                        tc::mma_commit(&bars.q_done);
+                    }
+                    ok = pv(c + 1 != b);
+                }
+                ok = ok && pv(b != 0);
+            }
+            // every MMA issued so far has completed before TMEM is released
+            tc::mma_commit(&bars.drain);
+            mbar_wait(&bars.drain, 0, a.err, nullptr, lim);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ carried query
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t xf_ph = 0, qd_ph = 0, qt_ph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+            const int b = tile_of(t, a.BH, a.N).b;
+            if (b == 0) continue;
+            ok = group_all(1, 128, mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim));
+            if (!ok) break;
+            qt_ph ^= 1;
+            // fp32 master of the carried rows starts as Qh_b (no update for b == 1)
+            if (b >= 2) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = ld_shared_v4(sQb + tc::swz_off(r, cc * 4 + q, kC));
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[e]);
+                            float2 f = __bfloat1622float2(h);
+                            v[q * 8 + 2 * e] = __float_as_uint(f.x);
+                            v[q * 8 + 2 * e + 1] = __float_as_uint(f.y);
+                        }
+                    }
+                    tc::tmem_st32(lane_addr + kColQ + cc * 32, v);
+                }
+            }
+            // second arrival on qb_empty (the first is the MMA commit after the
+            // last S of this tile): the next Qh load waits for this group too,
+            // so the Qh barrier never runs a phase ahead of it.
+            named_bar(1, 128);
+            if (threadIdx.x == 64) mbar_arrive(&bars.qb_empty);
+            tc::tmem_wait_st();
+            for (int c = b - 1; c >= 1; --c) {
+                ok = group_all(1, 128, mbar_wait(&bars.x_full, xf_ph, a.err, abort_word, lim));
+                if (!ok) break;
+                xf_ph ^= 1;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_addr + kColX + cc * 32, v);
+                    store_row_chunk_bf16(sXb, r, cc, v, -1.f);
+                }
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                named_bar(1, 128);
+                if (threadIdx.x == 64) mbar_arrive(&bars.xb_full);
+                ok = group_all(1, 128, mbar_wait(&bars.q_done, qd_ph, a.err, abort_word, lim));
+                if (!ok) break;
+                qd_ph ^= 1;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_addr + kColQ + cc * 32, v);
+                    store_row_chunk_bf16(sQb, r, cc, v, 1.f);
+                }
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                named_bar(1, 128);
+                if (threadIdx.x == 64) mbar_arrive(&bars.qb_conv_full);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+        const float sl2 = a.scale * kLog2e;
+        const bool fox = a.F != nullptr;
+        uint32_t sf_ph = 0, od_ph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+            const Tile tl = tile_of(t, a.BH, a.N);
+            const int b = tl.b, bh = tl.bh;
+            const float *Frow = fox ? a.F + (size_t)bh * a.Lp : nullptr;
+            const float fi = fox ? Frow[b * kC + r] * kLog2e : 0.f;
+            // diagonal chunk: within-chunk logits from the prep kernel
+            if (fox) bars.fsm[r] = Frow[b * kC + r] * kLog2e;
+            named_bar(2, 128);
+            float m, l;
+            uint32_t pk[kC / 2];  // P row as packed bf16 pairs
+            {
+                const float4 *srow = reinterpret_cast<const float4 *>(
+                    a.Sd + (((size_t)bh * a.N + b) * kC + r) * kC);
+                float mx = -INFINITY;
+#pragma unroll 8
+                for (int j4 = 0; j4 < kC / 4; ++j4) {
+                    const float4 s4 = srow[j4];
+                    const float xs[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * j4 + e;
+                        float v = xs[e] * sl2;
+                        if (fox) v += fi - bars.fsm[j];
+                        if (j <= r) mx = fmaxf(mx, v);
+                    }
+                }
+                m = mx;  // finite: j = r is always present
+                float sum = 0.f;
+#pragma unroll
+                for (int j4 = 0; j4 < kC / 4; ++j4) {
+                    const float4 s4 = srow[j4];
+                    const float xs[4] = {s4.x, s4.y, s4.z, s4.w};
+                    float p[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * j4 + e;
+                        float v = xs[e] * sl2;
+                        if (fox) v += fi - bars.fsm[j];
+                        p[e] = (j <= r) ? exp2f(v - m) : 0.f;
+                        sum += p[e];
+                    }
+                    pk[2 * j4] = pack_bf16(p[0], p[1]);
+                    pk[2 * j4 + 1] = pack_bf16(p[2], p[3]);
+                }
+                l = sum;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    st_shared_v4(sPb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
+                                 pk[4 * j + 2], pk[4 * j + 3]);
+                tc::fence_proxy_async();
+                named_bar(2, 128);
+                if (threadIdx.x == 192) mbar_arrive(&bars.p_full);
+            }
+            for (int c = b - 1; c >= 0; --c) {
+                if (fox) bars.fsm[r] = Frow[c * kC + r] * kLog2e;
+                ok = group_all(2, 128, mbar_wait(&bars.s_full, sf_ph, a.err, abort_word, lim));
+                if (!ok) break;
+                sf_ph ^= 1;
+                tc::fence_after_sync();
+                // pass 1: row max of the scaled logits (the barrier above also
+                // published this chunk's FoX prefix)
+                float mx = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_addr + kColS + cc * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(v[i]) * sl2;
+                        if (fox) x += fi - bars.fsm[cc * 32 + i];
+                        mx = fmaxf(mx, x);
+                    }
+                }
+                // lazy rescale: keep the reference max unless it grows by > 2^8
+                const bool rescale = mx - m > kRescaleThreshold;
+                const float mnew = rescale ? mx : m;
+                const float alpha = rescale ? exp2f(m - mnew) : 1.f;
+                // pass 2: probabilities, packed to bf16
+                float sum = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_addr + kColS + cc * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float x0 = __uint_as_float(v[i]) * sl2;
+                        float x1 = __uint_as_float(v[i + 1]) * sl2;
+                        if (fox) {
+                            x0 += fi - bars.fsm[cc * 32 + i];
+                            x1 += fi - bars.fsm[cc * 32 + i + 1];
+                        }
+                        const float p0 = exp2f(x0 - mnew), p1 = exp2f(x1 - mnew);
+                        sum += p0 + p1;
+                        pk[cc * 16 + i / 2] = pack_bf16(p0, p1);
+                    }
+                }
+                tc::fence_before_sync();
+                named_bar(2, 128);
+                if (threadIdx.x == 192) mbar_arrive(&bars.s_empty);
+                // previous PV done: P buffer free and O stable
+                ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
+                if (!ok) break;
+                od_ph ^= 1;
+                tc::fence_after_sync();
+                if (rescale) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t v[32];
+                        tc::tmem_ld32(lane_addr + kColO + cc * 32, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tc::tmem_st32(lane_addr + kColO + cc * 32, v);
+                    }
+                    tc::tmem_wait_st();
+                }
+                l = l * alpha + sum;
+                m = mnew;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    st_shared_v4(sPb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
+                                 pk[4 * j + 2], pk[4 * j + 3]);
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                named_bar(2, 128);
+                if (threadIdx.x == 192) mbar_arrive(&bars.p_full);
+            }
+            if (!ok) break;
+            // epilogue: out = O / l, lse = ln(2) * (m + log2 l)
+            ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
+            if (!ok) break;
+            od_ph ^= 1;
+            tc::fence_after_sync();
+            const int row = b * kC + r;
+            const float inv = 1.f / l;
+            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.L + row) * kD;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t v[32];
+                tc::tmem_ld32(lane_addr + kColO + cc * 32, v);
+                if (row < a.L) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 u;
+                        u.x = pack_bf16(__uint_as_float(v[q * 8 + 0]) * inv,
+                                        __uint_as_float(v[q * 8 + 1]) * inv);
+                        u.y = pack_bf16(__uint_as_float(v[q * 8 + 2]) * inv,
+                                        __uint_as_float(v[q * 8 + 3]) * inv);
+                        u.z = pack_bf16(__uint_as_float(v[q * 8 + 4]) * inv,
+                                        __uint_as_float(v[q * 8 + 5]) * inv);
+                        u.w = pack_bf16(__uint_as_float(v[q * 8 + 6]) * inv,
+                                        __uint_as_float(v[q * 8 + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + cc * 32 + q * 8) = u;
+                    }
+                }
+            }
+            if (a.lse && row < a.L) a.lse[(size_t)bh * a.L + row] = (m + log2f(l)) * kLn2;
+            tc::fence_before_sync();
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
+                            cudaStream_t st) {
+    const int T = a.N * a.BH;
+    const int grid = T < num_sms ? T : num_sms;
+    cudaError_t e = cudaFuncSetAttribute(flash_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    flash_tc_kernel<<<grid, kThreadsTC, kSmemBytes, st>>>(maps, a);
+    return cudaGetLastError();
+}
+
+}  // namespace path
