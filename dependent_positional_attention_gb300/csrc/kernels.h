@@ -67,7 +67,7 @@ cudaError_t launch_kcache_sweep(const KcacheArgs &a, cudaStream_t st);
 
 // Tensor-core scan (bf16, head_dim 128, chunk 128).  Maps: 3-D bf16 tensors
 // [BH][rows][128] in 64 x 128 boxes with 128-byte swizzle.
-struct __align__(64) FlashTcMaps {
+struct FlashTcMaps {
     CUtensorMap qh, kh, wt;  // workspace, rows = Lp
     CUtensorMap w, v;        // inputs, rows = L
 };

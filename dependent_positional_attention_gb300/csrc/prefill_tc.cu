@@ -60,7 +60,11 @@ struct Bars {
 constexpr int kSmemBytes = kOffBar + (int)((sizeof(Bars) + 127) / 128 * 128) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 
+// Warpgroup barrier.  bar.sync is a warp-aligned instruction: every lane of
+// the warp must execute it together, so the warp is reconverged first (lanes
+// may leave a bounded wait loop at different iterations).
 __device__ __forceinline__ void named_bar(int id, int n) {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
@@ -68,6 +72,7 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 // wait that gave up in one thread makes the whole group leave together.
 __device__ __forceinline__ bool group_all(int id, int n, bool ok) {
     uint32_t r;
+    __syncwarp();
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
         "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
@@ -335,6 +340,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             // so the Qh barrier never runs a phase ahead of it.
             named_bar(1, 128);
             if (threadIdx.x == 64) mbar_arrive(&bars.qb_empty);
+            __syncwarp();
             tc::tmem_wait_st();
             for (int c = b - 1; c >= 1; --c) {
                 ok = group_all(1, 128, mbar_wait(&bars.x_full, xf_ph, a.err, abort_word, lim));
@@ -449,9 +455,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         mx = fmaxf(mx, x);
                     }
                 }
-                // lazy rescale: keep the reference max unless it grows by > 2^8
-                const bool rescale = mx - m > kRescaleThreshold;
-                const float mnew = rescale ? mx : m;
+                // lazy rescale: keep the reference max unless it grows by > 2^8.
+                // The decision is made per warp (the O rescale uses warp-aligned
+                // TMEM loads/stores); a lane that did not need it rescales by its
+                // exact factor, which is <= 1.
+                const bool rescale = __any_sync(0xffffffffu, mx - m > kRescaleThreshold);
+                const float mnew = rescale ? fmaxf(m, mx) : m;
                 const float alpha = rescale ? exp2f(m - mnew) : 1.f;
                 // pass 2: probabilities, packed to bf16
                 float sum = 0.f;
@@ -515,6 +524,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t v[32];
+                __syncwarp();  // the ragged-row branch below diverges; the load is warp-aligned
                 tc::tmem_ld32(lane_addr + kColO + cc * 32, v);
                 if (row < a.L) {
 #pragma unroll
@@ -538,6 +548,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
 
     tc::fence_before_sync();
+    __syncwarp();
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
