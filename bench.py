@@ -1,0 +1,414 @@
+"""Benchmark of the PaTH attention hot path on GB300.
+
+Headline: PaTH prefill forward, B8 H12 L4096 d128 bf16 (one step = the UT
+prep kernel + the tensor-core scan kernel over one batch).  The same line
+also reports, as nested objects, the PaTH-FoX prefill (same shape), the
+long-context prefill (B1 H12 L32768, beta mostly near 2) and the decode
+workload (B16 H12 d128, 65536 cached tokens, 256 steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on
+its own GPU (weak scaling, no data-path collective); the elapsed time is the
+max over ranks.  `--impl reference` times the fp64 CPU oracle on sampled
+query rows of the headline workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import dependent_positional_attention_gb300 as pa  # noqa: E402
+from dependent_positional_attention_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "PaTH prefill tokens/s & TFLOP/s (L=4K,d=128,bf16); decode HBM GB/s"
+CHUNK = 128
+
+
+def prefill_flops(B, H, L, d, C=CHUNK):
+    """Algorithmic FLOPs: QK^T + PV over the causal triangle (2 d L^2 per head),
+    the carried-query update (two C x C x d GEMMs per off-diagonal chunk pair
+    except the last: 4 C^2 d (N-1)(N-2)/2), and the chunk UT transform
+    (16 L C d).  Returns (scan_flops, prep_flops)."""
+    N = math.ceil(L / C)
+    scan = (2 * d * L * L + 4 * C * C * d * (N - 1) * (N - 2) / 2) * B * H
+    prep = 16 * L * C * d * B * H
+    return scan, prep
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during a timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_prefill(x, steps, warmup, ws, fox=False, sampler=None):
+    """Times K prefill steps (prep + scan) with CUDA events on the launching
+    stream; returns (ms_per_step, prep_ms, scan_ms)."""
+    q, k, v, w, beta = (x[n] for n in ("q", "k", "v", "w", "beta"))
+    log_f = x.get("log_f") if fox else None
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    ws_t = pa.path_attn_prefill_prep(q, k, w, beta, log_f=log_f)
+    for _ in range(warmup):
+        pa.path_attn_prefill_prep(q, k, w, beta, log_f=log_f, workspace=ws_t)
+        pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        pa.path_attn_prefill_prep(q, k, w, beta, log_f=log_f, workspace=ws_t)
+        ev[i][1].record(stream)
+        pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(ws)
+    total = t0.elapsed_time(t1) / steps
+    prep = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    scan = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    if pa.path_attn_device_status() != 0:
+        raise RuntimeError("device error flag set during prefill timing")
+    return total, prep, scan, clocks
+
+
+def prefill_block(wlk, steps, warmup, ws, peaks, seed=0, sampler=None):
+    x = wl.workload_inputs(wlk, seed=seed, device="cuda")
+    B, H, L, d = wlk.batch, wlk.heads, wlk.seq_len, wlk.head_dim
+    ms, prep_ms, scan_ms, clocks = timed_prefill(x, steps, warmup, ws, fox=wlk.fox,
+                                                 sampler=sampler)
+    ms = max_over_ranks(ms, ws)
+    scan_f, prep_f = prefill_flops(B, H, L, d)
+    tflops = ws * (scan_f + prep_f) / (ms * 1e-3) / 1e12
+    scan_tf = scan_f / (scan_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    res = {
+        "workload": wlk.name, "tokens_per_s": ws * B * L / (ms * 1e-3), "tflops": tflops,
+        "ms_per_step": ms, "prep_ms": prep_ms, "scan_ms": scan_ms,
+        "flops_per_step": scan_f + prep_f,
+        "roofline": {"kernel": "flash_tc_kernel (tensor-core scan)", "bound": "tensor",
+                     "achieved": scan_tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": scan_tf / peak, "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 dense (burst)"},
+    }
+    del x
+    torch.cuda.empty_cache()
+    return res, clocks
+
+
+def e2e_prefill(wlk, steps, warmup, ws, seed=0):
+    """Same metric through the public API with pinned host buffers: each step
+    copies the inputs host->device, runs the prefill, copies out back."""
+    xh = wl.workload_inputs(wlk, seed=seed, device="cpu")
+    xh = {n: t.pin_memory() for n, t in xh.items()}
+    xd = {n: torch.empty_like(t, device="cuda") for n, t in xh.items()}
+    out_h = torch.empty_like(xh["q"]).pin_memory()
+    q = xd["q"]
+    stream = torch.cuda.current_stream()
+    ws_t = torch.empty(pa.path_attn_prefill_workspace_size(pa._prefill_desc(q, None, 0)),
+                       device="cuda", dtype=torch.uint8)
+    out_d = torch.empty_like(q)
+
+    def step():
+        for n in xh:
+            xd[n].copy_(xh[n], non_blocking=True)
+        pa.path_attn_prefill_fwd(xd["q"], xd["k"], xd["v"], xd["w"], xd["beta"],
+                                 log_f=xd.get("log_f"), out=out_d, workspace=ws_t,
+                                 want_lse=False)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / steps, ws)
+    h2d = sum(t.numel() * t.element_size() for t in xh.values())
+    d2h = out_h.numel() * out_h.element_size()
+    return {"value": ws * wlk.batch * wlk.seq_len / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def decode_block(wlk, steps, warmup, ws, peaks, seed=0):
+    B, H, d, L0 = wlk.batch, wlk.heads, wlk.head_dim, wlk.prefix_len
+    nsteps = steps if steps > 0 else wlk.steps
+    cap = L0 + warmup + nsteps
+    x = wl.prefill_inputs(B, H, L0, d, "bf16", seed=seed, device="cuda")
+    kc = torch.zeros((B, H, cap, d), device="cuda", dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    pa.path_attn_build_kcache(x["k"], x["w"], x["beta"], kc)
+    vc[:, :, :L0] = x["v"]
+    del x
+    torch.cuda.empty_cache()
+    toks = [wl.decode_token(B, H, d, "bf16", seed=10_000 + seed + t, device="cuda")
+            for t in range(warmup + nsteps)]
+    out = torch.empty((B, H, d), device="cuda", dtype=torch.bfloat16)
+    wsz = pa.path_attn_decode_workspace_size(pa.decode_desc(kc))
+    wsp = torch.empty(max(wsz, 16), device="cuda", dtype=torch.uint8)
+    t = L0
+    for i in range(warmup):
+        g = toks[i]
+        pa.path_attn_decode_step(kc, vc, t, g["q"], g["k"], g["v"], g["w"], g["beta"], out=out,
+                                 workspace=wsp)
+        t += 1
+    stream = torch.cuda.current_stream()
+    barrier(ws)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1)]
+    evs[0].record(stream)
+    bytes_total = 0
+    for i in range(nsteps):
+        g = toks[warmup + i]
+        pa.path_attn_decode_step(kc, vc, t, g["q"], g["k"], g["v"], g["w"], g["beta"], out=out,
+                                 workspace=wsp)
+        bytes_total += 3 * B * H * t * d * 2  # read K, write K, read V
+        t += 1
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if pa.path_attn_device_status() != 0:
+        raise RuntimeError("device error flag set during decode timing")
+    ms = max_over_ranks(total_ms / nsteps, ws)
+    gbs = bytes_total / nsteps / (ms * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    res = {"workload": wlk.name, "tokens_per_s": ws * B / (ms * 1e-3), "ms_per_step": ms,
+           "steps": nsteps, "hbm_gbs": gbs * ws,
+           "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel",
+                        "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                        "frac": gbs / peak, "traffic": None,
+                        "peak_source": peaks["source"] + " copy bandwidth"}}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+class OracleSampler:
+    """fp64 oracle on uniformly sampled query rows of a few heads of a
+    workload (inputs drawn once, with the workload's seeded generator)."""
+
+    def __init__(self, wlk, heads=8, seed=3):
+        x = wl.workload_inputs(wlk, seed=0, device="cpu")
+        BH = wlk.batch * wlk.heads
+        self.g = torch.Generator().manual_seed(seed)
+        sel = torch.randperm(BH, generator=self.g)[:heads].tolist()
+        flat = {n: t.reshape((BH,) + tuple(t.shape[2:]))[sel].double().numpy()
+                for n, t in x.items()}
+        self.args = [flat[n] for n in ("q", "k", "v", "w", "beta")]
+        self.log_f = flat.get("log_f")
+        self.heads, self.L = heads, wlk.seq_len
+        self.threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+    def run(self, rows_per_head):
+        import oracle
+        rows = torch.randint(0, self.L, (rows_per_head,), generator=self.g).tolist()
+        t0 = time.perf_counter()
+        oracle.prefill(*self.args, log_f=self.log_f, rows=rows)
+        return time.perf_counter() - t0, rows_per_head * self.heads
+
+    def calibrated(self, target_s):
+        dt, n = self.run(8)
+        return max(8, min(4096, int(target_s / max(dt / n, 1e-7) / self.heads)))
+
+
+# ----------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="headline workload only (no FoX / long / decode objects)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_info()
+    head = wl.PREFILL_4K
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps, warm = args.steps, max(args.warmup, 0)
+        import oracle
+        oracle.build()
+        smp = OracleSampler(head, heads=2, seed=100)
+        per_step = smp.calibrated(0.5)
+        threads = smp.threads
+        rates = []
+        for i in range(warm + steps):
+            dt, n = smp.run(per_step)
+            if i >= warm:
+                rates.append((n, dt))
+        n_tot = sum(n for n, _ in rates)
+        t_tot = sum(dt for _, dt in rates)
+        value = n_tot / t_tot
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+                "ms_per_step": 1e3 * t_tot / steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": head.name, "batch": head.batch, "heads": head.heads,
+                           "seq_len": head.seq_len, "head_dim": head.head_dim},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                                 "kind": "oracle",
+                                 "sample": "%d uniformly sampled query rows of 2 heads per step"
+                                           % (n_tot // max(steps, 1))},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from dependent_positional_attention_gb300 import build as pa_build
+    pa_build.build()
+    pa.load_library()
+    peaks = load_peaks()
+    warmup = max(3, args.warmup)
+    steps = max(1, args.steps)
+
+    sampler = ClockSampler() if rank == 0 else None
+    main_res, clocks = prefill_block(head, steps, warmup, ws, peaks, sampler=sampler)
+    e2e = e2e_prefill(head, max(3, steps // 2), 2, ws)
+    extra = {}
+    if not args.skip_extra:
+        extra["fox_4k"], _ = prefill_block(wl.FOX_4K, steps, warmup, ws, peaks)
+        extra["long_32k"], _ = prefill_block(wl.PREFILL_32K, max(3, steps // 4), 3, ws, peaks)
+        extra["decode_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws, peaks)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        smp = OracleSampler(head, heads=8)
+        dt, n = smp.run(smp.calibrated(10.0))
+        threads = smp.threads
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": "%d uniformly sampled query rows (8 heads) of the B8 H12 L4096 "
+                         "workload, %.1f s" % (n, dt)}
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": main_res["tokens_per_s"], "unit": "tokens/s",
+        "n_gpus": ws, "steps": steps, "warmup": warmup, "ms_per_step": main_res["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": head.name, "batch_per_gpu": head.batch, "heads": head.heads,
+                   "seq_len": head.seq_len, "head_dim": head.head_dim, "chunk": CHUNK,
+                   "l2": "inputs larger than L2 (%.0f MB read per step)"
+                         % (5 * head.batch * head.heads * head.seq_len * head.head_dim * 2 / 1e6),
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "tflops": main_res["tflops"], "prep_ms": main_res["prep_ms"],
+        "scan_ms": main_res["scan_ms"], "roofline": main_res["roofline"],
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": 2 * steps,
+        "workloads": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

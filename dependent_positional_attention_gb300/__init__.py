@@ -13,7 +13,8 @@ import os
 import threading
 
 __all__ = [
-    "PathAttnError", "load_library", "path_attn_prefill_fwd", "path_attn_decode_step",
+    "PathAttnError", "load_library", "path_attn_prefill_fwd", "path_attn_prefill_prep",
+    "path_attn_prefill_scan", "path_attn_decode_step",
     "path_attn_build_kcache", "path_attn_prefill_workspace_size",
     "path_attn_decode_workspace_size", "path_attn_build_kcache_workspace_size",
     "path_attn_device_status", "path_attn_selftest_bounded_wait", "EXPORTED_SYMBOLS",
@@ -26,7 +27,8 @@ PATH_OK, PATH_ERR_INVALID_ARG, PATH_ERR_UNSUPPORTED, PATH_ERR_CUDA, PATH_ERR_TIM
 PATH_F32, PATH_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = (
-    "path_attn_prefill_workspace_size", "path_attn_prefill_fwd",
+    "path_attn_prefill_workspace_size", "path_attn_prefill_fwd", "path_attn_prefill_prep",
+    "path_attn_prefill_scan",
     "path_attn_decode_workspace_size", "path_attn_decode_step",
     "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
     "path_attn_device_status", "path_attn_selftest_bounded_wait",
@@ -80,6 +82,8 @@ def load_library(path: str | None = None):
         lib.path_attn_prefill_workspace_size.restype = _SZ
         lib.path_attn_prefill_fwd.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                               _VP, _SZ, _VP]
+        lib.path_attn_prefill_prep.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
+        lib.path_attn_prefill_scan.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
         lib.path_attn_decode_workspace_size.argtypes = [dd]
         lib.path_attn_decode_workspace_size.restype = _SZ
         lib.path_attn_decode_step.argtypes = [dd, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
@@ -93,7 +97,8 @@ def load_library(path: str | None = None):
         lib.path_attn_status_string.restype = ctypes.c_char_p
         lib.path_attn_last_error.restype = ctypes.c_char_p
         lib.path_attn_version.restype = ctypes.c_int32
-        for f in ("path_attn_prefill_fwd", "path_attn_decode_step", "path_attn_build_kcache",
+        for f in ("path_attn_prefill_fwd", "path_attn_prefill_prep", "path_attn_prefill_scan",
+                  "path_attn_decode_step", "path_attn_build_kcache",
                   "path_attn_device_status", "path_attn_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         if path is None:
@@ -177,6 +182,39 @@ def path_attn_prefill_fwd(q, k, v, w, beta, log_f=None, out=None, lse=None, scal
         ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+    return out, lse
+
+
+def path_attn_prefill_prep(q, k, w, beta, log_f=None, scale=None, chunk=0, workspace=None,
+                          stream=None):
+    """Stage 1 of the prefill (see path_attn_prefill_prep in include/path_attn.h).
+    Returns the workspace tensor to pass to path_attn_prefill_scan."""
+    import torch
+    lib = load_library()
+    desc = _prefill_desc(q, scale, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(path_attn_prefill_workspace_size(desc), 16),
+                                device=q.device, dtype=torch.uint8)
+    _check(lib.path_attn_prefill_prep(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(w), _ptr(beta), _ptr(log_f),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return workspace
+
+
+def path_attn_prefill_scan(q, w, v, workspace, log_f=None, out=None, lse=None, scale=None,
+                          chunk=0, stream=None):
+    """Stage 2 of the prefill (see path_attn_prefill_scan in include/path_attn.h);
+    q is used for its shape and dtype only.  Returns (out, lse)."""
+    import torch
+    lib = load_library()
+    desc = _prefill_desc(q, scale, chunk)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    _check(lib.path_attn_prefill_scan(
+        ctypes.byref(desc), _ptr(w), _ptr(v), _ptr(log_f), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
 
 

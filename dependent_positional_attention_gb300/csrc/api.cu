@@ -193,31 +193,29 @@ size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc) {
     return p.total;
 }
 
-path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void *q,
-                                    const void *k, const void *v, const void *w,
-                                    const float *beta, const float *log_f, void *out,
-                                    float *lse, void *workspace, size_t workspace_bytes,
-                                    path_stream_t stream) {
+path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void *q,
+                                     const void *k, const void *w, const float *beta,
+                                     const float *log_f, void *workspace,
+                                     size_t workspace_bytes, path_stream_t stream) {
     PrefillPlan p;
     path_status_t s = plan_prefill(desc, &p);
     if (s != PATH_OK) return s;
-    const void *req[] = {q, k, v, w, beta, out, workspace};
-    const char *names[] = {"q", "k", "v", "w", "beta", "out", "workspace"};
-    for (int i = 0; i < 7; ++i) {
+    const void *req[] = {q, k, w, beta, workspace};
+    const char *names[] = {"q", "k", "w", "beta", "workspace"};
+    for (int i = 0; i < 5; ++i) {
         if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
         if (!aligned16(req[i]))
             return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
     }
     if (log_f && !aligned16(log_f)) return fail(PATH_ERR_INVALID_ARG, "log_f is not 16-byte aligned");
-    if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
     if (workspace_bytes < p.total)
         return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
                     p.total);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-    float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
     if (log_f) {
-        s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
+        s = cuda_status(
+            launch_fox_prefix(log_f, at<float>(workspace, p.off_F), p.L, p.Lp, p.BH, st),
+            "fox prefix launch");
         if (s != PATH_OK) return s;
     }
     PrepSimtArgs pa;
@@ -229,20 +227,43 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
     pa.scratch = at<float>(workspace, p.off_scratch);
     pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
     pa.keys_only = 0;
-    s = cuda_status(launch_prep_simt(pa, p.bf16, p.bf16, st), "prep launch");
-    if (s != PATH_OK) return s;
+    return cuda_status(launch_prep_simt(pa, p.bf16, p.bf16, st), "prep launch");
+}
 
+path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void *w,
+                                     const void *v, const float *log_f, void *out, float *lse,
+                                     void *workspace, size_t workspace_bytes,
+                                     path_stream_t stream) {
+    PrefillPlan p;
+    path_status_t s = plan_prefill(desc, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {w, v, out, workspace};
+    const char *names[] = {"w", "v", "out", "workspace"};
+    for (int i = 0; i < 4; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+    if (workspace_bytes < p.total)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.total);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const void *Qh = at<char>(workspace, p.off_Qh), *Kh = at<char>(workspace, p.off_Kh);
+    const void *Wt = at<char>(workspace, p.off_Wt);
+    const float *Sd = at<float>(workspace, p.off_Sd);
+    const float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
     if (p.bf16) {
         FlashTcMaps maps;
         const bool enc =
-            encode_tmap_bf16_3d(&maps.qh, pa.Qh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&maps.kh, pa.Kh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&maps.wt, pa.Wt, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.qh, Qh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.kh, Kh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.wt, Wt, 128, p.Lp, p.BH, 64, 128) &&
             encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128) &&
             encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         FlashTcArgs ta;
-        ta.Sd = pa.Sd; ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
+        ta.Sd = Sd; ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
         ta.scale = desc->scale; ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
@@ -250,10 +271,26 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
         return cuda_status(launch_flash_tc(maps, ta, sms, st), "tensor-core scan launch");
     }
     FlashSimtArgs fa;
-    fa.Qh = pa.Qh; fa.Kh = pa.Kh; fa.Wt = pa.Wt; fa.w = w; fa.v = v;
-    fa.Sd = pa.Sd; fa.F = F; fa.out = out; fa.lse = lse; fa.scale = desc->scale;
+    fa.Qh = Qh; fa.Kh = Kh; fa.Wt = Wt; fa.w = w; fa.v = v;
+    fa.Sd = Sd; fa.F = F; fa.out = out; fa.lse = lse; fa.scale = desc->scale;
     fa.BH = p.BH; fa.L = p.L; fa.Lp = p.Lp; fa.N = p.N; fa.C = p.C; fa.d = p.d;
     return cuda_status(launch_flash_simt(fa, st), "scan launch");
+}
+
+path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void *q,
+                                    const void *k, const void *v, const void *w,
+                                    const float *beta, const float *log_f, void *out,
+                                    float *lse, void *workspace, size_t workspace_bytes,
+                                    path_stream_t stream) {
+    if (!v) return fail(PATH_ERR_INVALID_ARG, "v is NULL");
+    if (!out) return fail(PATH_ERR_INVALID_ARG, "out is NULL");
+    if (!aligned16(v)) return fail(PATH_ERR_INVALID_ARG, "v is not 16-byte aligned");
+    if (!aligned16(out)) return fail(PATH_ERR_INVALID_ARG, "out is not 16-byte aligned");
+    if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+    path_status_t s = path_attn_prefill_prep(desc, q, k, w, beta, log_f, workspace,
+                                             workspace_bytes, stream);
+    if (s != PATH_OK) return s;
+    return path_attn_prefill_scan(desc, w, v, log_f, out, lse, workspace, workspace_bytes, stream);
 }
 
 size_t path_attn_decode_workspace_size(const path_decode_desc_t *desc) {
