@@ -29,7 +29,7 @@ PATH_F32, PATH_BF16 = 0, 1
 EXPORTED_SYMBOLS = (
     "path_attn_prefill_workspace_size", "path_attn_prefill_fwd", "path_attn_prefill_prep",
     "path_attn_prefill_scan",
-    "path_attn_decode_workspace_size", "path_attn_decode_step",
+    "path_attn_decode_workspace_size", "path_attn_decode_step", "path_attn_decode_step_noalloc",
     "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
     "path_attn_device_status", "path_attn_selftest_bounded_wait",
     "path_attn_status_string", "path_attn_last_error", "path_attn_version",
@@ -88,6 +88,8 @@ def load_library(path: str | None = None):
         lib.path_attn_decode_workspace_size.restype = _SZ
         lib.path_attn_decode_step.argtypes = [dd, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
                                               _VP, _VP, _VP, _VP, _SZ, _VP]
+        lib.path_attn_decode_step_noalloc.argtypes = [dd, _VP, _VP, ctypes.c_int32, _VP, _VP,
+                                                      _VP, _VP, _VP, _VP, _VP]
         lib.path_attn_build_kcache_workspace_size.argtypes = [pd]
         lib.path_attn_build_kcache_workspace_size.restype = _SZ
         lib.path_attn_build_kcache.argtypes = [pd, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP,
@@ -98,7 +100,8 @@ def load_library(path: str | None = None):
         lib.path_attn_last_error.restype = ctypes.c_char_p
         lib.path_attn_version.restype = ctypes.c_int32
         for f in ("path_attn_prefill_fwd", "path_attn_prefill_prep", "path_attn_prefill_scan",
-                  "path_attn_decode_step", "path_attn_build_kcache",
+                  "path_attn_decode_step", "path_attn_decode_step_noalloc",
+                  "path_attn_build_kcache",
                   "path_attn_device_status", "path_attn_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         if path is None:
@@ -254,6 +257,18 @@ def path_attn_decode_step(k_cache, v_cache, cache_len, q_t, k_t, v_t, w_t, beta_
         ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), int(cache_len), _ptr(q_t), _ptr(k_t),
         _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def path_attn_decode_step_noalloc(k_cache, v_cache, cache_len, q_t, k_t, v_t, w_t, beta_t,
+                                  out, scale=None, stream=None):
+    """path_attn_decode_step without a workspace (see include/path_attn.h):
+    for callers that cannot allocate device memory.  `out` must be given."""
+    lib = load_library()
+    desc = decode_desc(k_cache, scale)
+    _check(lib.path_attn_decode_step_noalloc(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), int(cache_len), _ptr(q_t), _ptr(k_t),
+        _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(out), _stream(stream)))
     return out
 
 

@@ -181,6 +181,12 @@ path_status_t cuda_status(cudaError_t e, const char *what) {
 }
 
 }  // namespace
+
+// Sets the message path_attn_last_error() returns on this host thread.
+void record_last_error(const char *msg) {
+    snprintf(g_msg, sizeof g_msg, "%s", msg ? msg : "");
+}
+
 }  // namespace path
 
 using namespace path;

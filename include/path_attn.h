@@ -151,6 +151,32 @@ path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cach
                                     size_t workspace_bytes, path_stream_t stream);
 
 /*
+ * path_attn_decode_step without a workspace, for callers that cannot
+ * allocate device memory: plugins running inside a host framework that owns
+ * all GPU memory and gives them no allocator, and token loops that must not
+ * call cudaMalloc because it can synchronise the device.  The PaTH pages have
+ * no counterpart to this call; it computes exactly what path_attn_decode_step
+ * computes, with the same arguments minus the workspace.
+ *
+ * The split-KV partial results live in one fixed device array of 8 MiB that
+ * every GPU loading the library holds until the process exits.  A step needs
+ * batch * heads * ceil(cache_len / 1024) * (head_dim + 2) * 4 bytes of it;
+ * larger steps are rejected with PATH_ERR_INVALID_ARG and a message naming
+ * both sizes (use path_attn_decode_step then).  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array, which keeps the last call's contents, so calls that
+ * overlap on the GPU (different streams, or different host threads on the
+ * same device) race with each other: serialise them.  Nothing is allocated
+ * or freed by this call.
+ */
+path_status_t path_attn_decode_step_noalloc(const path_decode_desc_t *desc, void *k_cache,
+                                            void *v_cache, int32_t cache_len, const void *q_t,
+                                            const void *k_t, const void *v_t, const void *w_t,
+                                            const float *beta_t, void *out,
+                                            path_stream_t stream);
+
+/*
  * Key cache after a prefill of seq_len tokens, as the decode step expects it:
  *     k_cache[j] = H_{L-1} ... H_{j+1} k_j    (j < L = desc->seq_len),
  * i.e. every key transformed by all later transitions (inference bullet of

@@ -85,3 +85,16 @@ def test_workspace_grows_with_problem(lib):
     b = lib.path_attn_prefill_workspace_size(ctypes.byref(D(2, 1, 128, 128, 1, 0.1, 0)))
     c = lib.path_attn_prefill_workspace_size(ctypes.byref(D(1, 1, 129, 128, 1, 0.1, 0)))
     assert 0 < a < b and a < c
+
+
+def test_noalloc_decode_rejects_steps_beyond_its_fixed_scratch(lib):
+    """Rejected before any CUDA call, so this runs without a GPU."""
+    desc = pa.DecodeDesc(64, 64, 128, 1 << 20, 1, 0.088)
+    rc = lib.path_attn_decode_step_noalloc(ctypes.byref(desc), FAKE, FAKE, 500000, FAKE, FAKE,
+                                           FAKE, FAKE, FAKE, FAKE, None)
+    assert rc == pa.PATH_ERR_INVALID_ARG
+    msg = lib.path_attn_last_error()
+    assert b"scratch" in msg and b"8388608" in msg
+    small = pa.DecodeDesc(1, 1, 128, 16, 1, 0.088)
+    assert lib.path_attn_decode_step_noalloc(ctypes.byref(small), FAKE, FAKE, 16, FAKE, FAKE,
+                                             FAKE, FAKE, FAKE, FAKE, None) == pa.PATH_ERR_INVALID_ARG
