@@ -107,7 +107,8 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     p->off_Wt = off; off = align_up(off + rows * p->d * p->esize, 256);
     p->off_Sd = off; off = align_up(off + cc * 4, 256);
     p->off_F = off; off = align_up(off + rows * 4, 256);
-    p->off_scratch = off; off = align_up(off + cc * 5 * 4, 256);
+    // fp32 scratch of the SIMT prep (the tensor-core prep keeps it on chip)
+    p->off_scratch = off; off = align_up(off + (p->bf16 ? 0 : cc * 5 * 4), 256);
     p->total = off;
     return ok();
 }
@@ -224,6 +225,24 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
             "fox prefix launch");
         if (s != PATH_OK) return s;
     }
+    if (p.bf16) {
+        PrepTcMaps maps;
+        const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.k, k, 128, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128);
+        if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+        PrepTcArgs ta;
+        ta.beta = beta;
+        ta.Qh = at<char>(workspace, p.off_Qh);
+        ta.Kh = at<char>(workspace, p.off_Kh);
+        ta.Wt = at<char>(workspace, p.off_Wt);
+        ta.Sd = at<float>(workspace, p.off_Sd);
+        ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        ta.err = error_flag_ptr();
+        const int sms = num_sms();
+        if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+        return cuda_status(launch_prep_tc(maps, ta, sms, st), "tensor-core prep launch");
+    }
     PrepSimtArgs pa;
     pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
     pa.Qh = at<char>(workspace, p.off_Qh);
@@ -233,7 +252,7 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
     pa.scratch = at<float>(workspace, p.off_scratch);
     pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
     pa.keys_only = 0;
-    return cuda_status(launch_prep_simt(pa, p.bf16, p.bf16, st), "prep launch");
+    return cuda_status(launch_prep_simt(pa, false, false, st), "prep launch");
 }
 
 path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void *w,

@@ -84,6 +84,23 @@ struct FlashTcArgs {
 cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
                             cudaStream_t st);
 
+// Tensor-core prep (bf16, head_dim 128, chunk 128): maps over the raw q, k, w
+// inputs ([BH][L][128], 64 x 128 boxes, 128-byte swizzle).
+struct PrepTcMaps {
+    CUtensorMap q, k, w;
+};
+
+struct PrepTcArgs {
+    const float *beta;
+    void *Qh, *Kh, *Wt;
+    float *Sd;
+    int BH, L, Lp, N;
+    uint32_t *err;
+};
+
+cudaError_t launch_prep_tc(const PrepTcMaps &maps, const PrepTcArgs &a, int num_sms,
+                           cudaStream_t st);
+
 cudaError_t launch_selftest_wait(uint32_t *err_flag, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace path
