@@ -13,12 +13,15 @@
 // the update MMA); only its bf16 shadow in shared memory feeds the next MMAs.
 //
 // One CTA per SM (persistent), tiles ordered by decreasing work.  Warp roles:
-//   warp 0      TMA producer: Qh_b, then a 4-slot ring of W_c, Kh_c, Wt_c, V
-//   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2-5   carried-query warpgroup: X -> -X bf16 (A operand of the
+//   warps 0-3   carried-query warpgroup: X -> -X bf16 (A operand of the
 //               update), Qt fp32 -> bf16 shadow, Qt initialisation
-//   warps 6-9   softmax warpgroup: logits, online softmax with lazy rescale
+//   warps 4-7   softmax warpgroup: logits, online softmax with lazy rescale
 //               of O, P -> bf16, epilogue (out, lse)
+//   warp 8      TMA producer: Qh_b, then a 4-slot ring of W_c, Kh_c, Wt_c, V
+//   warp 9      MMA issuer (one thread) and TMEM owner; warps 10-11 idle
+// Registers are rebalanced at start (setmaxnreg): the producer/MMA group
+// drops to 120 per thread, the two compute groups rise to 192 (the launch's
+// 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512).
 // MMA issue order per step c: X_c, S_c, update_c, PV_{c+1}; the PV of a chunk
 // runs one step late so the softmax has a full step of slack.
 // TMEM columns: [0,128) Qt fp32, [128,256) X, [256,384) S, [384,512) O.
@@ -35,7 +38,7 @@ namespace {
 constexpr int kD = 128, kC = 128;
 constexpr int kSlots = 4;
 constexpr int kTileBytes = kC * kD * 2;  // 32 KB bf16 tile
-constexpr int kThreadsTC = 320;
+constexpr int kThreadsTC = 384;  // 3 warpgroups
 constexpr uint32_t kColQ = 0, kColX = 128, kColS = 256, kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -102,18 +105,17 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-// Writes 32 fp32 values (columns 32*cc .. 32*cc+31 of row r), optionally
-// negated, as bf16 into a swizzled 128-column operand tile.
-__device__ __forceinline__ void store_row_chunk_bf16(uint32_t tile, int r, int cc,
-                                                     const uint32_t (&v)[32], float sign) {
+// Writes a full 128-value fp32 row (optionally negated) as bf16 into a
+// swizzled 128-column operand tile.
+__device__ __forceinline__ void store_row_bf16(uint32_t tile, int r, const uint32_t (&v)[128],
+                                               float sign) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int j = cc * 4 + q;
+    for (int j = 0; j < 16; ++j) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(sign * __uint_as_float(v[q * 8 + 2 * e]),
-                             sign * __uint_as_float(v[q * 8 + 2 * e + 1]));
+            w[e] = pack_bf16(sign * __uint_as_float(v[j * 8 + 2 * e]),
+                             sign * __uint_as_float(v[j * 8 + 2 * e + 1]));
         st_shared_v4(tile + tc::swz_off(r, j, kC), w[0], w[1], w[2], w[3]);
     }
 }
@@ -129,6 +131,7 @@ __device__ __forceinline__ Tile tile_of(int t, int BH, int N) {
     return x;
 }
 
+template <bool kFox>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     flash_tc_kernel(const __grid_constant__ FlashTcMaps maps, FlashTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         bars.abort_word = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 9) {
         tc::tmem_alloc(&bars.tmem_base, 512);
         tc::tmem_relinquish();
     }
@@ -171,8 +174,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = bars.tmem_base;
-
-    if (warp == 0) {
+    if (warp >= 8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+      if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tc::prefetch_tmap(&maps.qh);
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int slot = 0;
@@ -302,7 +306,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_wait(&bars.drain, 0, a.err, nullptr, lim);
         }
         __syncwarp();
-    } else if (warp < 6) {
+      }
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+      if (warp < 4) {
         // ------------------------------------------------------------ carried query
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             // last S of this tile): the next Qh load waits for this group too,
             // so the Qh barrier never runs a phase ahead of it.
             named_bar(1, 128);
-            if (threadIdx.x == 64) mbar_arrive(&bars.qb_empty);
+            if (threadIdx.x == 0) mbar_arrive(&bars.qb_empty);
             __syncwarp();
             tc::tmem_wait_st();
             for (int c = b - 1; c >= 1; --c) {
@@ -347,39 +354,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!ok) break;
                 xf_ph ^= 1;
                 tc::fence_after_sync();
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_addr + kColX + cc * 32, v);
-                    store_row_chunk_bf16(sXb, r, cc, v, -1.f);
+                {
+                    uint32_t v[128];
+                    tc::tmem_ld128(lane_addr + kColX, v);
+                    store_row_bf16(sXb, r, v, -1.f);
                 }
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 named_bar(1, 128);
-                if (threadIdx.x == 64) mbar_arrive(&bars.xb_full);
+                if (threadIdx.x == 0) mbar_arrive(&bars.xb_full);
                 ok = group_all(1, 128, mbar_wait(&bars.q_done, qd_ph, a.err, abort_word, lim));
                 if (!ok) break;
                 qd_ph ^= 1;
                 tc::fence_after_sync();
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_addr + kColQ + cc * 32, v);
-                    store_row_chunk_bf16(sQb, r, cc, v, 1.f);
+                {
+                    uint32_t v[128];
+                    tc::tmem_ld128(lane_addr + kColQ, v);
+                    store_row_bf16(sQb, r, v, 1.f);
                 }
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 named_bar(1, 128);
-                if (threadIdx.x == 64) mbar_arrive(&bars.qb_conv_full);
+                if (threadIdx.x == 0) mbar_arrive(&bars.qb_conv_full);
             }
         }
-    } else {
+      } else {
         // ------------------------------------------------------------ softmax
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
         const float sl2 = a.scale * kLog2e;
-        const bool fox = a.F != nullptr;
+        constexpr bool fox = kFox;
         uint32_t sf_ph = 0, od_ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                  pk[4 * j + 2], pk[4 * j + 3]);
                 tc::fence_proxy_async();
                 named_bar(2, 128);
-                if (threadIdx.x == 192) mbar_arrive(&bars.p_full);
+                if (threadIdx.x == 128) mbar_arrive(&bars.p_full);
             }
             for (int c = b - 1; c >= 0; --c) {
                 if (fox) bars.fsm[r] = Frow[c * kC + r] * kLog2e;
@@ -441,19 +446,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!ok) break;
                 sf_ph ^= 1;
                 tc::fence_after_sync();
-                // pass 1: row max of the scaled logits (the barrier above also
-                // published this chunk's FoX prefix)
+                // one load of the logit row; S is free for the next MMA after it
+                uint32_t v[128];
+                tc::tmem_ld128(lane_addr + kColS, v);
                 float mx = -INFINITY;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_addr + kColS + cc * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(v[i]) * sl2;
-                        if (fox) x += fi - bars.fsm[cc * 32 + i];
-                        mx = fmaxf(mx, x);
-                    }
+                for (int j = 0; j < kC; ++j) {
+                    float t = __uint_as_float(v[j]) * sl2;
+                    if (kFox) t += fi - bars.fsm[j];
+                    v[j] = __float_as_uint(t);
+                    mx = fmaxf(mx, t);
                 }
                 // lazy rescale: keep the reference max unless it grows by > 2^8.
                 // The decision is made per warp (the O rescale uses warp-aligned
@@ -462,28 +464,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 const bool rescale = __any_sync(0xffffffffu, mx - m > kRescaleThreshold);
                 const float mnew = rescale ? fmaxf(m, mx) : m;
                 const float alpha = rescale ? exp2f(m - mnew) : 1.f;
-                // pass 2: probabilities, packed to bf16
                 float sum = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_addr + kColS + cc * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float x0 = __uint_as_float(v[i]) * sl2;
-                        float x1 = __uint_as_float(v[i + 1]) * sl2;
-                        if (fox) {
-                            x0 += fi - bars.fsm[cc * 32 + i];
-                            x1 += fi - bars.fsm[cc * 32 + i + 1];
-                        }
-                        const float p0 = exp2f(x0 - mnew), p1 = exp2f(x1 - mnew);
-                        sum += p0 + p1;
-                        pk[cc * 16 + i / 2] = pack_bf16(p0, p1);
-                    }
+                for (int j = 0; j < kC / 2; ++j) {
+                    const float p0 = exp2f(__uint_as_float(v[2 * j]) - mnew);
+                    const float p1 = exp2f(__uint_as_float(v[2 * j + 1]) - mnew);
+                    sum += p0 + p1;
+                    pk[j] = pack_bf16(p0, p1);
                 }
                 tc::fence_before_sync();
                 named_bar(2, 128);
-                if (threadIdx.x == 192) mbar_arrive(&bars.s_empty);
+                if (threadIdx.x == 128) mbar_arrive(&bars.s_empty);
                 // previous PV done: P buffer free and O stable
                 ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
                 if (!ok) break;
@@ -510,7 +501,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 named_bar(2, 128);
-                if (threadIdx.x == 192) mbar_arrive(&bars.p_full);
+                if (threadIdx.x == 128) mbar_arrive(&bars.p_full);
             }
             if (!ok) break;
             // epilogue: out = O / l, lse = ln(2) * (m + log2 l)
@@ -522,13 +513,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             const float inv = 1.f / l;
             __nv_bfloat16 *orow = a.out + ((size_t)bh * a.L + row) * kD;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t v[32];
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t v[64];
                 __syncwarp();  // the ragged-row branch below diverges; the load is warp-aligned
-                tc::tmem_ld32(lane_addr + kColO + cc * 32, v);
+                tc::tmem_ld64(lane_addr + kColO + cc * 64, v);
                 if (row < a.L) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 8; ++q) {
                         uint4 u;
                         u.x = pack_bf16(__uint_as_float(v[q * 8 + 0]) * inv,
                                         __uint_as_float(v[q * 8 + 1]) * inv);
@@ -538,7 +529,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                         __uint_as_float(v[q * 8 + 5]) * inv);
                         u.w = pack_bf16(__uint_as_float(v[q * 8 + 6]) * inv,
                                         __uint_as_float(v[q * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + cc * 32 + q * 8) = u;
+                        *reinterpret_cast<uint4 *>(orow + cc * 64 + q * 8) = u;
                     }
                 }
             }
@@ -547,10 +538,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
     }
 
+    }
     tc::fence_before_sync();
     __syncwarp();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 9) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, 512);
     }
@@ -562,10 +554,12 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
                             cudaStream_t st) {
     const int T = a.N * a.BH;
     const int grid = T < num_sms ? T : num_sms;
-    cudaError_t e = cudaFuncSetAttribute(flash_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    void (*kern)(const FlashTcMaps, FlashTcArgs) =
+        a.F ? flash_tc_kernel<true> : flash_tc_kernel<false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    flash_tc_kernel<<<grid, kThreadsTC, kSmemBytes, st>>>(maps, a);
+    kern<<<grid, kThreadsTC, kSmemBytes, st>>>(maps, a);
     return cudaGetLastError();
 }
 
