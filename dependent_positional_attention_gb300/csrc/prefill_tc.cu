@@ -85,6 +85,14 @@ __device__ __forceinline__ bool group_all(int id, int n, bool ok) {
     return r != 0;
 }
 
+// 2^x on the MUFU unit (inputs here are <= 0 after the max subtraction;
+// results below 2^-126 flush to zero, which a softmax weight can ignore).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -237,6 +245,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (lane == 0) {
             int slot = 0;
             uint32_t ph = 0, qt_ph = 0, qc_ph = 0, xb_ph = 0, se_ph = 0, pf_ph = 0;
+            const uint32_t qb_lo = tc::desc_lo(sQb, false), xb_lo = tc::desc_lo(sXb, false);
+            const uint32_t pb_lo = tc::desc_lo(sPb, false);
             bool ok = true;
             auto take = [&](uint32_t &addr) -> bool {
                 if (!mbar_wait(&bars.full[slot], ph, a.err, abort_word, lim)) return false;
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim)) return false;
                 pf_ph ^= 1;
                 tc::fence_after_sync();
-                tc::gemm_128x128x128(tmem + kColO, sPb, vaddr, true, accumulate);
+                tc::gemm128_lo<true>(tmem + kColO, pb_lo, tc::desc_lo(vaddr, true), accumulate);
                 release();
                 tc::mma_commit(&bars.o_done);
                 return true;
@@ -276,7 +286,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     uint32_t addr;
                     if (c >= 1) {
                         if (!(ok = take(addr))) break;
-                        tc::gemm_128x128x128(tmem + kColX, sQb, addr, false, false);
+                        tc::gemm128_lo<false>(tmem + kColX, qb_lo, tc::desc_lo(addr, false), false);
                         release();
                         tc::mma_commit(&bars.x_full);
                     }
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (!(ok = mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim))) break;
                     se_ph ^= 1;
                     tc::fence_after_sync();
-                    tc::gemm_128x128x128(tmem + kColS, sQb, addr, false, false);
+                    tc::gemm128_lo<false>(tmem + kColS, qb_lo, tc::desc_lo(addr, false), false);
                     release();
                     tc::mma_commit(&bars.s_full);
                     if (c == 0) tc::mma_commit(&bars.qb_empty);
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         if (!(ok = mbar_wait(&bars.xb_full, xb_ph, a.err, abort_word, lim))) break;
                         xb_ph ^= 1;
                         tc::fence_after_sync();
-                        tc::gemm_128x128x128(tmem + kColQ, sXb, addr, true, true);
+                        tc::gemm128_lo<true>(tmem + kColQ, xb_lo, tc::desc_lo(addr, true), true);
                         release();
                         tc::mma_commit(&bars.q_done);
                     }
@@ -396,7 +406,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             if (fox) bars.fsm[r] = Frow[b * kC + r] * kLog2e;
             named_bar(2, 128);
             float m, l;
-            uint32_t pk[kC / 2];  // P row as packed bf16 pairs
             {
                 const float4 *srow = reinterpret_cast<const float4 *>(
                     a.Sd + (((size_t)bh * a.N + b) * kC + r) * kC);
@@ -415,27 +424,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 m = mx;  // finite: j = r is always present
                 float sum = 0.f;
+#pragma unroll 2
+                for (int j8 = 0; j8 < kC / 8; ++j8) {
+                    const float4 s0 = srow[2 * j8], s1 = srow[2 * j8 + 1];
+                    const float xs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                    float p[8];
 #pragma unroll
-                for (int j4 = 0; j4 < kC / 4; ++j4) {
-                    const float4 s4 = srow[j4];
-                    const float xs[4] = {s4.x, s4.y, s4.z, s4.w};
-                    float p[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * j4 + e;
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * j8 + e;
                         float v = xs[e] * sl2;
                         if (fox) v += fi - bars.fsm[j];
-                        p[e] = (j <= r) ? exp2f(v - m) : 0.f;
+                        p[e] = (j <= r) ? ex2(v - m) : 0.f;
                         sum += p[e];
                     }
-                    pk[2 * j4] = pack_bf16(p[0], p[1]);
-                    pk[2 * j4 + 1] = pack_bf16(p[2], p[3]);
+                    st_shared_v4(sPb + tc::swz_off(r, j8, kC), pack_bf16(p[0], p[1]),
+                                 pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
+                                 pack_bf16(p[6], p[7]));
                 }
                 l = sum;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    st_shared_v4(sPb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
-                                 pk[4 * j + 2], pk[4 * j + 3]);
                 tc::fence_proxy_async();
                 named_bar(2, 128);
                 if (threadIdx.x == 128) mbar_arrive(&bars.p_full);
@@ -446,16 +452,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!ok) break;
                 sf_ph ^= 1;
                 tc::fence_after_sync();
-                // one load of the logit row; S is free for the next MMA after it
+                // one load of the logit row, then S is released to the next MMA
                 uint32_t v[128];
                 tc::tmem_ld128(lane_addr + kColS, v);
+                tc::fence_before_sync();
+                named_bar(2, 128);  // also publishes this chunk's FoX prefix
+                if (threadIdx.x == 128) mbar_arrive(&bars.s_empty);
                 float mx = -INFINITY;
+                if (kFox) {
 #pragma unroll
-                for (int j = 0; j < kC; ++j) {
-                    float t = __uint_as_float(v[j]) * sl2;
-                    if (kFox) t += fi - bars.fsm[j];
-                    v[j] = __float_as_uint(t);
-                    mx = fmaxf(mx, t);
+                    for (int j = 0; j < kC; ++j) {
+                        const float t = fmaf(__uint_as_float(v[j]), sl2, fi - bars.fsm[j]);
+                        v[j] = __float_as_uint(t);
+                        mx = fmaxf(mx, t);
+                    }
+                } else {
+                    // max of the scaled logits from the raw extreme (min if scale < 0)
+                    if (sl2 >= 0.f) {
+#pragma unroll
+                        for (int j = 0; j < kC; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+                    } else {
+                        mx = INFINITY;
+#pragma unroll
+                        for (int j = 0; j < kC; ++j) mx = fminf(mx, __uint_as_float(v[j]));
+                    }
+                    mx *= sl2;
                 }
                 // lazy rescale: keep the reference max unless it grows by > 2^8.
                 // The decision is made per warp (the O rescale uses warp-aligned
@@ -464,17 +485,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 const bool rescale = __any_sync(0xffffffffu, mx - m > kRescaleThreshold);
                 const float mnew = rescale ? fmaxf(m, mx) : m;
                 const float alpha = rescale ? exp2f(m - mnew) : 1.f;
-                float sum = 0.f;
+                // probabilities, packed to bf16 pairs (the logits die as they go)
+                const float xs = kFox ? 1.f : sl2;  // FoX rows already hold scaled logits
+                float sum0 = 0.f, sum1 = 0.f;
+                uint32_t pk[kC / 2];
 #pragma unroll
-                for (int j = 0; j < kC / 2; ++j) {
-                    const float p0 = exp2f(__uint_as_float(v[2 * j]) - mnew);
-                    const float p1 = exp2f(__uint_as_float(v[2 * j + 1]) - mnew);
-                    sum += p0 + p1;
-                    pk[j] = pack_bf16(p0, p1);
+                for (int j4 = 0; j4 < kC / 4; ++j4) {
+                    float p[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        p[e] = ex2(fmaf(__uint_as_float(v[4 * j4 + e]), xs, -mnew));
+                    sum0 += p[0] + p[1];
+                    sum1 += p[2] + p[3];
+                    pk[2 * j4] = pack_bf16(p[0], p[1]);
+                    pk[2 * j4 + 1] = pack_bf16(p[2], p[3]);
                 }
-                tc::fence_before_sync();
-                named_bar(2, 128);
-                if (threadIdx.x == 128) mbar_arrive(&bars.s_empty);
                 // previous PV done: P buffer free and O stable
                 ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
                 if (!ok) break;
@@ -483,21 +508,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (rescale) {
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t v[32];
-                        tc::tmem_ld32(lane_addr + kColO + cc * 32, v);
+                        uint32_t o[32];
+                        tc::tmem_ld32(lane_addr + kColO + cc * 32, o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                        tc::tmem_st32(lane_addr + kColO + cc * 32, v);
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tc::tmem_st32(lane_addr + kColO + cc * 32, o);
                     }
                     tc::tmem_wait_st();
                 }
-                l = l * alpha + sum;
-                m = mnew;
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     st_shared_v4(sPb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
                                  pk[4 * j + 2], pk[4 * j + 3]);
+                l = l * alpha + (sum0 + sum1);
+                m = mnew;
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 named_bar(2, 128);

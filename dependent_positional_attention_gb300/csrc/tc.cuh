@@ -175,5 +175,42 @@ __device__ __forceinline__ void gemm_128x128x128(uint32_t d_tmem, uint32_t a_bas
     }
 }
 
+// Low / high 32-bit words of an SW128 descriptor for a tile at `saddr`:
+// K-major (leading offset unused) or MN-major (leading offset = 16 KB, the
+// distance between the two 64-column sub-tiles of a 128-row tile).  The high
+// word holds the 1024-byte stride, the version and the swizzle mode.  A
+// shared address is below 2^18, so adding (byte offset >> 4) to the low word
+// never carries out of the 14-bit start-address field.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, bool mn_major) {
+    return ((saddr >> 4) & 0x3FFFu) | ((mn_major ? (16384u >> 4) : 1u) << 16);
+}
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+__device__ __forceinline__ void mma_bf16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 ad, {%1, %5};\n\t"
+        "mov.b64 bd, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        : "memory");
+}
+
+// gemm_128x128x128 with precomputed descriptor low words (a_lo K-major;
+// b_lo K-major or MN-major per B_MN).
+template <bool B_MN>
+__device__ __forceinline__ void gemm128_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                           bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(128, 128, false, B_MN);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+        const uint32_t boff = B_MN ? (uint32_t)(kk * 128) : aoff;
+        mma_bf16_lohi(d_tmem, a_lo + aoff, b_lo + boff, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
 }  // namespace tc
 }  // namespace path
