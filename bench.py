@@ -38,11 +38,12 @@ CHUNK = 128
 
 def prefill_flops(B, H, L, d, C=CHUNK):
     """Algorithmic FLOPs: QK^T + PV over the causal triangle (2 d L^2 per head),
-    the carried-query update (two C x C x d GEMMs per off-diagonal chunk pair
-    except the last: 4 C^2 d (N-1)(N-2)/2), and the chunk UT transform
-    (16 L C d).  Returns (scan_flops, prep_flops)."""
+    the carried-query update (one C x d x d product with the chunk's d x d
+    transition matrix per off-diagonal chunk pair except the last:
+    2 C d^2 (N-1)(N-2)/2), and the chunk UT transform (16 L C d).
+    Returns (scan_flops, prep_flops)."""
     N = math.ceil(L / C)
-    scan = (2 * d * L * L + 4 * C * C * d * (N - 1) * (N - 2) / 2) * B * H
+    scan = (2 * d * L * L + 2 * C * d * d * (N - 1) * (N - 2) / 2) * B * H
     prep = 16 * L * C * d * B * H
     return scan, prep
 

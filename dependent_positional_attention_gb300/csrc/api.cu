@@ -235,7 +235,7 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
         ta.beta = beta;
         ta.Qh = at<char>(workspace, p.off_Qh);
         ta.Kh = at<char>(workspace, p.off_Kh);
-        ta.Wt = at<char>(workspace, p.off_Wt);
+        ta.Pm = at<char>(workspace, p.off_Wt);  // the bf16 path keeps the chunk product here
         ta.Sd = at<float>(workspace, p.off_Sd);
         ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.err = error_flag_ptr();
@@ -283,8 +283,7 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
         const bool enc =
             encode_tmap_bf16_3d(&maps.qh, Qh, 128, p.Lp, p.BH, 64, 128) &&
             encode_tmap_bf16_3d(&maps.kh, Kh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&maps.wt, Wt, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&maps.pm, Wt, 128, p.Lp, p.BH, 64, 128) &&
             encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         FlashTcArgs ta;

@@ -68,8 +68,8 @@ cudaError_t launch_kcache_sweep(const KcacheArgs &a, cudaStream_t st);
 // Tensor-core scan (bf16, head_dim 128, chunk 128).  Maps: 3-D bf16 tensors
 // [BH][rows][128] in 64 x 128 boxes with 128-byte swizzle.
 struct FlashTcMaps {
-    CUtensorMap qh, kh, wt;  // workspace, rows = Lp
-    CUtensorMap w, v;        // inputs, rows = L
+    CUtensorMap qh, kh, pm;  // workspace, rows = Lp (pm: per chunk a 128 x 128 matrix)
+    CUtensorMap v;           // input, rows = L
 };
 
 struct FlashTcArgs {
@@ -92,7 +92,7 @@ struct PrepTcMaps {
 
 struct PrepTcArgs {
     const float *beta;
-    void *Qh, *Kh, *Wt;
+    void *Qh, *Kh, *Pm;  // Pm: per chunk the 128 x 128 chunk product I - W^T T W
     float *Sd;
     int BH, L, Lp, N;
     uint32_t *err;

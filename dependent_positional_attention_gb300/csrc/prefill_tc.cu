@@ -6,25 +6,27 @@
 // within-chunk logits Sd from the prep kernel; for every earlier chunk c the
 // carried query rows Qt (which start as the boundary-adjusted rows Qh_b) give
 //     S_c = Qt Kh_c^T            (logits against boundary-adjusted keys)
-//     X_c = Qt W_c^T,  Qt <- Qt - X_c Wt_c     (apply the chunk product)
+//     Qt <- Qt Pm_c              (chunk product, Pm_c = I - W_c^T T_c W_c)
 //     O  += softmax-weights(S_c) V_c           (online softmax)
-// All four contractions are 128 x 128 x 128 bf16 MMAs with fp32 accumulation
-// in tensor memory.  Qt keeps an fp32 master copy in TMEM (the accumulator of
-// the update MMA); only its bf16 shadow in shared memory feeds the next MMAs.
+// Each contraction is a 128 x 128 x 128 bf16 MMA with fp32 accumulation in
+// tensor memory; the carried rows live in shared memory as bf16 (the A
+// operand of the next MMAs).  Applying the whole chunk product as one d x d
+// matrix takes one MMA per chunk instead of two (Qt W^T, then X Wt) and
+// re-rounds the carried rows once per chunk rather than rounding a
+// correction term of their own size.
 //
 // One CTA per SM (persistent), tiles ordered by decreasing work.  Warp roles:
-//   warps 0-3   carried-query warpgroup: X -> -X bf16 (A operand of the
-//               update), Qt fp32 -> bf16 shadow, Qt initialisation
+//   warps 0-3   carried-query warpgroup: Qt Pm_c (TMEM, fp32) -> bf16 shadow
 //   warps 4-7   softmax warpgroup: logits, online softmax with lazy rescale
 //               of O, P -> bf16, epilogue (out, lse)
-//   warp 8      TMA producer: Qh_b, then a 4-slot ring of W_c, Kh_c, Wt_c, V
+//   warp 8      TMA producer: Qh_b, then a 5-slot ring of Pm_c, Kh_c, V
 //   warp 9      MMA issuer (one thread) and TMEM owner; warps 10-11 idle
 // Registers are rebalanced at start (setmaxnreg): the producer/MMA group
 // drops to 120 per thread, the two compute groups rise to 192 (the launch's
 // 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512).
-// MMA issue order per step c: X_c, S_c, update_c, PV_{c+1}; the PV of a chunk
-// runs one step late so the softmax has a full step of slack.
-// TMEM columns: [0,128) Qt fp32, [128,256) X, [256,384) S, [384,512) O.
+// MMA issue order per step c: U_c = Qt Pm_c (the critical chain), S_c,
+// PV_{c+1}; the PV of a chunk runs one step late so the softmax has a full
+// step of slack.  TMEM columns: [0,128) U, [256,384) S, [384,512) O.
 // Every wait is bounded; on timeout the kernel sets the device error flag,
 // drains its outstanding copies and MMAs, frees TMEM and exits.
 
@@ -36,24 +38,23 @@ namespace path {
 namespace {
 
 constexpr int kD = 128, kC = 128;
-constexpr int kSlots = 4;
+constexpr int kSlots = 5;
 constexpr int kTileBytes = kC * kD * 2;  // 32 KB bf16 tile
 constexpr int kThreadsTC = 384;  // 3 warpgroups
-constexpr uint32_t kColQ = 0, kColX = 128, kColS = 256, kColO = 384;
+constexpr uint32_t kColU = 0, kColS = 256, kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // dynamic shared memory layout (offsets from a 1024-aligned base)
 constexpr int kOffQb = 0;
-constexpr int kOffXb = kOffQb + kTileBytes;
-constexpr int kOffPb = kOffXb + kTileBytes;
+constexpr int kOffPb = kOffQb + kTileBytes;
 constexpr int kOffRing = kOffPb + kTileBytes;
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
 
 struct Bars {
     uint64_t full[kSlots], empty[kSlots];
-    uint64_t qb_tma_full, qb_empty, x_full, xb_full, q_done, qb_conv_full;
+    uint64_t qb_tma_full, qb_empty, u_done, qb_free, qb_conv_full;
     uint64_t s_full, s_empty, p_full, o_done, drain;
     uint32_t tmem_base;
     int abort_word;
@@ -147,7 +148,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBar);
     const uint32_t sQb = smem_u32(smem + kOffQb);
-    const uint32_t sXb = smem_u32(smem + kOffXb);
     const uint32_t sPb = smem_u32(smem + kOffPb);
     const uint32_t sRing = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,9 +162,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         mbar_init(&bars.qb_tma_full, 1);
         mbar_init(&bars.qb_empty, 2);  // MMA commit + carried-query group
-        mbar_init(&bars.x_full, 1);
-        mbar_init(&bars.xb_full, 1);
-        mbar_init(&bars.q_done, 1);
+        mbar_init(&bars.u_done, 1);
+        mbar_init(&bars.qb_free, 1);
         mbar_init(&bars.qb_conv_full, 1);
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.s_empty, 1);
@@ -189,12 +188,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (lane == 0) {
             tc::prefetch_tmap(&maps.qh);
             tc::prefetch_tmap(&maps.kh);
-            tc::prefetch_tmap(&maps.wt);
-            tc::prefetch_tmap(&maps.w);
+            tc::prefetch_tmap(&maps.pm);
             tc::prefetch_tmap(&maps.v);
             int slot = 0;
             uint32_t ph = 0, qe_ph = 0;
-            int last_par[kSlots] = {-1, -1, -1, -1};
+            int last_par[kSlots] = {-1, -1, -1, -1, -1};
             int q_last_par = -1;
             uint32_t q_loads = 0;
             bool ok = true;
@@ -225,9 +223,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     q_last_par = (int)(q_loads++ & 1);
                 }
                 for (int c = b - 1; c >= 0 && ok; --c) {
-                    if (c >= 1) ok = ok && load(&maps.w, c * kC, bh);
+                    if (c >= 1) ok = ok && load(&maps.pm, c * kC, bh);
                     ok = ok && load(&maps.kh, c * kC, bh);
-                    if (c >= 1) ok = ok && load(&maps.wt, c * kC, bh);
                     ok = ok && load(&maps.v, (c + 1) * kC, bh);
                 }
                 ok = ok && load(&maps.v, 0, bh);
@@ -244,8 +241,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int slot = 0;
-            uint32_t ph = 0, qt_ph = 0, qc_ph = 0, xb_ph = 0, se_ph = 0, pf_ph = 0;
-            const uint32_t qb_lo = tc::desc_lo(sQb, false), xb_lo = tc::desc_lo(sXb, false);
+            uint32_t ph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0, pf_ph = 0;
+            const uint32_t qb_lo = tc::desc_lo(sQb, false);
             const uint32_t pb_lo = tc::desc_lo(sPb, false);
             bool ok = true;
             auto take = [&](uint32_t &addr) -> bool {
@@ -285,10 +282,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     tc::fence_after_sync();
                     uint32_t addr;
                     if (c >= 1) {
+                        // carried rows through the chunk product: U = Qt Pm_c
                         if (!(ok = take(addr))) break;
-                        tc::gemm128_lo<false>(tmem + kColX, qb_lo, tc::desc_lo(addr, false), false);
+                        tc::gemm128_lo<true>(tmem + kColU, qb_lo, tc::desc_lo(addr, true), false);
                         release();
-                        tc::mma_commit(&bars.x_full);
+                        tc::mma_commit(&bars.u_done);
                     }
                     if (!(ok = take(addr))) break;
                     if (!(ok = mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim))) break;
@@ -297,16 +295,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     tc::gemm128_lo<false>(tmem + kColS, qb_lo, tc::desc_lo(addr, false), false);
                     release();
                     tc::mma_commit(&bars.s_full);
-                    if (c == 0) tc::mma_commit(&bars.qb_empty);
-                    if (c >= 1) {
-                        if (!(ok = take(addr))) break;
-                        if (!(ok = mbar_wait(&bars.xb_full, xb_ph, a.err, abort_word, lim))) break;
-                        xb_ph ^= 1;
-                        tc::fence_after_sync();
-                        tc::gemm128_lo<true>(tmem + kColQ, xb_lo, tc::desc_lo(addr, true), true);
-                        release();
-                        tc::mma_commit(&bars.q_done);
-                    }
+                    // Qt's shadow is free once S_c (its last reader) completes
+                    tc::mma_commit(c >= 1 ? &bars.qb_free : &bars.qb_empty);
                     ok = pv(c + 1 != b);
                 }
                 ok = ok && pv(b != 0);
@@ -324,7 +314,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t xf_ph = 0, qd_ph = 0, qt_ph = 0;
+        uint32_t ud_ph = 0, qf_ph = 0, qt_ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
             const int b = tile_of(t, a.BH, a.N).b;
@@ -332,58 +322,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             ok = group_all(1, 128, mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim));
             if (!ok) break;
             qt_ph ^= 1;
-            // fp32 master of the carried rows starts as Qh_b (no update for b == 1)
-            if (b >= 2) {
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 u = ld_shared_v4(sQb + tc::swz_off(r, cc * 4 + q, kC));
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[e]);
-                            float2 f = __bfloat1622float2(h);
-                            v[q * 8 + 2 * e] = __float_as_uint(f.x);
-                            v[q * 8 + 2 * e + 1] = __float_as_uint(f.y);
-                        }
-                    }
-                    tc::tmem_st32(lane_addr + kColQ + cc * 32, v);
-                }
-            }
             // second arrival on qb_empty (the first is the MMA commit after the
             // last S of this tile): the next Qh load waits for this group too,
             // so the Qh barrier never runs a phase ahead of it.
             named_bar(1, 128);
             if (threadIdx.x == 0) mbar_arrive(&bars.qb_empty);
-            __syncwarp();
-            tc::tmem_wait_st();
             for (int c = b - 1; c >= 1; --c) {
-                ok = group_all(1, 128, mbar_wait(&bars.x_full, xf_ph, a.err, abort_word, lim));
+                ok = group_all(1, 128, mbar_wait(&bars.u_done, ud_ph, a.err, abort_word, lim));
                 if (!ok) break;
-                xf_ph ^= 1;
+                ud_ph ^= 1;
                 tc::fence_after_sync();
+                uint32_t pk[64];
                 {
                     uint32_t v[128];
-                    tc::tmem_ld128(lane_addr + kColX, v);
-                    store_row_bf16(sXb, r, v, -1.f);
+                    tc::tmem_ld128(lane_addr + kColU, v);
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        pk[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
                 }
-                tc::fence_proxy_async();
                 tc::fence_before_sync();
-                named_bar(1, 128);
-                if (threadIdx.x == 0) mbar_arrive(&bars.xb_full);
-                ok = group_all(1, 128, mbar_wait(&bars.q_done, qd_ph, a.err, abort_word, lim));
+                ok = group_all(1, 128, mbar_wait(&bars.qb_free, qf_ph, a.err, abort_word, lim));
                 if (!ok) break;
-                qd_ph ^= 1;
-                tc::fence_after_sync();
-                {
-                    uint32_t v[128];
-                    tc::tmem_ld128(lane_addr + kColQ, v);
-                    store_row_bf16(sQb, r, v, 1.f);
-                }
+                qf_ph ^= 1;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    st_shared_v4(sQb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
+                                 pk[4 * j + 2], pk[4 * j + 3]);
                 tc::fence_proxy_async();
-                tc::fence_before_sync();
                 named_bar(1, 128);
                 if (threadIdx.x == 0) mbar_arrive(&bars.qb_conv_full);
             }

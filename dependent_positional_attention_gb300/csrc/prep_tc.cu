@@ -9,6 +9,9 @@
 //   Qh = Q - (M_le * Q W^T) Wt                 (boundary-adjusted queries)
 //   Kh = K - Y W                               (boundary-adjusted keys)
 //   Sd = Q K^T - (M_le * Q W^T) Y^T            (within-chunk logits)
+//   Pm = I - W^T Wt                            (chunk product H_first...H_last,
+//                                               as the d x d matrix applied to
+//                                               carried query rows: q <- q Pm)
 // with M_le[r][s] = s <= r and M_gt[r][s] = s > r.  Nine 128 x 128 x 128
 // contractions run as tcgen05 MMAs (bf16 operands, fp32 accumulation in
 // TMEM); T is solved in fp32 on the CUDA cores by forward substitution, two
@@ -20,9 +23,10 @@
 //   P3 solve T (fp32 smem)
 //   P4 T -> bf16 tile, -(M_le*QW) -> bf16 tile, (M_gt*KW) -> bf16 tile
 //   P5 MMA Wt = T W -> cols 0, Y = (M_gt*KW) T^T -> cols 256
-//   P6 Wt -> bf16 tile + workspace, Y -> bf16 tile
-//   P7 MMA -(M_le*QW) Wt -> cols 128, Y W -> cols 0, += -(M_le*QW) Y^T -> cols 384
-//   P8 Qh, Kh, Sd -> workspace
+//   P6 Wt -> bf16 tile, Y -> bf16 tile
+//   P7 MMA -(M_le*QW) Wt -> cols 128, Y W -> cols 0, += -(M_le*QW) Y^T -> cols 384,
+//      W^T Wt -> cols 256
+//   P8 Qh, Kh, Sd, Pm -> workspace
 
 #include "common.cuh"
 #include "kernels.h"
@@ -322,8 +326,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (!mma_sync()) break;
         // ---------------------------------------------------------------- P6
         {
-            __nv_bfloat16 *wt_out =
-                static_cast<__nv_bfloat16 *>(a.Wt) + ((size_t)bh * a.Lp + c0 + r) * kC;
             const uint32_t src = (half == 0) ? kColA : kColC;
             const uint32_t dst = (half == 0) ? sWt : sY;
 #pragma unroll
@@ -331,17 +333,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 uint32_t v[32];
                 tc::tmem_ld32(tmem + lane_off + src + cc * 32, v);
                 tile_store32(dst, r, cc, v, [](int, float x) { return x; });
-                if (half == 0) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 u;
-                        u.x = pack2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
-                        u.y = pack2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
-                        u.z = pack2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
-                        u.w = pack2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
-                        *reinterpret_cast<uint4 *>(wt_out + cc * 32 + q * 8) = u;
-                    }
-                }
             }
         }
         tc::fence_proxy_async();
@@ -353,6 +344,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             tc::gemm_128x128x128(tmem + kColB, sQm, sWt, true, false);  // -(M_le*QW) Wt
             tc::gemm_128x128x128(tmem + kColA, sY, sW, true, false);    // Y W
             tc::gemm_128x128x128(tmem + kColD, sQm, sY, false, true);   // QK^T - (M_le*QW) Y^T
+            tc::gemm128_lo2<true, true>(tmem + kColC, tc::desc_lo(sW, true),
+                                        tc::desc_lo(sWt, true), false);  // W^T Wt
         }
         if (!mma_sync()) break;
         // ---------------------------------------------------------------- P8
@@ -380,6 +373,27 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     u.w = pack2(x[6] + sign * __uint_as_float(v[q * 8 + 6]),
                                 x[7] + sign * __uint_as_float(v[q * 8 + 7]));
                     *reinterpret_cast<uint4 *>(dst + cc * 32 + q * 8) = u;
+                }
+            }
+            // Pm = I - W^T Wt, row r (input dimension), columns half*64 ..
+            __nv_bfloat16 *pm = static_cast<__nv_bfloat16 *>(a.Pm) + row * kC;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t v[32];
+                const int col = half * 64 + cc * 32;
+                tc::tmem_ld32(tmem + lane_off + kColC + col, v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        x[e] = ((col + q * 8 + e) == r ? 1.f : 0.f) - __uint_as_float(v[q * 8 + e]);
+                    uint4 u;
+                    u.x = pack2(x[0], x[1]);
+                    u.y = pack2(x[2], x[3]);
+                    u.z = pack2(x[4], x[5]);
+                    u.w = pack2(x[6], x[7]);
+                    *reinterpret_cast<uint4 *>(pm + col + q * 8) = u;
                 }
             }
             float *sd = a.Sd + (((size_t)bh * a.N + chunk) * kC + r) * kC;

@@ -198,6 +198,22 @@ __device__ __forceinline__ void mma_bf16_lohi(uint32_t d_tmem, uint32_t a_lo, ui
         : "memory");
 }
 
+// gemm_128x128x128 with precomputed descriptor low words; A_MN / B_MN select
+// MN-major operands (rows = K; each row holds 128 M or N values as two
+// 64-column sub-tiles 16 KB apart), else K-major.
+template <bool B_MN, bool A_MN>
+__device__ __forceinline__ void gemm128_lo2(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                            bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(128, 128, A_MN, B_MN);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t koff = (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+        const uint32_t aoff = A_MN ? (uint32_t)(kk * 128) : koff;
+        const uint32_t boff = B_MN ? (uint32_t)(kk * 128) : koff;
+        mma_bf16_lohi(d_tmem, a_lo + aoff, b_lo + boff, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
 // gemm_128x128x128 with precomputed descriptor low words (a_lo K-major;
 // b_lo K-major or MN-major per B_MN).
 template <bool B_MN>
