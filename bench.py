@@ -138,9 +138,9 @@ def timed_prefill(x, steps, warmup, ws, fox=False, sampler=None):
     stream = torch.cuda.current_stream()
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
-    ws_t = pa.path_attn_prefill_prep(q, k, w, beta, log_f=log_f)
+    ws_t = pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f)
     for _ in range(warmup):
-        pa.path_attn_prefill_prep(q, k, w, beta, log_f=log_f, workspace=ws_t)
+        pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f, workspace=ws_t)
         pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     barrier(ws)
@@ -152,7 +152,7 @@ def timed_prefill(x, steps, warmup, ws, fox=False, sampler=None):
     t0.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
-        pa.path_attn_prefill_prep(q, k, w, beta, log_f=log_f, workspace=ws_t)
+        pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f, workspace=ws_t)
         ev[i][1].record(stream)
         pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
         ev[i][2].record(stream)

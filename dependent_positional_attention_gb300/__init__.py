@@ -82,7 +82,7 @@ def load_library(path: str | None = None):
         lib.path_attn_prefill_workspace_size.restype = _SZ
         lib.path_attn_prefill_fwd.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                               _VP, _SZ, _VP]
-        lib.path_attn_prefill_prep.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
+        lib.path_attn_prefill_prep.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
         lib.path_attn_prefill_scan.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
         lib.path_attn_decode_workspace_size.argtypes = [dd]
         lib.path_attn_decode_workspace_size.restype = _SZ
@@ -188,7 +188,7 @@ def path_attn_prefill_fwd(q, k, v, w, beta, log_f=None, out=None, lse=None, scal
     return out, lse
 
 
-def path_attn_prefill_prep(q, k, w, beta, log_f=None, scale=None, chunk=0, workspace=None,
+def path_attn_prefill_prep(q, k, v, w, beta, log_f=None, scale=None, chunk=0, workspace=None,
                           stream=None):
     """Stage 1 of the prefill (see path_attn_prefill_prep in include/path_attn.h).
     Returns the workspace tensor to pass to path_attn_prefill_scan."""
@@ -199,7 +199,7 @@ def path_attn_prefill_prep(q, k, w, beta, log_f=None, scale=None, chunk=0, works
         workspace = torch.empty(max(path_attn_prefill_workspace_size(desc), 16),
                                 device=q.device, dtype=torch.uint8)
     _check(lib.path_attn_prefill_prep(
-        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(w), _ptr(beta), _ptr(log_f),
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return workspace
 

@@ -201,15 +201,15 @@ size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc) {
 }
 
 path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void *q,
-                                     const void *k, const void *w, const float *beta,
-                                     const float *log_f, void *workspace,
+                                     const void *k, const void *v, const void *w,
+                                     const float *beta, const float *log_f, void *workspace,
                                      size_t workspace_bytes, path_stream_t stream) {
     PrefillPlan p;
     path_status_t s = plan_prefill(desc, &p);
     if (s != PATH_OK) return s;
-    const void *req[] = {q, k, w, beta, workspace};
-    const char *names[] = {"q", "k", "w", "beta", "workspace"};
-    for (int i = 0; i < 5; ++i) {
+    const void *req[] = {q, k, v, w, beta, workspace};
+    const char *names[] = {"q", "k", "v", "w", "beta", "workspace"};
+    for (int i = 0; i < 6; ++i) {
         if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
         if (!aligned16(req[i]))
             return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
@@ -229,14 +229,20 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
         PrepTcMaps maps;
         const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.L, p.BH, 64, 128) &&
                          encode_tmap_bf16_3d(&maps.k, k, 128, p.L, p.BH, 64, 128) &&
-                         encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128);
+                         encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         PrepTcArgs ta;
         ta.beta = beta;
+        ta.F = log_f ? at<float>(workspace, p.off_F) : nullptr;
+        ta.scale = desc->scale;
         ta.Qh = at<char>(workspace, p.off_Qh);
         ta.Kh = at<char>(workspace, p.off_Kh);
         ta.Pm = at<char>(workspace, p.off_Wt);  // the bf16 path keeps the chunk product here
-        ta.Sd = at<float>(workspace, p.off_Sd);
+        // the bf16 path keeps each chunk's own attention block where the fp32
+        // path keeps its within-chunk logits
+        ta.OD = at<__nv_bfloat16>(workspace, p.off_Sd);
+        ta.LSD = at<float>(workspace, p.off_Sd + (size_t)p.BH * p.Lp * 128 * 2);
         ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
@@ -287,7 +293,10 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
             encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         FlashTcArgs ta;
-        ta.Sd = Sd; ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
+        ta.OD = reinterpret_cast<const __nv_bfloat16 *>(Sd);
+        ta.LSD = reinterpret_cast<const float *>(reinterpret_cast<const char *>(Sd) +
+                                                 (size_t)p.BH * p.Lp * 128 * 2);
+        ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
         ta.scale = desc->scale; ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
@@ -311,7 +320,7 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
     if (!aligned16(v)) return fail(PATH_ERR_INVALID_ARG, "v is not 16-byte aligned");
     if (!aligned16(out)) return fail(PATH_ERR_INVALID_ARG, "out is not 16-byte aligned");
     if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
-    path_status_t s = path_attn_prefill_prep(desc, q, k, w, beta, log_f, workspace,
+    path_status_t s = path_attn_prefill_prep(desc, q, k, v, w, beta, log_f, workspace,
                                              workspace_bytes, stream);
     if (s != PATH_OK) return s;
     return path_attn_prefill_scan(desc, w, v, log_f, out, lse, workspace, workspace_bytes, stream);

@@ -73,7 +73,9 @@ struct FlashTcMaps {
 };
 
 struct FlashTcArgs {
-    const float *Sd, *F;
+    const __nv_bfloat16 *OD;  // [BH][Lp][128] each chunk's own attention output (prep)
+    const float *LSD;         // [BH][Lp] its log-sum-exp
+    const float *F;
     __nv_bfloat16 *out;
     float *lse;
     float scale;
@@ -87,13 +89,16 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
 // Tensor-core prep (bf16, head_dim 128, chunk 128): maps over the raw q, k, w
 // inputs ([BH][L][128], 64 x 128 boxes, 128-byte swizzle).
 struct PrepTcMaps {
-    CUtensorMap q, k, w;
+    CUtensorMap q, k, w, v;
 };
 
 struct PrepTcArgs {
     const float *beta;
+    const float *F;      // FoX prefix sums [BH][Lp] (natural log units) or null
+    float scale;
     void *Qh, *Kh, *Pm;  // Pm: per chunk the 128 x 128 chunk product I - W^T T W
-    float *Sd;
+    __nv_bfloat16 *OD;   // [BH][Lp][128] each chunk's own attention output, normalised
+    float *LSD;          // [BH][Lp] its log-sum-exp (natural log)
     int BH, L, Lp, N;
     uint32_t *err;
 };

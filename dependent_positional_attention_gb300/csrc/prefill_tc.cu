@@ -2,9 +2,11 @@
 //
 // Blockwise algorithm of the PaTH Attention summary (section "3. 효율적인
 // 학습 및 추론", FlashAttention-style algorithm): per query chunk b (128 rows)
-// the key chunks are visited right to left.  The diagonal chunk uses the
-// within-chunk logits Sd from the prep kernel; for every earlier chunk c the
-// carried query rows Qt (which start as the boundary-adjusted rows Qh_b) give
+// the key chunks are visited right to left.  The prep kernel has already
+// attended each chunk to itself (normalised output OD and log-sum-exp LSD);
+// the online softmax starts from that state, and for every earlier chunk c
+// the carried query rows Qt (which start as the boundary-adjusted rows Qh_b)
+// give
 //     S_c = Qt Kh_c^T            (logits against boundary-adjusted keys)
 //     Qt <- Qt Pm_c              (chunk product, Pm_c = I - W_c^T T_c W_c)
 //     O  += softmax-weights(S_c) V_c           (online softmax)
@@ -26,7 +28,8 @@
 // 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512).
 // MMA issue order per step c: U_c = Qt Pm_c (the critical chain), S_c,
 // PV_{c+1}; the PV of a chunk runs one step late so the softmax has a full
-// step of slack.  TMEM columns: [0,128) U, [256,384) S, [384,512) O.
+// step of slack.  Chunk-0 tiles need no scan: the softmax group copies the
+// prep's result.  TMEM columns: [0,128) U, [256,384) S, [384,512) O.
 // Every wait is bounded; on timeout the kernel sets the device error flag,
 // drains its outstanding copies and MMAs, frees TMEM and exits.
 
@@ -104,29 +107,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-// Writes a full 128-value fp32 row (optionally negated) as bf16 into a
-// swizzled 128-column operand tile.
-__device__ __forceinline__ void store_row_bf16(uint32_t tile, int r, const uint32_t (&v)[128],
-                                               float sign) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(sign * __uint_as_float(v[j * 8 + 2 * e]),
-                             sign * __uint_as_float(v[j * 8 + 2 * e + 1]));
-        st_shared_v4(tile + tc::swz_off(r, j, kC), w[0], w[1], w[2], w[3]);
-    }
 }
 
 struct Tile {
@@ -212,20 +192,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
                 const Tile tl = tile_of(t, a.BH, a.N);
                 const int b = tl.b, bh = tl.bh;
-                if (b >= 1) {
-                    ok = mbar_wait(&bars.qb_empty, qe_ph ^ 1, a.err, abort_word, lim);
-                    qe_ph ^= 1;
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&bars.qb_tma_full, kTileBytes);
-                    tc::tma_load_3d(smem + kOffQb, &maps.qh, 0, b * kC, bh, &bars.qb_tma_full);
-                    tc::tma_load_3d(smem + kOffQb + kTileBytes / 2, &maps.qh, 64, b * kC, bh,
-                                    &bars.qb_tma_full);
-                    q_last_par = (int)(q_loads++ & 1);
-                }
+                if (b == 0) continue;
+                ok = mbar_wait(&bars.qb_empty, qe_ph ^ 1, a.err, abort_word, lim);
+                qe_ph ^= 1;
+                if (!ok) break;
+                mbar_arrive_expect_tx(&bars.qb_tma_full, kTileBytes);
+                tc::tma_load_3d(smem + kOffQb, &maps.qh, 0, b * kC, bh, &bars.qb_tma_full);
+                tc::tma_load_3d(smem + kOffQb + kTileBytes / 2, &maps.qh, 64, b * kC, bh,
+                                &bars.qb_tma_full);
+                q_last_par = (int)(q_loads++ & 1);
                 for (int c = b - 1; c >= 0 && ok; --c) {
                     if (c >= 1) ok = ok && load(&maps.pm, c * kC, bh);
                     ok = ok && load(&maps.kh, c * kC, bh);
-                    ok = ok && load(&maps.v, (c + 1) * kC, bh);
+                    if (c < b - 1) ok = ok && load(&maps.v, (c + 1) * kC, bh);
                 }
                 ok = ok && load(&maps.v, 0, bh);
             }
@@ -257,19 +236,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     ph ^= 1;
                 }
             };
-            auto pv = [&](bool accumulate) -> bool {
+            // O already holds the chunk's own attention block (written by the
+            // softmax group), so every PV accumulates
+            auto pv = [&]() -> bool {
                 uint32_t vaddr;
                 if (!take(vaddr)) return false;
                 if (!mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim)) return false;
                 pf_ph ^= 1;
                 tc::fence_after_sync();
-                tc::gemm128_lo<true>(tmem + kColO, pb_lo, tc::desc_lo(vaddr, true), accumulate);
+                tc::gemm128_lo<true>(tmem + kColO, pb_lo, tc::desc_lo(vaddr, true), true);
                 release();
                 tc::mma_commit(&bars.o_done);
                 return true;
             };
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
                 const int b = tile_of(t, a.BH, a.N).b;
+                if (b == 0) continue;
                 for (int c = b - 1; c >= 0 && ok; --c) {
                     if (c == b - 1) {
                         ok = mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim);
@@ -297,9 +279,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     tc::mma_commit(&bars.s_full);
                     // Qt's shadow is free once S_c (its last reader) completes
                     tc::mma_commit(c >= 1 ? &bars.qb_free : &bars.qb_empty);
-                    ok = pv(c + 1 != b);
+                    if (c < b - 1) ok = pv();
                 }
-                ok = ok && pv(b != 0);
+                ok = ok && pv();
             }
             // every MMA issued so far has completed before TMEM is released
             tc::mma_commit(&bars.drain);
@@ -367,50 +349,40 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             const int b = tl.b, bh = tl.bh;
             const float *Frow = fox ? a.F + (size_t)bh * a.Lp : nullptr;
             const float fi = fox ? Frow[b * kC + r] * kLog2e : 0.f;
-            // diagonal chunk: within-chunk logits from the prep kernel
-            if (fox) bars.fsm[r] = Frow[b * kC + r] * kLog2e;
-            named_bar(2, 128);
-            float m, l;
-            {
-                const float4 *srow = reinterpret_cast<const float4 *>(
-                    a.Sd + (((size_t)bh * a.N + b) * kC + r) * kC);
-                float mx = -INFINITY;
-#pragma unroll 8
-                for (int j4 = 0; j4 < kC / 4; ++j4) {
-                    const float4 s4 = srow[j4];
-                    const float xs[4] = {s4.x, s4.y, s4.z, s4.w};
+            const int row = b * kC + r;
+            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lp + row) * kD;
+            const float lsd = a.LSD[(size_t)bh * a.Lp + row];
+            if (b == 0) {
+                // the chunk attends only to itself: the prep's result is final
+                if (row < a.L) {
+                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.L + row) * kD;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        reinterpret_cast<uint4 *>(orow)[j] = reinterpret_cast<const uint4 *>(odrow)[j];
+                    if (a.lse) a.lse[(size_t)bh * a.L + row] = lsd;
+                }
+                continue;
+            }
+            // start from the chunk's own block: O = OD (weights summing to 1
+            // against the reference m = LSD in log2 units), l = 1
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t o[32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = reinterpret_cast<const uint4 *>(odrow)[cc * 4 + q];
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * j4 + e;
-                        float v = xs[e] * sl2;
-                        if (fox) v += fi - bars.fsm[j];
-                        if (j <= r) mx = fmaxf(mx, v);
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                        o[q * 8 + 2 * e] = __float_as_uint(f.x);
+                        o[q * 8 + 2 * e + 1] = __float_as_uint(f.y);
                     }
                 }
-                m = mx;  // finite: j = r is always present
-                float sum = 0.f;
-#pragma unroll 2
-                for (int j8 = 0; j8 < kC / 8; ++j8) {
-                    const float4 s0 = srow[2 * j8], s1 = srow[2 * j8 + 1];
-                    const float xs[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                    float p[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 8 * j8 + e;
-                        float v = xs[e] * sl2;
-                        if (fox) v += fi - bars.fsm[j];
-                        p[e] = (j <= r) ? ex2(v - m) : 0.f;
-                        sum += p[e];
-                    }
-                    st_shared_v4(sPb + tc::swz_off(r, j8, kC), pack_bf16(p[0], p[1]),
-                                 pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                                 pack_bf16(p[6], p[7]));
-                }
-                l = sum;
-                tc::fence_proxy_async();
-                named_bar(2, 128);
-                if (threadIdx.x == 128) mbar_arrive(&bars.p_full);
+                tc::tmem_st32(lane_addr + kColO + cc * 32, o);
             }
+            tc::tmem_wait_st();
+            float m = lsd * kLog2e, l = 1.f;
             for (int c = b - 1; c >= 0; --c) {
                 if (fox) bars.fsm[r] = Frow[c * kC + r] * kLog2e;
                 ok = group_all(2, 128, mbar_wait(&bars.s_full, sf_ph, a.err, abort_word, lim));
@@ -465,11 +437,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     pk[2 * j4] = pack_bf16(p[0], p[1]);
                     pk[2 * j4 + 1] = pack_bf16(p[2], p[3]);
                 }
-                // previous PV done: P buffer free and O stable
-                ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
-                if (!ok) break;
-                od_ph ^= 1;
-                tc::fence_after_sync();
+                // previous PV done: P buffer free and O stable (the first step
+                // follows the previous tile's epilogue, which waited already)
+                if (c < b - 1) {
+                    ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
+                    if (!ok) break;
+                    od_ph ^= 1;
+                    tc::fence_after_sync();
+                }
                 if (rescale) {
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
@@ -499,7 +474,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             if (!ok) break;
             od_ph ^= 1;
             tc::fence_after_sync();
-            const int row = b * kC + r;
             const float inv = 1.f / l;
             __nv_bfloat16 *orow = a.out + ((size_t)bh * a.L + row) * kD;
 #pragma unroll

@@ -25,8 +25,12 @@
 //   P5 MMA Wt = T W -> cols 0, Y = (M_gt*KW) T^T -> cols 256
 //   P6 Wt -> bf16 tile, Y -> bf16 tile
 //   P7 MMA -(M_le*QW) Wt -> cols 128, Y W -> cols 0, += -(M_le*QW) Y^T -> cols 384,
-//      W^T Wt -> cols 256
-//   P8 Qh, Kh, Sd, Pm -> workspace
+//      W^T Wt -> cols 256   (the chunk's V is loaded meanwhile)
+//   P8 Qh, Kh, Pm -> workspace
+//   P9 causal softmax of the within-chunk logits (cols 384) -> P bf16 tile;
+//      MMA P V -> cols 256
+//   P10 the chunk's own attention output (normalised, bf16) and its log-sum-exp
+//      -> workspace; the scan starts every query tile from them
 
 #include "common.cuh"
 #include "kernels.h"
@@ -44,17 +48,18 @@ constexpr int kOffR1 = 3 * kTile;            // G fp32, then T bf16 | -(M_le*QW)
 constexpr int kR1Bytes = 65 * 1024;          // >= 128 * 129 * 4
 constexpr int kOffR2 = kOffR1 + kR1Bytes;    // T fp32, then KWm/Y bf16 | Wt bf16
 constexpr int kOffBar = kOffR2 + 64 * 1024;
-constexpr int kSmemP = kOffBar + 1024 + 1024;
+constexpr int kSmemP = kOffBar + 640 + 1024;
 static_assert(kC * kGs * 4 <= kR1Bytes, "G staging does not fit");
 static_assert(kSmemP <= 232448, "shared memory budget exceeded");
 constexpr uint32_t kColA = 0, kColB = 128, kColC = 256, kColD = 384;
 
 struct PBars {
-    uint64_t tma, mma;
+    uint64_t tma, mma, vbar;
     uint32_t tmem_base;
     int ok;
     float beta[kC];
 };
+static_assert(sizeof(PBars) <= 640, "barrier block too large");
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -214,6 +219,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     if (tid == 0) {
         mbar_init(&bars.tma, 1);
         mbar_init(&bars.mma, 1);
+        mbar_init(&bars.vbar, 1);
         bars.ok = 1;
         fence_mbar_init();
     }
@@ -225,7 +231,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = bars.tmem_base;
-    uint32_t ph_tma = 0, ph_mma = 0;
+    uint32_t ph_tma = 0, ph_mma = 0, ph_v = 0;
+    const float sl2 = a.scale * 1.4426950408889634f;
 
     // thread 0 waits for the MMAs committed so far; result shared by the block
     auto mma_sync = [&]() {
@@ -324,6 +331,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             tc::gemm_128x128x128(tmem + kColC, sY, sT, false, false);  // Y = KWm T^T
         }
         if (!mma_sync()) break;
+        if (tid == 0) {
+            // the chunk's values, for its own attention block, into the free T tile
+            mbar_arrive_expect_tx(&bars.vbar, kTile);
+            tc::tma_load_3d(smem + kOffR1, &maps.v, 0, c0, bh, &bars.vbar);
+            tc::tma_load_3d(smem + kOffR1 + kTile / 2, &maps.v, 64, c0, bh, &bars.vbar);
+        }
         // ---------------------------------------------------------------- P6
         {
             const uint32_t src = (half == 0) ? kColA : kColC;
@@ -396,18 +409,79 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     *reinterpret_cast<uint4 *>(pm + col + q * 8) = u;
                 }
             }
-            float *sd = a.Sd + (((size_t)bh * a.N + chunk) * kC + r) * kC;
+        }
+        // ---------------------------------------------------------------- P9
+        // causal softmax of the within-chunk logits, rows r, columns half*64..
+        float m_row, l_row;
+        {
+            // per-row partial max / sum of the two column halves, in the R2
+            // region (its Y / Wt tiles were last read by the P7 MMAs)
+            float(*red)[2][kC] = reinterpret_cast<float(*)[2][kC]>(smem + kOffR2);
+            const float *F = a.F ? a.F + (size_t)bh * a.Lp + c0 : nullptr;
+            const float fi = F ? F[r] * 1.4426950408889634f : 0.f;
+            uint32_t v[64];
+            tc::tmem_ld64(tmem + lane_off + kColD + half * 64, v);
+            float mx = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t v[32];
-                const int col = half * 64 + cc * 32;
-                tc::tmem_ld32(tmem + lane_off + kColD + col, v);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4 *>(sd + col + q * 4) =
-                        make_float4(__uint_as_float(v[q * 4]), __uint_as_float(v[q * 4 + 1]),
-                                    __uint_as_float(v[q * 4 + 2]), __uint_as_float(v[q * 4 + 3]));
+            for (int i = 0; i < 64; ++i) {
+                const int j = half * 64 + i;
+                float x = __uint_as_float(v[i]) * sl2;
+                if (F) x += fi - F[j] * 1.4426950408889634f;
+                x = (j <= r) ? x : -INFINITY;
+                v[i] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
             }
+            red[0][half][r] = mx;
+            __syncthreads();
+            m_row = fmaxf(red[0][0][r], red[0][1][r]);  // finite: column r is unmasked
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x = __uint_as_float(v[q * 8 + e]);
+                    float y;
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x - m_row));
+                    p[e] = (x == -INFINITY) ? 0.f : y;
+                    sum += p[e];
+                }
+                sts128(sQm + tc::swz_off(r, half * 8 + q, kC), pack2(p[0], p[1]), pack2(p[2], p[3]),
+                       pack2(p[4], p[5]), pack2(p[6], p[7]));
+            }
+            red[1][half][r] = sum;
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+            l_row = red[1][0][r] + red[1][1][r];
+        }
+        if (tid == 0) {
+            if (!mbar_wait(&bars.vbar, ph_v, a.err, nullptr, kWaitLimitNs)) {
+                bars.ok = 0;
+            } else {
+                tc::gemm_128x128x128(tmem + kColC, sQm, sT, true, false);  // P V
+            }
+        }
+        ph_v ^= 1;
+        if (!mma_sync()) break;
+        // ---------------------------------------------------------------- P10
+        {
+            const size_t row = (size_t)bh * a.Lp + c0 + r;
+            __nv_bfloat16 *od = a.OD + row * kC + half * 64;
+            const float inv = 1.f / l_row;
+            uint32_t v[64];
+            tc::tmem_ld64(tmem + lane_off + kColC + half * 64, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 u;
+                u.x = pack2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
+                u.y = pack2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
+                u.z = pack2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
+                u.w = pack2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
+                *reinterpret_cast<uint4 *>(od + q * 8) = u;
+            }
+            if (half == 0) a.LSD[row] = (m_row + log2f(l_row)) * 0.6931471805599453f;
         }
         tc::fence_before_sync();
         __syncthreads();  // Q, K tiles and TMEM free before the next chunk's loads

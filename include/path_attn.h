@@ -100,8 +100,8 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
  *
  * path_attn_prefill_prep: per chunk, the UT transform of the chunk's
  * transitions and everything derived from it (boundary-adjusted rows, the
- * compact chunk product, within-chunk logits), plus the FoX prefix sums when
- * log_f != NULL; written into the workspace.
+ * chunk product, the chunk's own causal attention block), plus the FoX
+ * prefix sums when log_f != NULL; written into the workspace.
  *
  * path_attn_prefill_scan: the right-to-left blockwise scan with online
  * softmax over the prep results; w and v are the same tensors given to the
@@ -109,8 +109,8 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
  * prep call (only its presence is used here).
  */
 path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void *q,
-                                     const void *k, const void *w, const float *beta,
-                                     const float *log_f, void *workspace,
+                                     const void *k, const void *v, const void *w,
+                                     const float *beta, const float *log_f, void *workspace,
                                      size_t workspace_bytes, path_stream_t stream);
 path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void *w,
                                      const void *v, const float *log_f, void *out, float *lse,
