@@ -60,6 +60,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         : "memory");
 }
 
+// One poll of the phase with the given parity, without a suspend-time hint
+// (returns at once).
+__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// One wait of up to ~1 ms (the hardware may suspend the thread meanwhile).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -72,14 +87,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on the phase with the given parity.  Gives up after
-// `limit_ns` of device time, sets the error flag and the CTA abort word, and
-// returns false.  Also returns false at once when another role of the CTA has
-// already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err_flag,
-                                          volatile int *abort_word, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer_ns();
+// Slow path of mbar_wait: polls with the suspend hint and reads the global
+// timer, which costs a few hundred cycles, so it is entered only after a
+// first plain poll has failed.
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, uint32_t *err_flag,
+                                            volatile int *abort_word, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort_word && *abort_word) return false;
@@ -89,6 +102,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
             return false;
         }
     }
+}
+
+// Bounded wait on the phase with the given parity.  Gives up after
+// `limit_ns` of device time, sets the error flag and the CTA abort word, and
+// returns false.  Also returns false once another role of the CTA has
+// aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err_flag,
+                                          volatile int *abort_word, uint64_t limit_ns) {
+    if (mbar_poll(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err_flag, abort_word, limit_ns);
 }
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of device time
