@@ -230,18 +230,23 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
         const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.L, p.BH, 64, 128) &&
                          encode_tmap_bf16_3d(&maps.k, k, 128, p.L, p.BH, 64, 128) &&
                          encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128) &&
-                         encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
+                         encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.qh, at<char>(workspace, p.off_Qh), 128, p.Lp,
+                                             p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.kh, at<char>(workspace, p.off_Kh), 128, p.Lp,
+                                             p.BH, 64, 128) &&
+                         // the bf16 path keeps the chunk product where the fp32
+                         // path keeps Wt, and each chunk's own attention block
+                         // where the fp32 path keeps its within-chunk logits
+                         encode_tmap_bf16_3d(&maps.pm, at<char>(workspace, p.off_Wt), 128, p.Lp,
+                                             p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.od, at<char>(workspace, p.off_Sd), 128, p.Lp,
+                                             p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         PrepTcArgs ta;
         ta.beta = beta;
         ta.F = log_f ? at<float>(workspace, p.off_F) : nullptr;
         ta.scale = desc->scale;
-        ta.Qh = at<char>(workspace, p.off_Qh);
-        ta.Kh = at<char>(workspace, p.off_Kh);
-        ta.Pm = at<char>(workspace, p.off_Wt);  // the bf16 path keeps the chunk product here
-        // the bf16 path keeps each chunk's own attention block where the fp32
-        // path keeps its within-chunk logits
-        ta.OD = at<__nv_bfloat16>(workspace, p.off_Sd);
         ta.LSD = at<float>(workspace, p.off_Sd + (size_t)p.BH * p.Lp * 128 * 2);
         ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.err = error_flag_ptr();

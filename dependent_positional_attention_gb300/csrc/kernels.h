@@ -86,19 +86,21 @@ struct FlashTcArgs {
 cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
                             cudaStream_t st);
 
-// Tensor-core prep (bf16, head_dim 128, chunk 128): maps over the raw q, k, w
-// inputs ([BH][L][128], 64 x 128 boxes, 128-byte swizzle).
+// Tensor-core prep (bf16, head_dim 128, chunk 128): maps over the raw q, k, w,
+// v inputs ([BH][L][128]) and over the Qh, Kh, Pm, OD outputs ([BH][Lp][128]),
+// all with 64 x 128 boxes and the 128-byte swizzle.
 struct PrepTcMaps {
     CUtensorMap q, k, w, v;
+    CUtensorMap qh, kh, pm, od;
 };
 
 struct PrepTcArgs {
     const float *beta;
     const float *F;      // FoX prefix sums [BH][Lp] (natural log units) or null
     float scale;
-    void *Qh, *Kh, *Pm;  // Pm: per chunk the 128 x 128 chunk product I - W^T T W
-    __nv_bfloat16 *OD;   // [BH][Lp][128] each chunk's own attention output, normalised
-    float *LSD;          // [BH][Lp] its log-sum-exp (natural log)
+    // Qh, Kh, Pm (per chunk the 128 x 128 product I - W^T T W) and OD (each
+    // chunk's own attention output, normalised) are written through the maps.
+    float *LSD;          // [BH][Lp] log-sum-exp of the OD rows (natural log)
     int BH, L, Lp, N;
     uint32_t *err;
 };

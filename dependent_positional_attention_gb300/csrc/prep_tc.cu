@@ -42,14 +42,13 @@ namespace {
 constexpr int kC = 128;
 constexpr int kTile = kC * kC * 2;  // bf16 128 x 128 operand tile
 constexpr int kThreadsP = 256;
-constexpr int kGs = kC + 1;  // fp32 G row stride (conflict-free row writes and row reads)
 constexpr int kOffQ = 0, kOffK = kTile, kOffW = 2 * kTile;
 constexpr int kOffR1 = 3 * kTile;            // G fp32, then T bf16 | -(M_le*QW) bf16
-constexpr int kR1Bytes = 65 * 1024;          // >= 128 * 129 * 4
+constexpr int kR1Bytes = 64 * 1024;
 constexpr int kOffR2 = kOffR1 + kR1Bytes;    // T fp32, then KWm/Y bf16 | Wt bf16
 constexpr int kOffBar = kOffR2 + 64 * 1024;
 constexpr int kSmemP = kOffBar + 640 + 1024;
-static_assert(kC * kGs * 4 <= kR1Bytes, "G staging does not fit");
+static_assert(kC * kC * 4 <= kR1Bytes, "G staging does not fit");
 static_assert(kSmemP <= 232448, "shared memory budget exceeded");
 constexpr uint32_t kColA = 0, kColB = 128, kColC = 256, kColD = 384;
 
@@ -111,89 +110,147 @@ __device__ __forceinline__ void tile_load8(uint32_t tile, int r, int j, float (&
     }
 }
 
-// Linv = (I + A)^{-1} for A[i][k] = beta_i G[i][k] (k < i), by blocks:
-// invert the eight 16 x 16 diagonal blocks by forward substitution, then
-// merge sibling blocks (sizes 16, 32, 64) with X21 = -Inv(B2) A21 Inv(B1).
-// G: fp32 [128][kGs] (symmetric, only k < i used).  Tf: fp32 [128][128]
-// receives Linv, zero above the diagonal.  The intermediate A21 Inv(B1) of a
-// merge is parked in the upper-right block of the pair (zero afterwards).
-// 256 threads; each merge step gives every active thread one 4 x 4 tile.
-__device__ __forceinline__ void unit_lower_inverse(const float *G, float *Tf, const float *beta,
-                                                   int tid) {
-    for (int e = tid; e < kC * kC / 4; e += kThreadsP)
-        reinterpret_cast<float4 *>(Tf)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+// fp32 128 x 128 matrices in shared memory (G, then T): row stride 128 floats,
+// the 16-byte groups of row r permuted by group ^ sw_f(r).  sw_f takes eight
+// different values on eight consecutive rows (from a multiple of 8) and four
+// different values of sw_f >> 1 on four consecutive rows (from a multiple of
+// 4), so that a warp touches every bank once both when it reads an m16n8k8
+// A fragment (8 rows x 4 columns) and a B fragment (4 rows x 8 columns), and
+// when one lane per row writes one group.
+__device__ __forceinline__ int sw_f(int r) { return ((r & 3) << 1) | ((r >> 2) & 1); }
+__device__ __forceinline__ int sw(int r, int c) {
+    return r * kC + (((c >> 2) ^ sw_f(r)) << 2) + (c & 3);
+}
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// x = hi + lo with both parts tf32; hi*hi + hi*lo + lo*hi carries a product
+// to about fp32 accuracy ("3xTF32").
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc[n] += X[rows ra .. ra+15][k] * Y[k][cols cb + 8n .. +7] for k in [k_lo, k_hi),
+// X and Y fp32 in the sw layout (X's column and Y's row offsets included in
+// xc, yr); three tf32 MMAs per 16 x 8 x 8 step.
+template <int NT>
+__device__ __forceinline__ void mma3_rows(float (&acc)[NT][4], const float *X, int ra, int xc,
+                                          const float *Y, int yr, int cb, int k_lo, int k_hi,
+                                          int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(X[sw(ra + g, xc + k0 + t)], ah[0], al[0]);
+        split_tf32(X[sw(ra + g + 8, xc + k0 + t)], ah[1], al[1]);
+        split_tf32(X[sw(ra + g, xc + k0 + t + 4)], ah[2], al[2]);
+        split_tf32(X[sw(ra + g + 8, xc + k0 + t + 4)], ah[3], al[3]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            uint32_t bh[2], bl[2];
+            split_tf32(Y[sw(yr + k0 + t, cb + 8 * n + g)], bh[0], bl[0]);
+            split_tf32(Y[sw(yr + k0 + t + 4, cb + 8 * n + g)], bh[1], bl[1]);
+            mma_tf32(acc[n], al, bh);
+            mma_tf32(acc[n], ah, bl);
+            mma_tf32(acc[n], ah, bh);
+        }
+    }
+}
+
+// Writes sign * acc (m16n8 accumulator fragments) to Z[rows ra ..][cols cb + 8n ..].
+template <int NT>
+__device__ __forceinline__ void store_frag(float *Z, int ra, int cb, const float (&acc)[NT][4],
+                                           float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        *reinterpret_cast<float2 *>(Z + sw(ra + g, cb + 8 * n + 2 * t)) =
+            make_float2(sign * acc[n][0], sign * acc[n][1]);
+        *reinterpret_cast<float2 *>(Z + sw(ra + g + 8, cb + 8 * n + 2 * t)) =
+            make_float2(sign * acc[n][2], sign * acc[n][3]);
+    }
+}
+
+// One merge level of the blocked solve for T.  For each pair of sibling
+// diagonal blocks of size S starting at r1 and r2 = r1 + S,
+//   T21 = -T22 G21 T11
+// (from T = L^{-1} diag(beta), L = I + strict_lower(diag(beta) G): the
+// lower-left block of L^{-1} is -L22^{-1} diag(beta_2) G21 L11^{-1}).
+// Phase A forms P = G21 T11 and parks it in G's upper-right block of the
+// pair, which the solve never reads otherwise (G is symmetric and only its
+// lower blocks are used); phase B forms -T22 P into T.  Warp w takes one
+// 16-row stripe and half of the columns of one pair; the k range skips the
+// steps where T11 (upper triangle, phase A) or T22 (phase B) is zero.
+template <int S>
+__device__ __forceinline__ void ut_merge(float *G, float *Tf, int warp, int lane) {
+    constexpr int WPP = S / 8;   // warps per pair
+    constexpr int NT = S / 16;   // 8-column tiles per warp
+    static_assert((kC / (2 * S)) * WPP == kThreadsP / 32, "one stripe per warp");
+    const int pair = warp / WPP, q = warp % WPP;
+    const int r1 = pair * 2 * S, r2 = r1 + S;
+    const int i0 = (q >> 1) * 16, j0 = (q & 1) * NT * 8;
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    // P[i][j] = sum_k G21[i][k] T11[k][j]; T11[k][j] = 0 for k < j
+    mma3_rows<NT>(acc, G, r2 + i0, r1, Tf, r1, r1 + j0, j0, S, lane);
+    store_frag<NT>(G, r1 + i0, r2 + j0, acc, 1.f, lane);
     __syncthreads();
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    // T21[i][j] = -sum_k T22[i][k] P[k][j]; T22[i][k] = 0 for k > i
+    mma3_rows<NT>(acc, Tf, r2 + i0, r2, G, r1, r2 + j0, 0, i0 + 16, lane);
+    store_frag<NT>(Tf, r2 + i0, r1 + j0, acc, -1.f, lane);
+    __syncthreads();
+}
+
+// T = (I + strict_lower(diag(beta) G))^{-1} diag(beta) into Tf (fp32, sw
+// layout, zero above the diagonal).  G: fp32 in the sw layout (symmetric; its
+// upper blocks are overwritten).  The eight 16 x 16 diagonal blocks are
+// solved by forward substitution (one column per thread, scaled by beta of
+// that column), then merged at sizes 16, 32 and 64 on the tensor cores.
+__device__ __forceinline__ void ut_solve(float *G, float *Tf, const float *beta, int tid) {
+    // zero the blocks above the 16 x 16 diagonal; nothing else writes them
+    for (int e = tid; e < kC * kC / 4; e += kThreadsP) {
+        const int row = e >> 5, lgrp = (e & 31) ^ sw_f(row);
+        if ((lgrp >> 2) > (row >> 4))
+            reinterpret_cast<float4 *>(Tf)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (tid < kC) {
         const int o = (tid >> 4) * 16, c = tid & 15;
+        // right-looking: once x[k] is known, fold it into every later row
         float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float s = (i == c) ? 1.f : 0.f;
-            const float bi = beta[o + i];
+        for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int k = 0; k < i; ++k) s = fmaf(-bi * G[(o + i) * kGs + o + k], x[k], s);
-            x[i] = (i < c) ? 0.f : s;
+        for (int k = 0; k < 16; ++k) {
+            if (k < c) x[k] = 0.f;
+#pragma unroll
+            for (int i = k + 1; i < 16; ++i)
+                x[i] = fmaf(-beta[o + i] * G[sw(o + i, o + k)], x[k], x[i]);
         }
+        const float bc = beta[o + c];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) Tf[(o + i) * kC + o + c] = x[i];
+        for (int i = 0; i < 16; ++i) Tf[sw(o + i, o + c)] = x[i] * bc;
     }
     __syncthreads();
-    for (int s = 16; s < kC; s *= 2) {
-        const int tiles_per_pair = (s / 4) * (s / 4);
-        const int ntiles = (kC / (2 * s)) * tiles_per_pair;
-        const bool active = tid < ntiles;
-        const int pair = tid / tiles_per_pair, t = tid % tiles_per_pair;
-        const int i0 = (t / (s / 4)) * 4, j0 = (t % (s / 4)) * 4;
-        const int r1 = pair * 2 * s, r2 = r1 + s;
-        // P = A21 Inv(B1)  ->  Tf[r1 + i][r2 + j]
-        if (active) {
-            float acc[4][4] = {};
-            for (int k = 0; k < s; ++k) {
-                const float4 bv = *reinterpret_cast<const float4 *>(Tf + (r1 + k) * kC + r1 + j0);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float av = G[(r2 + i0 + u) * kGs + r1 + k];
-                    acc[u][0] = fmaf(av, bv.x, acc[u][0]);
-                    acc[u][1] = fmaf(av, bv.y, acc[u][1]);
-                    acc[u][2] = fmaf(av, bv.z, acc[u][2]);
-                    acc[u][3] = fmaf(av, bv.w, acc[u][3]);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float bi = beta[r2 + i0 + u];
-                *reinterpret_cast<float4 *>(Tf + (r1 + i0 + u) * kC + r2 + j0) =
-                    make_float4(bi * acc[u][0], bi * acc[u][1], bi * acc[u][2], bi * acc[u][3]);
-            }
-        }
-        __syncthreads();
-        // X21 = -Inv(B2) P  ->  Tf[r2 + i][r1 + j]
-        if (active) {
-            float acc[4][4] = {};
-            for (int k = 0; k < s; ++k) {
-                const float4 pv = *reinterpret_cast<const float4 *>(Tf + (r1 + k) * kC + r2 + j0);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float av = Tf[(r2 + i0 + u) * kC + r2 + k];
-                    acc[u][0] = fmaf(av, pv.x, acc[u][0]);
-                    acc[u][1] = fmaf(av, pv.y, acc[u][1]);
-                    acc[u][2] = fmaf(av, pv.z, acc[u][2]);
-                    acc[u][3] = fmaf(av, pv.w, acc[u][3]);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                *reinterpret_cast<float4 *>(Tf + (r2 + i0 + u) * kC + r1 + j0) =
-                    make_float4(-acc[u][0], -acc[u][1], -acc[u][2], -acc[u][3]);
-        }
-        __syncthreads();
-        if (active)
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                *reinterpret_cast<float4 *>(Tf + (r1 + i0 + u) * kC + r2 + j0) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-        __syncthreads();
-    }
+    const int warp = tid >> 5, lane = tid & 31;
+    ut_merge<16>(G, Tf, warp, lane);
+    ut_merge<32>(G, Tf, warp, lane);
+    ut_merge<64>(G, Tf, warp, lane);
 }
 
 __global__ void __launch_bounds__(kThreadsP, 1)
@@ -252,6 +309,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int n = min(kC, a.L - c0);
         // ---------------------------------------------------------------- P1
         if (tid == 0) {
+            // the previous chunk's output stores have read the tiles reloaded here
+            tc::bulk_wait_read();
             mbar_arrive_expect_tx(&bars.tma, 3 * kTile);
             tc::tma_load_3d(smem + kOffQ, &maps.q, 0, c0, bh, &bars.tma);
             tc::tma_load_3d(smem + kOffQ + kTile / 2, &maps.q, 64, c0, bh, &bars.tma);
@@ -259,6 +318,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             tc::tma_load_3d(smem + kOffK + kTile / 2, &maps.k, 64, c0, bh, &bars.tma);
             tc::tma_load_3d(smem + kOffW, &maps.w, 0, c0, bh, &bars.tma);
             tc::tma_load_3d(smem + kOffW + kTile / 2, &maps.w, 64, c0, bh, &bars.tma);
+            const int next = job + gridDim.x;
+            if (next < total) {
+                const int nbh = next / a.N, nc0 = (next % a.N) * kC;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    tc::tma_prefetch_3d(&maps.q, 64 * x, nc0, nbh);
+                    tc::tma_prefetch_3d(&maps.k, 64 * x, nc0, nbh);
+                    tc::tma_prefetch_3d(&maps.w, 64 * x, nc0, nbh);
+                    tc::tma_prefetch_3d(&maps.v, 64 * x, nc0, nbh);
+                }
+            }
             if (!mbar_wait(&bars.tma, ph_tma, a.err, nullptr, kWaitLimitNs)) {
                 bars.ok = 0;
             } else {
@@ -280,26 +350,31 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 const int col = half * 64 + cc * 32;
                 tc::tmem_ld32(tmem + lane_off + kColA + col, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) Gf[r * kGs + col + i] = __uint_as_float(v[i]);
+                for (int g = 0; g < 8; ++g)
+                    *reinterpret_cast<float4 *>(Gf + sw(r, col + 4 * g)) =
+                        make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                    __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
             }
         }
         __syncthreads();
         // ---------------------------------------------------------------- P3
-        // Linv = (I + strict_lower(diag(beta) G))^{-1} into Tf (fp32, unit lower
-        // triangular); T = Linv diag(beta) is formed when converting to bf16.
-        unit_lower_inverse(Gf, Tf, bsm, tid);
+        // T = (I + strict_lower(diag(beta) G))^{-1} diag(beta) into Tf (fp32)
+        ut_solve(Gf, Tf, bsm, tid);
         // ---------------------------------------------------------------- P4
         if (warp < 4) {
-            // T fp32 -> bf16 tile (row i, column c), one column per thread
-            const int c = tid;
-            const float bc = bsm[c];
-            for (int i = 0; i < kC; ++i) {
-                const float t = (i >= c) ? Tf[i * kC + c] * bc : 0.f;
-                const __nv_bfloat16 h = __float2bfloat16_rn(t);
-                const uint32_t addr = sT + tc::swz_off(i, c >> 3, kC) + (c & 7) * 2;
-                asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
-                             "h"(*reinterpret_cast<const unsigned short *>(&h))
-                             : "memory");
+            // T fp32 -> bf16 tile, one row per thread.  Stored group pairs
+            // (2n, 2n+1) hold the logical pair n ^ (sw_f >> 1), swapped when
+            // sw_f is odd; visiting them in an order rotated by the row makes
+            // the eight lanes of a load phase read different banks.
+            const int f = sw_f(r);
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                const int n = (j + r) & 15;
+                const float4 y0 = *reinterpret_cast<const float4 *>(Tf + r * kC + n * 8);
+                const float4 y1 = *reinterpret_cast<const float4 *>(Tf + r * kC + n * 8 + 4);
+                const float4 x0 = (f & 1) ? y1 : y0, x1 = (f & 1) ? y0 : y1;
+                sts128(sT + tc::swz_off(r, n ^ (f >> 1), kC), pack2(x0.x, x0.y), pack2(x0.z, x0.w),
+                       pack2(x1.x, x1.y), pack2(x1.z, x1.w));
             }
         } else {
             // -(M_le * Q W^T) -> bf16 tile
@@ -362,10 +437,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         if (!mma_sync()) break;
         // ---------------------------------------------------------------- P8
+        // Qh (rows of threads 0-127) over the Q tile and Kh (threads 128-255)
+        // over the K tile, in place; Pm over the W tile (its last readers, the
+        // P7 MMAs, are complete); then one thread stores the three tiles.
         {
-            const size_t row = (size_t)bh * a.Lp + c0 + r;
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(half == 0 ? a.Qh : a.Kh) + row * kC;
-            const uint32_t src_tile = half == 0 ? sQ : sK;
+            const uint32_t tile = half == 0 ? sQ : sK;
             const uint32_t col = half == 0 ? kColB : kColA;
             const float sign = half == 0 ? 1.f : -1.f;  // Qh = Q + (-M QW) Wt, Kh = K - Y W
 #pragma unroll
@@ -375,40 +451,40 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float x[8];
-                    tile_load8(src_tile, r, cc * 4 + q, x);
-                    uint4 u;
-                    u.x = pack2(x[0] + sign * __uint_as_float(v[q * 8 + 0]),
-                                x[1] + sign * __uint_as_float(v[q * 8 + 1]));
-                    u.y = pack2(x[2] + sign * __uint_as_float(v[q * 8 + 2]),
-                                x[3] + sign * __uint_as_float(v[q * 8 + 3]));
-                    u.z = pack2(x[4] + sign * __uint_as_float(v[q * 8 + 4]),
-                                x[5] + sign * __uint_as_float(v[q * 8 + 5]));
-                    u.w = pack2(x[6] + sign * __uint_as_float(v[q * 8 + 6]),
-                                x[7] + sign * __uint_as_float(v[q * 8 + 7]));
-                    *reinterpret_cast<uint4 *>(dst + cc * 32 + q * 8) = u;
+                    tile_load8(tile, r, cc * 4 + q, x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] += sign * __uint_as_float(v[q * 8 + e]);
+                    sts128(tile + tc::swz_off(r, cc * 4 + q, kC), pack2(x[0], x[1]),
+                           pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
                 }
             }
             // Pm = I - W^T Wt, row r (input dimension), columns half*64 ..
-            __nv_bfloat16 *pm = static_cast<__nv_bfloat16 *>(a.Pm) + row * kC;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[32];
-                const int col = half * 64 + cc * 32;
-                tc::tmem_ld32(tmem + lane_off + kColC + col, v);
+                const int col0 = half * 64 + cc * 32;
+                tc::tmem_ld32(tmem + lane_off + kColC + col0, v);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        x[e] = ((col + q * 8 + e) == r ? 1.f : 0.f) - __uint_as_float(v[q * 8 + e]);
-                    uint4 u;
-                    u.x = pack2(x[0], x[1]);
-                    u.y = pack2(x[2], x[3]);
-                    u.z = pack2(x[4], x[5]);
-                    u.w = pack2(x[6], x[7]);
-                    *reinterpret_cast<uint4 *>(pm + col + q * 8) = u;
+                        x[e] = ((col0 + q * 8 + e) == r ? 1.f : 0.f) - __uint_as_float(v[q * 8 + e]);
+                    sts128(sW + tc::swz_off(r, half * 8 + cc * 4 + q, kC), pack2(x[0], x[1]),
+                           pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
                 }
             }
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                tc::tma_store_3d(&maps.qh, smem + kOffQ + x * (kTile / 2), 64 * x, c0, bh);
+                tc::tma_store_3d(&maps.kh, smem + kOffK + x * (kTile / 2), 64 * x, c0, bh);
+                tc::tma_store_3d(&maps.pm, smem + kOffW + x * (kTile / 2), 64 * x, c0, bh);
+            }
+            tc::bulk_commit();
         }
         // ---------------------------------------------------------------- P9
         // causal softmax of the within-chunk logits, rows r, columns half*64..
@@ -466,26 +542,33 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         ph_v ^= 1;
         if (!mma_sync()) break;
         // ---------------------------------------------------------------- P10
+        // the chunk's own attention output, normalised, over the P tile (the
+        // PV MMA is complete), then stored by one thread
         {
-            const size_t row = (size_t)bh * a.Lp + c0 + r;
-            __nv_bfloat16 *od = a.OD + row * kC + half * 64;
             const float inv = 1.f / l_row;
             uint32_t v[64];
             tc::tmem_ld64(tmem + lane_off + kColC + half * 64, v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint4 u;
-                u.x = pack2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-                u.y = pack2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-                u.z = pack2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-                u.w = pack2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
-                *reinterpret_cast<uint4 *>(od + q * 8) = u;
-            }
-            if (half == 0) a.LSD[row] = (m_row + log2f(l_row)) * 0.6931471805599453f;
+            for (int q = 0; q < 8; ++q)
+                sts128(sQm + tc::swz_off(r, half * 8 + q, kC),
+                       pack2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv),
+                       pack2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv),
+                       pack2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv),
+                       pack2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv));
+            if (half == 0)
+                a.LSD[(size_t)bh * a.Lp + c0 + r] = (m_row + log2f(l_row)) * 0.6931471805599453f;
         }
+        tc::fence_proxy_async();
         tc::fence_before_sync();
-        __syncthreads();  // Q, K tiles and TMEM free before the next chunk's loads
+        __syncthreads();  // TMEM free, P tile rewritten, before the next chunk
+        if (tid == 0) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+                tc::tma_store_3d(&maps.od, smem + kOffR1 + kTile + x * (kTile / 2), 64 * x, c0, bh);
+            tc::bulk_commit();
+        }
     }
+    if (tid == 0) tc::bulk_wait();  // no store may outlive the CTA's shared memory
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
