@@ -53,10 +53,10 @@ static_assert(kSmemP <= 232448, "shared memory budget exceeded");
 constexpr uint32_t kColA = 0, kColB = 128, kColC = 256, kColD = 384;
 
 struct PBars {
-    uint64_t tma, mma, vbar;
+    uint64_t tma, tma2, mma, mma2, vbar;
     uint32_t tmem_base;
     int ok;
-    float beta[kC];
+    alignas(16) float beta[kC];
 };
 static_assert(sizeof(PBars) <= 640, "barrier block too large");
 
@@ -122,17 +122,13 @@ __device__ __forceinline__ int sw(int r, int c) {
     return r * kC + (((c >> 2) ^ sw_f(r)) << 2) + (c & 3);
 }
 
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// x = hi + lo with both parts tf32; hi*hi + hi*lo + lo*hi carries a product
-// to about fp32 accuracy ("3xTF32").
+// x = hi + lo + e with hi, lo tf32 values (fp32 bit patterns whose low 13
+// mantissa bits are clear) and |e| < 2^-20 |x|: hi*hi + hi*lo + lo*hi carries
+// a product to about fp32 accuracy ("3xTF32").  Truncation by a bit mask
+// keeps the split on the integer pipes.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_rna(x);
-    lo = tf32_rna(x - __uint_as_float(hi));
+    hi = __float_as_uint(x) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
 }
 
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
@@ -144,14 +140,16 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// acc[n] += X[rows ra .. ra+15][k] * Y[k][cols cb + 8n .. +7] for k in [k_lo, k_hi),
-// X and Y fp32 in the sw layout (X's column and Y's row offsets included in
-// xc, yr); three tf32 MMAs per 16 x 8 x 8 step.
+// acc[n] + acc2[n] += X[rows ra .. ra+15][k] * Y[k][cols cb + 8n .. +7] for k in
+// [k_lo, k_hi), X and Y fp32 in the sw layout (X's column and Y's row offsets
+// included in xc, yr); three tf32 MMAs per 16 x 8 x 8 step, the two small
+// cross terms accumulated apart from the main one.
 template <int NT>
-__device__ __forceinline__ void mma3_rows(float (&acc)[NT][4], const float *X, int ra, int xc,
-                                          const float *Y, int yr, int cb, int k_lo, int k_hi,
-                                          int lane) {
+__device__ __forceinline__ void mma3_rows(float (&acc)[NT][4], float (&acc2)[NT][4], const float *X,
+                                          int ra, int xc, const float *Y, int yr, int cb, int k_lo,
+                                          int k_hi, int lane) {
     const int g = lane >> 2, t = lane & 3;
+#pragma unroll 2
     for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
         uint32_t ah[4], al[4];
         split_tf32(X[sw(ra + g, xc + k0 + t)], ah[0], al[0]);
@@ -163,24 +161,25 @@ __device__ __forceinline__ void mma3_rows(float (&acc)[NT][4], const float *X, i
             uint32_t bh[2], bl[2];
             split_tf32(Y[sw(yr + k0 + t, cb + 8 * n + g)], bh[0], bl[0]);
             split_tf32(Y[sw(yr + k0 + t + 4, cb + 8 * n + g)], bh[1], bl[1]);
-            mma_tf32(acc[n], al, bh);
-            mma_tf32(acc[n], ah, bl);
+            mma_tf32(acc2[n], al, bh);
+            mma_tf32(acc2[n], ah, bl);
             mma_tf32(acc[n], ah, bh);
         }
     }
 }
 
-// Writes sign * acc (m16n8 accumulator fragments) to Z[rows ra ..][cols cb + 8n ..].
+// Writes sign * (acc + acc2) (m16n8 accumulator fragments) to
+// Z[rows ra ..][cols cb + 8n ..].
 template <int NT>
 __device__ __forceinline__ void store_frag(float *Z, int ra, int cb, const float (&acc)[NT][4],
-                                           float sign, int lane) {
+                                           const float (&acc2)[NT][4], float sign, int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
         *reinterpret_cast<float2 *>(Z + sw(ra + g, cb + 8 * n + 2 * t)) =
-            make_float2(sign * acc[n][0], sign * acc[n][1]);
+            make_float2(sign * (acc[n][0] + acc2[n][0]), sign * (acc[n][1] + acc2[n][1]));
         *reinterpret_cast<float2 *>(Z + sw(ra + g + 8, cb + 8 * n + 2 * t)) =
-            make_float2(sign * acc[n][2], sign * acc[n][3]);
+            make_float2(sign * (acc[n][2] + acc2[n][2]), sign * (acc[n][3] + acc2[n][3]));
     }
 }
 
@@ -193,27 +192,35 @@ __device__ __forceinline__ void store_frag(float *Z, int ra, int cb, const float
 // pair, which the solve never reads otherwise (G is symmetric and only its
 // lower blocks are used); phase B forms -T22 P into T.  Warp w takes one
 // 16-row stripe and half of the columns of one pair; the k range skips the
-// steps where T11 (upper triangle, phase A) or T22 (phase B) is zero.
+// steps where T11 (upper triangle, phase A) or T22 (phase B) is zero.  The
+// two warps that share a scheduler (w and w + 4) take the left and right
+// column halves and mirrored stripes, so that both phases give them equal
+// work.
 template <int S>
 __device__ __forceinline__ void ut_merge(float *G, float *Tf, int warp, int lane) {
-    constexpr int WPP = S / 8;   // warps per pair
+    constexpr int M = S / 16;    // 16-row stripes per block
     constexpr int NT = S / 16;   // 8-column tiles per warp
-    static_assert((kC / (2 * S)) * WPP == kThreadsP / 32, "one stripe per warp");
-    const int pair = warp / WPP, q = warp % WPP;
+    static_assert((kC / (2 * S)) * 2 * M == kThreadsP / 32, "one stripe per warp");
+    const int sched = warp & 3, h = warp >> 2;
+    const int pair = sched / M, u = sched % M;
     const int r1 = pair * 2 * S, r2 = r1 + S;
-    const int i0 = (q >> 1) * 16, j0 = (q & 1) * NT * 8;
-    float acc[NT][4];
+    const int i0 = (h ? M - 1 - u : u) * 16, j0 = h * NT * 8;
+    float acc[NT][4], acc2[NT][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = acc2[n][e] = 0.f;
     // P[i][j] = sum_k G21[i][k] T11[k][j]; T11[k][j] = 0 for k < j
-    mma3_rows<NT>(acc, G, r2 + i0, r1, Tf, r1, r1 + j0, j0, S, lane);
-    store_frag<NT>(G, r1 + i0, r2 + j0, acc, 1.f, lane);
+    mma3_rows<NT>(acc, acc2, G, r2 + i0, r1, Tf, r1, r1 + j0, j0, S, lane);
+    store_frag<NT>(G, r1 + i0, r2 + j0, acc, acc2, 1.f, lane);
     __syncthreads();
 #pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = acc2[n][e] = 0.f;
     // T21[i][j] = -sum_k T22[i][k] P[k][j]; T22[i][k] = 0 for k > i
-    mma3_rows<NT>(acc, Tf, r2 + i0, r2, G, r1, r2 + j0, 0, i0 + 16, lane);
-    store_frag<NT>(Tf, r2 + i0, r1 + j0, acc, -1.f, lane);
+    mma3_rows<NT>(acc, acc2, Tf, r2 + i0, r2, G, r1, r2 + j0, 0, i0 + 16, lane);
+    store_frag<NT>(Tf, r2 + i0, r1 + j0, acc, acc2, -1.f, lane);
     __syncthreads();
 }
 
@@ -230,17 +237,29 @@ __device__ __forceinline__ void ut_solve(float *G, float *Tf, const float *beta,
             reinterpret_cast<float4 *>(Tf)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (tid < kC) {
+        // column c of the diagonal block at o: x = (I + strict_lower(diag(beta) G))^{-1} e_c,
+        // right-looking: s[i] accumulates sum_{k<i} G[i][k] x[k] and x[k] = [k == c] - beta_k s[k].
+        // G[i][k] is read as G[k][i] (symmetry), one 16-byte group at a time.
         const int o = (tid >> 4) * 16, c = tid & 15;
-        // right-looking: once x[k] is known, fold it into every later row
-        float x[16];
+        float bt[16], s_[16], x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+        for (int q = 0; q < 4; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(beta + o + 4 * q);
+            bt[4 * q] = b4.x; bt[4 * q + 1] = b4.y; bt[4 * q + 2] = b4.z; bt[4 * q + 3] = b4.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s_[i] = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-            if (k < c) x[k] = 0.f;
+            x[k] = (k < c) ? 0.f : fmaf(-bt[k], s_[k], (k == c) ? 1.f : 0.f);
 #pragma unroll
-            for (int i = k + 1; i < 16; ++i)
-                x[i] = fmaf(-beta[o + i] * G[sw(o + i, o + k)], x[k], x[i]);
+            for (int q = (k + 1) >> 2; q < 4; ++q) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(G + sw(o + k, o + 4 * q));
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q + e > k) s_[4 * q + e] = fmaf(gv[e], x[k], s_[4 * q + e]);
+            }
         }
         const float bc = beta[o + c];
 #pragma unroll
@@ -275,7 +294,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
     if (tid == 0) {
         mbar_init(&bars.tma, 1);
+        mbar_init(&bars.tma2, 1);
         mbar_init(&bars.mma, 1);
+        mbar_init(&bars.mma2, 1);
         mbar_init(&bars.vbar, 1);
         bars.ok = 1;
         fence_mbar_init();
@@ -288,7 +309,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = bars.tmem_base;
-    uint32_t ph_tma = 0, ph_mma = 0, ph_v = 0;
+    uint32_t ph_tma = 0, ph_mma = 0, ph_mma2 = 0, ph_v = 0;
     const float sl2 = a.scale * 1.4426950408889634f;
 
     // thread 0 waits for the MMAs committed so far; result shared by the block
@@ -308,16 +329,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int c0 = chunk * kC;
         const int n = min(kC, a.L - c0);
         // ---------------------------------------------------------------- P1
+        // W first: G = W W^T alone lets the solve for T start while the
+        // other three products run
         if (tid == 0) {
             // the previous chunk's output stores have read the tiles reloaded here
             tc::bulk_wait_read();
-            mbar_arrive_expect_tx(&bars.tma, 3 * kTile);
-            tc::tma_load_3d(smem + kOffQ, &maps.q, 0, c0, bh, &bars.tma);
-            tc::tma_load_3d(smem + kOffQ + kTile / 2, &maps.q, 64, c0, bh, &bars.tma);
-            tc::tma_load_3d(smem + kOffK, &maps.k, 0, c0, bh, &bars.tma);
-            tc::tma_load_3d(smem + kOffK + kTile / 2, &maps.k, 64, c0, bh, &bars.tma);
+            mbar_arrive_expect_tx(&bars.tma, kTile);
             tc::tma_load_3d(smem + kOffW, &maps.w, 0, c0, bh, &bars.tma);
             tc::tma_load_3d(smem + kOffW + kTile / 2, &maps.w, 64, c0, bh, &bars.tma);
+            mbar_arrive_expect_tx(&bars.tma2, 2 * kTile);
+            tc::tma_load_3d(smem + kOffQ, &maps.q, 0, c0, bh, &bars.tma2);
+            tc::tma_load_3d(smem + kOffQ + kTile / 2, &maps.q, 64, c0, bh, &bars.tma2);
+            tc::tma_load_3d(smem + kOffK, &maps.k, 0, c0, bh, &bars.tma2);
+            tc::tma_load_3d(smem + kOffK + kTile / 2, &maps.k, 64, c0, bh, &bars.tma2);
             const int next = job + gridDim.x;
             if (next < total) {
                 const int nbh = next / a.N, nc0 = (next % a.N) * kC;
@@ -334,13 +358,24 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             } else {
                 tc::fence_after_sync();
                 tc::gemm_128x128x128(tmem + kColA, sW, sW, false, false);  // G
-                tc::gemm_128x128x128(tmem + kColB, sQ, sW, false, false);  // Q W^T
-                tc::gemm_128x128x128(tmem + kColC, sK, sW, false, false);  // K W^T
-                tc::gemm_128x128x128(tmem + kColD, sQ, sK, false, false);  // Q K^T
+                tc::mma_commit(&bars.mma);
+                if (!mbar_wait(&bars.tma2, ph_tma, a.err, nullptr, kWaitLimitNs)) {
+                    bars.ok = 0;
+                } else {
+                    tc::fence_after_sync();
+                    tc::gemm_128x128x128(tmem + kColB, sQ, sW, false, false);  // Q W^T
+                    tc::gemm_128x128x128(tmem + kColC, sK, sW, false, false);  // K W^T
+                    tc::gemm_128x128x128(tmem + kColD, sQ, sK, false, false);  // Q K^T
+                    tc::mma_commit(&bars.mma2);
+                }
+                if (!mbar_wait(&bars.mma, ph_mma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
             }
         }
         ph_tma ^= 1;
-        if (!mma_sync()) break;
+        ph_mma ^= 1;
+        __syncthreads();
+        tc::fence_after_sync();
+        if (!bars.ok) break;
         // ---------------------------------------------------------------- P2
         if (tid < kC) bsm[tid] = (tid < n) ? a.beta[(size_t)bh * a.L + c0 + tid] : 0.f;
         {
@@ -360,6 +395,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         // ---------------------------------------------------------------- P3
         // T = (I + strict_lower(diag(beta) G))^{-1} diag(beta) into Tf (fp32)
         ut_solve(Gf, Tf, bsm, tid);
+        // Q W^T, K W^T, Q K^T
+        if (tid == 0 && !mbar_wait(&bars.mma2, ph_mma2, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
+        ph_mma2 ^= 1;
+        __syncthreads();
+        tc::fence_after_sync();
+        if (!bars.ok) break;
         // ---------------------------------------------------------------- P4
         if (warp < 4) {
             // T fp32 -> bf16 tile, one row per thread.  Stored group pairs
