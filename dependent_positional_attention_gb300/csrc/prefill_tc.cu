@@ -11,17 +11,20 @@
 //     Qt <- Qt Pm_c              (chunk product, Pm_c = I - W_c^T T_c W_c)
 //     O  += softmax-weights(S_c) V_c           (online softmax)
 // Each contraction is a 128 x 128 x 128 bf16 MMA with fp32 accumulation in
-// tensor memory; the carried rows live in shared memory as bf16 (the A
-// operand of the next MMAs).  Applying the whole chunk product as one d x d
+// tensor memory.  The carried rows (after the first step) and the softmax
+// weights P are written back to tensor memory as bf16 and read from there as
+// the A operand, so that shared memory only carries the B operands: at
+// M = N = 128 an MMA with both operands in shared memory would take all of
+// its bandwidth.  Applying the whole chunk product as one d x d
 // matrix takes one MMA per chunk instead of two (Qt W^T, then X Wt) and
 // re-rounds the carried rows once per chunk rather than rounding a
 // correction term of their own size.
 //
 // One CTA per SM (persistent), tiles ordered by decreasing work.  Warp roles:
-//   warps 0-3   carried-query warpgroup: Qt Pm_c (TMEM, fp32) -> bf16 shadow
+//   warps 0-3   carried-query warpgroup: Qt Pm_c (TMEM, fp32) -> bf16 (TMEM)
 //   warps 4-7   softmax warpgroup: logits, online softmax with lazy rescale
-//               of O, P -> bf16, epilogue (out, lse)
-//   warp 8      TMA producer: Qh_b, then a 5-slot ring of Pm_c, Kh_c, V
+//               of O, P -> bf16 (TMEM), epilogue (out, lse)
+//   warp 8      TMA producer: Qh_b, then a 6-slot ring of Pm_c, Kh_c, V
 //   warp 9      MMA issuer (one thread) and TMEM owner; warps 10-11 idle
 // Registers are rebalanced at start (setmaxnreg): the producer/MMA group
 // drops to 120 per thread, the two compute groups rise to 192 (the launch's
@@ -29,7 +32,8 @@
 // MMA issue order per step c: U_c = Qt Pm_c (the critical chain), S_c,
 // PV_{c+1}; the PV of a chunk runs one step late so the softmax has a full
 // step of slack.  Chunk-0 tiles need no scan: the softmax group copies the
-// prep's result.  TMEM columns: [0,128) U, [256,384) S, [384,512) O.
+// prep's result.  TMEM columns: [0,128) U, [128,192) Qt (bf16 pairs),
+// [192,256) P (bf16 pairs), [256,384) S, [384,512) O.
 // Every wait is bounded; on timeout the kernel sets the device error flag,
 // drains its outstanding copies and MMAs, frees TMEM and exits.
 
@@ -41,18 +45,17 @@ namespace path {
 namespace {
 
 constexpr int kD = 128, kC = 128;
-constexpr int kSlots = 5;
+constexpr int kSlots = 6;
 constexpr int kTileBytes = kC * kD * 2;  // 32 KB bf16 tile
 constexpr int kThreadsTC = 384;  // 3 warpgroups
-constexpr uint32_t kColU = 0, kColS = 256, kColO = 384;
+constexpr uint32_t kColU = 0, kColQt = 128, kColP = 192, kColS = 256, kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // dynamic shared memory layout (offsets from a 1024-aligned base)
 constexpr int kOffQb = 0;
-constexpr int kOffPb = kOffQb + kTileBytes;
-constexpr int kOffRing = kOffPb + kTileBytes;
+constexpr int kOffRing = kOffQb + kTileBytes;
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
 
 struct Bars {
@@ -102,13 +105,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
 struct Tile {
     int b, bh;
 };
@@ -128,7 +124,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBar);
     const uint32_t sQb = smem_u32(smem + kOffQb);
-    const uint32_t sPb = smem_u32(smem + kOffPb);
     const uint32_t sRing = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.N * a.BH;
@@ -172,7 +167,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             tc::prefetch_tmap(&maps.v);
             int slot = 0;
             uint32_t ph = 0, qe_ph = 0;
-            int last_par[kSlots] = {-1, -1, -1, -1, -1};
+            int last_par[kSlots];
+            for (int i = 0; i < kSlots; ++i) last_par[i] = -1;
             int q_last_par = -1;
             uint32_t q_loads = 0;
             bool ok = true;
@@ -222,7 +218,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             int slot = 0;
             uint32_t ph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0, pf_ph = 0;
             const uint32_t qb_lo = tc::desc_lo(sQb, false);
-            const uint32_t pb_lo = tc::desc_lo(sPb, false);
             bool ok = true;
             auto take = [&](uint32_t &addr) -> bool {
                 if (!mbar_wait(&bars.full[slot], ph, a.err, abort_word, lim)) return false;
@@ -244,7 +239,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim)) return false;
                 pf_ph ^= 1;
                 tc::fence_after_sync();
-                tc::gemm128_lo<true>(tmem + kColO, pb_lo, tc::desc_lo(vaddr, true), true);
+                tc::gemm128_ta<true>(tmem + kColO, tmem + kColP, tc::desc_lo(vaddr, true), true);
                 release();
                 tc::mma_commit(&bars.o_done);
                 return true;
@@ -262,11 +257,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                     if (!ok) break;
                     tc::fence_after_sync();
+                    // the first step reads Qh_b from shared memory, later steps
+                    // the carried rows from tensor memory
+                    const bool first = (c == b - 1);
                     uint32_t addr;
                     if (c >= 1) {
                         // carried rows through the chunk product: U = Qt Pm_c
                         if (!(ok = take(addr))) break;
-                        tc::gemm128_lo<true>(tmem + kColU, qb_lo, tc::desc_lo(addr, true), false);
+                        if (first)
+                            tc::gemm128_lo<true>(tmem + kColU, qb_lo, tc::desc_lo(addr, true), false);
+                        else
+                            tc::gemm128_ta<true>(tmem + kColU, tmem + kColQt, tc::desc_lo(addr, true),
+                                                 false);
                         release();
                         tc::mma_commit(&bars.u_done);
                     }
@@ -274,11 +276,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (!(ok = mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim))) break;
                     se_ph ^= 1;
                     tc::fence_after_sync();
-                    tc::gemm128_lo<false>(tmem + kColS, qb_lo, tc::desc_lo(addr, false), false);
+                    if (first)
+                        tc::gemm128_lo<false>(tmem + kColS, qb_lo, tc::desc_lo(addr, false), false);
+                    else
+                        tc::gemm128_ta<false>(tmem + kColS, tmem + kColQt, tc::desc_lo(addr, false),
+                                              false);
                     release();
                     tc::mma_commit(&bars.s_full);
-                    // Qt's shadow is free once S_c (its last reader) completes
-                    tc::mma_commit(c >= 1 ? &bars.qb_free : &bars.qb_empty);
+                    // Qh_b's tile is free after the first step; the carried rows
+                    // may be overwritten once U_c and S_c (their readers) complete
+                    if (first) tc::mma_commit(&bars.qb_empty);
+                    if (c >= 1) tc::mma_commit(&bars.qb_free);
                     if (c < b - 1) ok = pv();
                 }
                 ok = ok && pv();
@@ -294,7 +302,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (warp < 4) {
         // ------------------------------------------------------------ carried query
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t ud_ph = 0, qf_ph = 0, qt_ph = 0;
         bool ok = true;
@@ -322,15 +329,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     for (int j = 0; j < 64; ++j)
                         pk[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
                 }
-                tc::fence_before_sync();
                 ok = group_all(1, 128, mbar_wait(&bars.qb_free, qf_ph, a.err, abort_word, lim));
                 if (!ok) break;
                 qf_ph ^= 1;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    st_shared_v4(sQb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
-                                 pk[4 * j + 2], pk[4 * j + 3]);
-                tc::fence_proxy_async();
+                tc::fence_after_sync();
+                tc::tmem_st32(lane_addr + kColQt, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                tc::tmem_st32(lane_addr + kColQt + 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
                 named_bar(1, 128);
                 if (threadIdx.x == 0) mbar_arrive(&bars.qb_conv_full);
             }
@@ -457,13 +464,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                     tc::tmem_wait_st();
                 }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    st_shared_v4(sPb + tc::swz_off(r, j, kC), pk[4 * j], pk[4 * j + 1],
-                                 pk[4 * j + 2], pk[4 * j + 3]);
+                tc::tmem_st32(lane_addr + kColP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                tc::tmem_st32(lane_addr + kColP + 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                tc::tmem_wait_st();
                 l = l * alpha + (sum0 + sum1);
                 m = mnew;
-                tc::fence_proxy_async();
                 tc::fence_before_sync();
                 named_bar(2, 128);
                 if (threadIdx.x == 128) mbar_arrive(&bars.p_full);

@@ -260,5 +260,33 @@ __device__ __forceinline__ void gemm128_lo(uint32_t d_tmem, uint32_t a_lo, uint3
     }
 }
 
+// D (+)= A * B with A read from tensor memory at column a_tmem (lane field 0):
+// row i of A in lane i, 16-bit elements packed two per 32-bit column (even k
+// in the low half), K = 16 per instruction = 8 columns.  B as in mma_bf16_lohi.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 bd, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        : "memory");
+}
+
+// gemm128_lo with the 128 x 128 bf16 A operand in tensor memory (64 columns
+// from a_tmem, packed as in mma_bf16_ta).
+template <bool B_MN>
+__device__ __forceinline__ void gemm128_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                           bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16(128, 128, false, B_MN);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t boff = B_MN ? (uint32_t)(kk * 128) : (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+        mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_lo + boff, idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
 }  // namespace tc
 }  // namespace path
