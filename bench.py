@@ -16,6 +16,7 @@ query rows of the headline workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -37,14 +38,17 @@ CHUNK = 128
 
 
 def prefill_flops(B, H, L, d, C=CHUNK):
-    """Algorithmic FLOPs: QK^T + PV over the causal triangle (2 d L^2 per head),
-    the carried-query update (one C x d x d product with the chunk's d x d
-    transition matrix per off-diagonal chunk pair except the last:
-    2 C d^2 (N-1)(N-2)/2), and the chunk UT transform (16 L C d).
+    """Algorithmic FLOPs per head, split by kernel.
+    scan: QK^T + PV over the off-diagonal chunk pairs (4 C^2 d per pair,
+    N (N-1) / 2 pairs) plus the carried-query update (one C x d x d product
+    with a chunk's d x d transition matrix per pair (b, c) with c >= 1:
+    2 C d^2 (N-1)(N-2)/2).
+    prep: the chunk UT transform (16 L C d, the survey's count) plus each
+    chunk's own causal block (QK^T + PV over its lower triangle, 2 C^2 d).
     Returns (scan_flops, prep_flops)."""
     N = math.ceil(L / C)
-    scan = (2 * d * L * L + 2 * C * d * d * (N - 1) * (N - 2) / 2) * B * H
-    prep = 16 * L * C * d * B * H
+    scan = (4 * C * C * d * N * (N - 1) / 2 + 2 * C * d * d * (N - 1) * (N - 2) / 2) * B * H
+    prep = (16 * L * C * d + 2 * C * C * d * N) * B * H
     return scan, prep
 
 
@@ -122,12 +126,24 @@ def barrier(ws):
         torch.distributed.barrier()
 
 
+def _collective_device():
+    # NCCL reduces CUDA tensors; gloo (the CPU tests of this path) host tensors
+    return "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+
+
 def max_over_ranks(x, ws):
+    """The slowest rank's time: every rank times the same number of steps."""
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_collective_device())
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, ms_per_step_max, ws):
+    """Whole-job rate: every rank processes its own units (weak scaling, no
+    data-path collective); the job takes as long as its slowest rank."""
+    return ws * units_per_rank / (ms_per_step_max * 1e-3)
 
 
 def timed_prefill(x, steps, warmup, ws, fox=False, sampler=None):
@@ -175,11 +191,11 @@ def prefill_block(wlk, steps, warmup, ws, peaks, seed=0, sampler=None):
                                                  sampler=sampler)
     ms = max_over_ranks(ms, ws)
     scan_f, prep_f = prefill_flops(B, H, L, d)
-    tflops = ws * (scan_f + prep_f) / (ms * 1e-3) / 1e12
+    tflops = job_throughput(scan_f + prep_f, ms, ws) / 1e12
     scan_tf = scan_f / (scan_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     res = {
-        "workload": wlk.name, "tokens_per_s": ws * B * L / (ms * 1e-3), "tflops": tflops,
+        "workload": wlk.name, "tokens_per_s": job_throughput(B * L, ms, ws), "tflops": tflops,
         "ms_per_step": ms, "prep_ms": prep_ms, "scan_ms": scan_ms,
         "flops_per_step": scan_f + prep_f,
         "roofline": {"kernel": "flash_tc_kernel (tensor-core scan)", "bound": "tensor",
@@ -323,9 +339,16 @@ def main():
     ap.add_argument("--skip-extra", action="store_true",
                     help="headline workload only (no FoX / long / decode objects)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the headline workload's batch (smaller cases for "
+                         "profiler captures; the default is the headline B8)")
     args = ap.parse_args()
     ws, rank, local = dist_info()
     head = wl.PREFILL_4K
+    if args.batch:
+        head = dataclasses.replace(head, batch=args.batch,
+                                   name=head.name.replace("B%d " % head.batch,
+                                                          "B%d " % args.batch))
 
     if args.impl == "reference":
         if rank != 0:
