@@ -404,12 +404,15 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        smp = OracleSampler(head, heads=8)
+        # every head, so that about 10 s of oracle work fits under the cap of
+        # one sequence's worth of rows per head
+        nh = head.batch * head.heads
+        smp = OracleSampler(head, heads=nh)
         dt, n = smp.run(smp.calibrated(10.0))
         threads = smp.threads
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": "%d uniformly sampled query rows (8 heads) of the B8 H12 L4096 "
-                         "workload, %.1f s" % (n, dt)}
+               "sample": "%d uniformly sampled query rows (%d heads) of the %s workload, %.1f s"
+                         % (n, nh, head.name, dt)}
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
