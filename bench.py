@@ -52,6 +52,10 @@ def prefill_flops(B, H, L, d, C=CHUNK):
     return scan, prep
 
 
+# DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
+SCAN_TRAFFIC_B2 = 145.389312e6 + 12.049664e6
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -200,7 +204,12 @@ def prefill_block(wlk, steps, warmup, ws, peaks, seed=0, sampler=None):
         "flops_per_step": scan_f + prep_f,
         "roofline": {"kernel": "flash_tc_kernel (tensor-core scan)", "bound": "tensor",
                      "achieved": scan_tf, "peak": peak, "unit": "TFLOP/s",
-                     "frac": scan_tf / peak, "traffic": None,
+                     "frac": scan_tf / peak,
+                     # DRAM bytes per launch: ncu read + write of this kernel on the B2 case,
+                     # scaled by the batch (profiles/scan_prep_b2h12l4096.md); the headline B8
+                     # launch only
+                     "traffic": (SCAN_TRAFFIC_B2 * B / 2
+                                 if (H, L, d) == (12, 4096, 128) and not wlk.fox else None),
                      "peak_source": peaks["source"] + " bf16 dense (burst)"},
     }
     del x
