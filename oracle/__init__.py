@@ -49,12 +49,16 @@ def _declare(lib):
     lib.path_oracle_logits.argtypes = [_I64, _I64, _DBL, _PD, _PD, _PD, _PD, _PD, _PD]
     lib.path_oracle_decode_step.argtypes = [_I64, _I64, _I64, _I64, _DBL, _PD, _PD,
                                             _PD, _PD, _PD, _PD, _PD, _PD, ctypes.c_int]
+    lib.path_oracle_decode_step_fox.argtypes = [_I64, _I64, _I64, _I64, _DBL, _PD, _PD,
+                                                _PD, _PD, _PD, _PD, _PD, _PD, _PD, _PD,
+                                                ctypes.c_int]
     lib.path_oracle_build_kcache.argtypes = [_I64, _I64, _I64, _I64, _PD, _PD, _PD,
                                              _PD, ctypes.c_int]
     lib.path_oracle_boundary_rows.argtypes = [_I64, _I64, _I64, _PD, _PD, _PD, _PD,
                                               _PD, _PD]
     for f in (lib.path_oracle_prefill, lib.path_oracle_logits,
-              lib.path_oracle_decode_step, lib.path_oracle_build_kcache,
+              lib.path_oracle_decode_step, lib.path_oracle_decode_step_fox,
+              lib.path_oracle_build_kcache,
               lib.path_oracle_boundary_rows):
         f.restype = ctypes.c_int
     return lib
@@ -161,6 +165,33 @@ def decode_step(k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, scale=None,
                                      _p(w_t), _p(beta_t), _p(out), int(nthreads))
     if rc != 0:
         raise ValueError("path_oracle_decode_step failed: %d" % rc)
+    return out
+
+
+def decode_step_fox(k_cache, v_cache, lf_hist, t, q_t, k_t, v_t, w_t, beta_t, log_f_t,
+                    scale=None, nthreads=0, lib=None):
+    """One PaTH-FoX inference step: decode_step, plus the forget-gate bias
+    sum_{s=j+1}^{t} log f_s on the logit of cached key j (section 2, the
+    PaTH-FoX combination; section 3, inference).  lf_hist: float64 [BH, cap]
+    holding log f of tokens 0..t-1; log_f_t ([BH]) is stored at slot t.
+    Returns out [BH, d]."""
+    lib = lib or load()
+    assert k_cache.dtype == np.float64 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.float64 and v_cache.flags.c_contiguous
+    assert lf_hist.dtype == np.float64 and lf_hist.flags.c_contiguous
+    BH, cap, d = k_cache.shape
+    assert lf_hist.shape == (BH, cap)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    q_t, k_t, v_t, w_t, beta_t, log_f_t = (_f64(x) for x in (q_t, k_t, v_t, w_t, beta_t,
+                                                             log_f_t))
+    out = np.empty((BH, d), dtype=np.float64)
+    rc = lib.path_oracle_decode_step_fox(BH, cap, int(t), d, float(scale), _p(k_cache),
+                                         _p(v_cache), _p(lf_hist), _p(q_t), _p(k_t),
+                                         _p(v_t), _p(w_t), _p(beta_t), _p(log_f_t), _p(out),
+                                         int(nthreads))
+    if rc != 0:
+        raise ValueError("path_oracle_decode_step_fox failed: %d" % rc)
     return out
 
 

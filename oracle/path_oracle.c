@@ -176,11 +176,42 @@ int path_oracle_logits(int64_t L, int64_t d, double scale, const double *q,
 }
 
 /*
- * One decode step for every head (inference bullet of section 3).
- * k_cache, v_cache are [BH][cap][d]; positions 0..t-1 hold the cache as left
- * by the previous steps.  For j < t: k_j <- H_t k_j.  Then k_t, v_t are
- * written to slot t, and out = softmax_j(scale * k_j . q_t) v over j <= t.
- * q_t, k_t, v_t, w_t are [BH][d]; beta_t is [BH]; out is [BH][d].
+ * One head of a decode step (inference bullet of section 3): cached keys
+ * j < t take the new token's transition in place, k_j <- H_t k_j; (k_t, v_t)
+ * are written at slot t; then softmax attention of q_t over slots 0..t.  With
+ * a forget-gate history lf (PaTH-FoX, section 2), log f_t is stored at slot t
+ * and the logit of key j gains sum_{s=j+1}^{t} log f_s, accumulated from the
+ * right one term per key; the new token's own logit gains nothing.
+ */
+static int decode_head(int64_t cap, int64_t t, int64_t d, double scale, double *kc,
+                       double *vc, double *lf, const double *q_t, const double *k_t,
+                       const double *v_t, const double *w_t, double beta_t, double log_f_t,
+                       double *out)
+{
+    (void)cap;
+    for (int64_t j = 0; j < t; ++j)
+        apply_transition(kc + j * d, w_t, beta_t, d);
+    memcpy(kc + t * d, k_t, (size_t)d * sizeof(double));
+    memcpy(vc + t * d, v_t, (size_t)d * sizeof(double));
+    if (lf)
+        lf[t] = log_f_t;
+    double *logit = (double *)malloc((size_t)(t + 1) * sizeof(double));
+    if (!logit)
+        return -3;
+    double bias = 0.0;  /* sum_{s=j+1}^{t} log f_s */
+    for (int64_t j = t; j >= 0; --j) {
+        logit[j] = scale * dot(kc + j * d, q_t, d) + bias;
+        if (lf)
+            bias += lf[j];
+    }
+    softmax_rows(t + 1, d, logit, vc, out, NULL);
+    free(logit);
+    return 0;
+}
+
+/*
+ * One PaTH decode step for BH independent heads (see decode_head).
+ * k_cache, v_cache: [BH][cap][d], modified in place.
  */
 int path_oracle_decode_step(int64_t BH, int64_t cap, int64_t t, int64_t d,
                             double scale, double *k_cache, double *v_cache,
@@ -199,22 +230,46 @@ int path_oracle_decode_step(int64_t BH, int64_t cap, int64_t t, int64_t d,
     int err = 0;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t bh = 0; bh < BH; ++bh) {
-        double *kc = k_cache + bh * cap * d, *vc = v_cache + bh * cap * d;
-        const double *wt = w_t + bh * d;
-        for (int64_t j = 0; j < t; ++j)
-            apply_transition(kc + j * d, wt, beta_t[bh], d);
-        memcpy(kc + t * d, k_t + bh * d, (size_t)d * sizeof(double));
-        memcpy(vc + t * d, v_t + bh * d, (size_t)d * sizeof(double));
-        double *logit = (double *)malloc((size_t)(t + 1) * sizeof(double));
-        if (!logit) {
+        int e = decode_head(cap, t, d, scale, k_cache + bh * cap * d, v_cache + bh * cap * d,
+                            NULL, q_t + bh * d, k_t + bh * d, v_t + bh * d, w_t + bh * d,
+                            beta_t[bh], 0.0, out + bh * d);
+        if (e) {
 #pragma omp atomic write
-            err = -3;
-            continue;
+            err = e;
         }
-        for (int64_t j = 0; j <= t; ++j)
-            logit[j] = scale * dot(kc + j * d, q_t + bh * d, d);
-        softmax_rows(t + 1, d, logit, vc, out + bh * d, NULL);
-        free(logit);
+    }
+    return err;
+}
+
+/*
+ * One PaTH-FoX decode step (see decode_head).  lf_hist: [BH][cap], log f of
+ * tokens 0..t-1 on entry; log_f_t is stored at slot t.
+ */
+int path_oracle_decode_step_fox(int64_t BH, int64_t cap, int64_t t, int64_t d,
+                                double scale, double *k_cache, double *v_cache,
+                                double *lf_hist, const double *q_t, const double *k_t,
+                                const double *v_t, const double *w_t,
+                                const double *beta_t, const double *log_f_t, double *out,
+                                int nthreads)
+{
+    if (BH < 0 || d <= 0 || t < 0 || t >= cap || !lf_hist || !log_f_t)
+        return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        int e = decode_head(cap, t, d, scale, k_cache + bh * cap * d, v_cache + bh * cap * d,
+                            lf_hist + bh * cap, q_t + bh * d, k_t + bh * d, v_t + bh * d,
+                            w_t + bh * d, beta_t[bh], log_f_t[bh], out + bh * d);
+        if (e) {
+#pragma omp atomic write
+            err = e;
+        }
     }
     return err;
 }

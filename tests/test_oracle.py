@@ -372,6 +372,42 @@ def test_decode_steps_reproduce_prefill():
     np.testing.assert_allclose(kc, oracle.build_kcache(k, w, beta), atol=1e-12)
 
 
+def test_fox_decode_steps_reproduce_fox_prefill():
+    """PaTH-FoX at inference (section 2, the FoX combination; section 3,
+    inference): decoding with the forget-gate history reproduces the PaTH-FoX
+    prefill rows, whose bias the prefill oracle sums along each query's
+    reflection sweep; with log f = 0 it is the PaTH decode step."""
+    rng = np.random.default_rng(21)
+    BH, L, L0, d = 3, 36, 20, 8
+    q, k, v = (rng.standard_normal((BH, L, d)) for _ in range(3))
+    w = rng.standard_normal((BH, L, d))
+    w /= np.linalg.norm(w, axis=-1, keepdims=True)
+    beta = rng.uniform(0, 2, (BH, L))
+    log_f = np.log(1.0 / (1.0 + np.exp(-rng.normal(1.0, 1.0, (BH, L)))))
+    out_ref, _ = oracle.prefill(q, k, v, w, beta, log_f=log_f)
+    kc = oracle.build_kcache(k[:, :L0], w[:, :L0], beta[:, :L0], cap=L)
+    vc = np.zeros((BH, L, d))
+    vc[:, :L0] = v[:, :L0]
+    lf = np.zeros((BH, L))
+    lf[:, :L0] = log_f[:, :L0]
+    kc0, vc0 = kc.copy(), vc.copy()
+    for t in range(L0, L):
+        o = oracle.decode_step_fox(kc, vc, lf, t, q[:, t], k[:, t], v[:, t], w[:, t],
+                                   beta[:, t], log_f[:, t])
+        np.testing.assert_allclose(o, out_ref[:, t], atol=1e-12)
+    np.testing.assert_allclose(lf, log_f, atol=0)
+    # zero forget-gate logits: exactly the PaTH step, on the same cache
+    kcA, vcA = kc0.copy(), vc0.copy()
+    kcB, vcB = kc0.copy(), vc0.copy()
+    lfz = np.zeros((BH, L))
+    t = L0 + 1
+    oA = oracle.decode_step_fox(kcA, vcA, lfz, t, q[:, t], k[:, t], v[:, t], w[:, t],
+                                beta[:, t], np.zeros(BH))
+    oB = oracle.decode_step(kcB, vcB, t, q[:, t], k[:, t], v[:, t], w[:, t], beta[:, t])
+    np.testing.assert_allclose(oA, oB, atol=0)
+    np.testing.assert_allclose(kcA, kcB, atol=0)
+
+
 def test_oracle_rejects_bad_arguments():
     lib = oracle.load()
     assert lib.path_oracle_prefill(1, 4, 0, 1.0, None, None, None, None, None, None,

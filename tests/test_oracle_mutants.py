@@ -38,8 +38,15 @@ MUTANTS = {
         "        apply_transition(u, w + j * d, beta[j], d);\n"),
     "lse_without_max": ("*lse = mx + log(sum);", "*lse = log(sum);"),
     "softmax_unnormalised": ("out[m] /= sum;", "out[m] /= 1.0;"),
-    "decode_skips_last_key": ("for (int64_t j = 0; j < t; ++j)\n            apply_transition",
-                              "for (int64_t j = 0; j + 1 < t; ++j)\n            apply_transition"),
+    "decode_skips_last_key": ("for (int64_t j = 0; j < t; ++j)\n        apply_transition",
+                              "for (int64_t j = 0; j + 1 < t; ++j)\n        apply_transition"),
+    "decode_fox_bias_includes_own_gate": (
+        "        logit[j] = scale * dot(kc + j * d, q_t, d) + bias;\n"
+        "        if (lf)\n"
+        "            bias += lf[j];\n",
+        "        if (lf)\n"
+        "            bias += lf[j];\n"
+        "        logit[j] = scale * dot(kc + j * d, q_t, d) + bias;\n"),
     "kcache_sum_not_product": ("Mw[r] = dot(M + r * d, wh + j * d, d);", "Mw[r] = wh[j * d + r];"),
     "kcache_transposed_update": ("M[r * d + c] -= bb[j] * Mw[r] * wh[j * d + c];",
                                  "M[c * d + r] -= bb[j] * Mw[r] * wh[j * d + c];"),
