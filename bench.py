@@ -256,27 +256,39 @@ def e2e_prefill(wlk, steps, warmup, ws, seed=0):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
-def decode_block(wlk, steps, warmup, ws, peaks, seed=0):
+def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
+    """Decode steps over a prefilled cache; with fox, the PaTH-FoX step (the
+    forget-gate prefixes of the cached tokens built by path_attn_fox_prefix)."""
     B, H, d, L0 = wlk.batch, wlk.heads, wlk.head_dim, wlk.prefix_len
     nsteps = steps if steps > 0 else wlk.steps
     cap = L0 + warmup + nsteps
-    x = wl.prefill_inputs(B, H, L0, d, "bf16", seed=seed, device="cuda")
+    x = wl.prefill_inputs(B, H, L0, d, "bf16", seed=seed, fox=fox, device="cuda")
     kc = torch.zeros((B, H, cap, d), device="cuda", dtype=torch.bfloat16)
     vc = torch.zeros_like(kc)
     pa.path_attn_build_kcache(x["k"], x["w"], x["beta"], kc)
     vc[:, :, :L0] = x["v"]
+    fc = None
+    if fox:
+        fc = torch.zeros((B, H, cap), device="cuda", dtype=torch.float32)
+        pa.path_attn_fox_prefix(x["log_f"], fc)
     del x
     torch.cuda.empty_cache()
-    toks = [wl.decode_token(B, H, d, "bf16", seed=10_000 + seed + t, device="cuda")
+    toks = [wl.decode_token(B, H, d, "bf16", seed=10_000 + seed + t, device="cuda", fox=fox)
             for t in range(warmup + nsteps)]
+
+    def step(g, t):
+        if fox:
+            pa.path_attn_decode_step_fox(kc, vc, fc, t, g["q"], g["k"], g["v"], g["w"],
+                                         g["beta"], g["log_f"], out=out, workspace=wsp)
+        else:
+            pa.path_attn_decode_step(kc, vc, t, g["q"], g["k"], g["v"], g["w"], g["beta"],
+                                     out=out, workspace=wsp)
     out = torch.empty((B, H, d), device="cuda", dtype=torch.bfloat16)
     wsz = pa.path_attn_decode_workspace_size(pa.decode_desc(kc))
     wsp = torch.empty(max(wsz, 16), device="cuda", dtype=torch.uint8)
     t = L0
     for i in range(warmup):
-        g = toks[i]
-        pa.path_attn_decode_step(kc, vc, t, g["q"], g["k"], g["v"], g["w"], g["beta"], out=out,
-                                 workspace=wsp)
+        step(toks[i], t)
         t += 1
     stream = torch.cuda.current_stream()
     barrier(ws)
@@ -285,10 +297,10 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0):
     evs[0].record(stream)
     bytes_total = 0
     for i in range(nsteps):
-        g = toks[warmup + i]
-        pa.path_attn_decode_step(kc, vc, t, g["q"], g["k"], g["v"], g["w"], g["beta"], out=out,
-                                 workspace=wsp)
+        step(toks[warmup + i], t)
         bytes_total += 3 * B * H * t * d * 2  # read K, write K, read V
+        if fox:
+            bytes_total += B * H * t * 4  # read each key's forget-gate prefix
         t += 1
         evs[i + 1].record(stream)
     torch.cuda.synchronize()
@@ -298,13 +310,14 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0):
     ms = max_over_ranks(total_ms / nsteps, ws)
     gbs = bytes_total / nsteps / (ms * 1e-3) / 1e9
     peak = peaks["hbm_gbs"]
-    res = {"workload": wlk.name, "tokens_per_s": ws * B / (ms * 1e-3), "ms_per_step": ms,
+    name = wlk.name.replace("PaTH decode", "PaTH-FoX decode") if fox else wlk.name
+    res = {"workload": name, "tokens_per_s": ws * B / (ms * 1e-3), "ms_per_step": ms,
            "steps": nsteps, "hbm_gbs": gbs * ws,
            "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel",
                         "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                         "frac": gbs / peak, "traffic": None,
                         "peak_source": peaks["source"] + " copy bandwidth"}}
-    del kc, vc
+    del kc, vc, fc
     torch.cuda.empty_cache()
     return res
 
@@ -409,6 +422,8 @@ def main():
         extra["fox_4k"], _ = prefill_block(wl.FOX_4K, steps, warmup, ws, peaks)
         extra["long_32k"], _ = prefill_block(wl.PREFILL_32K, max(3, steps // 4), 3, ws, peaks)
         extra["decode_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws, peaks)
+        extra["decode_fox_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws,
+                                               peaks, fox=True)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle

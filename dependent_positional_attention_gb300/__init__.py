@@ -14,7 +14,8 @@ import threading
 
 __all__ = [
     "PathAttnError", "load_library", "path_attn_prefill_fwd", "path_attn_prefill_prep",
-    "path_attn_prefill_scan", "path_attn_decode_step",
+    "path_attn_prefill_scan", "path_attn_decode_step", "path_attn_decode_step_fox",
+    "path_attn_fox_prefix",
     "path_attn_build_kcache", "path_attn_prefill_workspace_size",
     "path_attn_decode_workspace_size", "path_attn_build_kcache_workspace_size",
     "path_attn_device_status", "path_attn_selftest_bounded_wait", "EXPORTED_SYMBOLS",
@@ -30,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "path_attn_prefill_workspace_size", "path_attn_prefill_fwd", "path_attn_prefill_prep",
     "path_attn_prefill_scan",
     "path_attn_decode_workspace_size", "path_attn_decode_step", "path_attn_decode_step_noalloc",
+    "path_attn_decode_step_fox", "path_attn_fox_prefix",
     "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
     "path_attn_device_status", "path_attn_selftest_bounded_wait",
     "path_attn_status_string", "path_attn_last_error", "path_attn_version",
@@ -90,6 +92,10 @@ def load_library(path: str | None = None):
                                               _VP, _VP, _VP, _VP, _SZ, _VP]
         lib.path_attn_decode_step_noalloc.argtypes = [dd, _VP, _VP, ctypes.c_int32, _VP, _VP,
                                                       _VP, _VP, _VP, _VP, _VP]
+        lib.path_attn_decode_step_fox.argtypes = [dd, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP,
+                                                  _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
+        lib.path_attn_fox_prefix.argtypes = [_VP, _VP, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, _VP]
         lib.path_attn_build_kcache_workspace_size.argtypes = [pd]
         lib.path_attn_build_kcache_workspace_size.restype = _SZ
         lib.path_attn_build_kcache.argtypes = [pd, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP,
@@ -258,6 +264,50 @@ def path_attn_decode_step(k_cache, v_cache, cache_len, q_t, k_t, v_t, w_t, beta_
         _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def path_attn_decode_step_fox(k_cache, v_cache, f_cache, cache_len, q_t, k_t, v_t, w_t, beta_t,
+                              log_f_t, out=None, scale=None, workspace=None, stream=None):
+    """One PaTH-FoX decode step (see path_attn_decode_step_fox in
+    include/path_attn.h).  As path_attn_decode_step, plus f_cache: float32
+    [B, H, capacity] of forget-gate log prefixes (slot cache_len is written)
+    and log_f_t: float32 [B, H]."""
+    import torch
+    lib = load_library()
+    B, H, cap, d = k_cache.shape
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", (B, H, cap, d), k_cache.dtype)
+    _need(f_cache, "f_cache", (B, H, cap), torch.float32)
+    for t, n in ((q_t, "q_t"), (k_t, "k_t"), (v_t, "v_t"), (w_t, "w_t")):
+        _need(t, n, (B, H, d), k_cache.dtype)
+    _need(beta_t, "beta_t", (B, H), torch.float32)
+    _need(log_f_t, "log_f_t", (B, H), torch.float32)
+    desc = decode_desc(k_cache, scale)
+    if out is None:
+        out = torch.empty_like(q_t)
+    _need(out, "out", (B, H, d), k_cache.dtype)
+    if workspace is None:
+        n = path_attn_decode_workspace_size(desc)
+        workspace = torch.empty(max(n, 16), device=k_cache.device, dtype=torch.uint8)
+    _check(lib.path_attn_decode_step_fox(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(f_cache), int(cache_len),
+        _ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(log_f_t), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def path_attn_fox_prefix(log_f, f_out, stream=None):
+    """f_out[b, h, i] = sum_{s<=i} log_f[b, h, s] for i < L, the last value
+    repeated beyond (see path_attn_fox_prefix in include/path_attn.h).
+    log_f: float32 [B, H, L]; f_out: float32 [B, H, capacity >= L]."""
+    import torch
+    lib = load_library()
+    B, H, L = log_f.shape
+    _need(log_f, "log_f", (B, H, L), torch.float32)
+    cap = f_out.shape[2]
+    _need(f_out, "f_out", (B, H, cap), torch.float32)
+    _check(lib.path_attn_fox_prefix(_ptr(log_f), _ptr(f_out), B * H, L, cap, _stream(stream)))
+    return f_out
 
 
 def path_attn_decode_step_noalloc(k_cache, v_cache, cache_len, q_t, k_t, v_t, w_t, beta_t,

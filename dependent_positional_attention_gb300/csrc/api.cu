@@ -369,6 +369,57 @@ path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cach
     return cuda_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)), "decode launch");
 }
 
+path_status_t path_attn_decode_step_fox(const path_decode_desc_t *desc, void *k_cache,
+                                        void *v_cache, float *f_cache, int32_t cache_len,
+                                        const void *q_t, const void *k_t, const void *v_t,
+                                        const void *w_t, const float *beta_t,
+                                        const float *log_f_t, void *out, void *workspace,
+                                        size_t workspace_bytes, path_stream_t stream) {
+    DecodePlan p;
+    path_status_t s = plan_decode(desc, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {k_cache, v_cache, q_t, k_t, v_t, w_t, beta_t, out, workspace};
+    const char *names[] = {"k_cache", "v_cache", "q_t", "k_t", "v_t", "w_t", "beta_t", "out",
+                           "workspace"};
+    for (int i = 0; i < 9; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (!f_cache) return fail(PATH_ERR_INVALID_ARG, "f_cache is NULL");
+    if (!log_f_t) return fail(PATH_ERR_INVALID_ARG, "log_f_t is NULL");
+    if ((reinterpret_cast<uintptr_t>(f_cache) & 3u) || (reinterpret_cast<uintptr_t>(log_f_t) & 3u))
+        return fail(PATH_ERR_INVALID_ARG, "f_cache and log_f_t must be 4-byte aligned");
+    if (cache_len < 0 || cache_len >= desc->cache_capacity)
+        return fail(PATH_ERR_INVALID_ARG, "cache_len %d outside [0, capacity %d)", cache_len,
+                    desc->cache_capacity);
+    if (workspace_bytes < p.ws_bytes)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.ws_bytes);
+    DecodeArgs a;
+    a.k_cache = k_cache; a.v_cache = v_cache; a.q_t = q_t; a.k_t = k_t; a.v_t = v_t;
+    a.w_t = w_t; a.beta_t = beta_t; a.out = out;
+    a.partials = static_cast<float *>(workspace);
+    a.scale = desc->scale;
+    a.BH = p.BH; a.d = desc->head_dim; a.cap = desc->cache_capacity; a.cache_len = cache_len;
+    a.keys_per_split = p.keys_per_split; a.max_splits = p.max_splits;
+    a.f_cache = f_cache; a.log_f_t = log_f_t;
+    return cuda_status(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)),
+                       "FoX decode launch");
+}
+
+path_status_t path_attn_fox_prefix(const float *log_f, float *f_out, int32_t heads_total,
+                                   int32_t len, int32_t out_len, path_stream_t stream) {
+    if (!log_f || !f_out) return fail(PATH_ERR_INVALID_ARG, "log_f and f_out must be non-NULL");
+    if (heads_total < 1 || len < 1 || out_len < len)
+        return fail(PATH_ERR_INVALID_ARG,
+                    "need heads_total >= 1 and 1 <= len <= out_len (got %d, %d, %d)",
+                    heads_total, len, out_len);
+    return cuda_status(launch_fox_prefix(log_f, f_out, len, out_len, heads_total,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                       "FoX prefix launch");
+}
+
 size_t path_attn_build_kcache_workspace_size(const path_prefill_desc_t *desc) {
     KcachePlan p;
     if (plan_kcache(desc, &p) != PATH_OK) return 0;

@@ -72,10 +72,22 @@ __device__ __forceinline__ float group_sum(float v) {
 }
 
 constexpr int kDecThreads = 256;
-constexpr int kDecUnroll = 4;
+// Keys in flight per thread and loop iteration: 8 for the PaTH step (88% of
+// measured HBM copy bandwidth on GB300 at a 64K-token cache, against 76% with
+// 4); the PaTH-FoX step, which also loads each key's forget-gate prefix, runs
+// best with 4 (84% against 66% with 8).
+template <bool FOX>
+__host__ __device__ constexpr int dec_unroll() { return FOX ? 4 : 8; }
 
-template <int D>
+// F_t = F_{t-1} + log f_t of the new token (PaTH-FoX), F_{-1} = 0.
+__device__ __forceinline__ float fox_prefix_now(const DecodeArgs &a, int bh) {
+    const float *fc = a.f_cache + (size_t)bh * a.cap;
+    return (a.cache_len > 0 ? fc[a.cache_len - 1] : 0.f) + a.log_f_t[bh];
+}
+
+template <int D, bool FOX>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a) {
+    constexpr int UNROLL = dec_unroll<FOX>();
     constexpr int LPK = D / 8;                      // lanes per key
     constexpr int KPW = 32 / LPK;                   // keys per warp per load
     constexpr int GROUPS = (kDecThreads / 32) * KPW;  // key groups per CTA
@@ -100,6 +112,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a)
     for (int i = 0; i < 8; ++i) qw = fmaf(q[i], w[i], qw);
     qw = group_sum<LPK>(qw);
     const float sl2 = a.scale * kLog2e;
+    // PaTH-FoX: key j's logit gains sum_{s=j+1}^{t} log f_s = F_t - F_j
+    const float *fc = FOX ? a.f_cache + (size_t)bh * a.cap : nullptr;
+    const float Ft = FOX ? fox_prefix_now(a, bh) : 0.f;
 
     __nv_bfloat16 *kc = static_cast<__nv_bfloat16 *>(a.k_cache) + (size_t)bh * a.cap * D + sub * 8;
     const __nv_bfloat16 *vc =
@@ -109,22 +124,25 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.f;
 
-    for (int base = j0; base < j1; base += GROUPS * kDecUnroll) {
-        uint4 kr[kDecUnroll], vr[kDecUnroll];
+    for (int base = j0; base < j1; base += GROUPS * UNROLL) {
+        uint4 kr[UNROLL], vr[UNROLL];
+        float fj[UNROLL];
 #pragma unroll
-        for (int u = 0; u < kDecUnroll; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int j = base + g + u * GROUPS;
             if (j < j1) {
                 kr[u] = *reinterpret_cast<const uint4 *>(kc + (size_t)j * D);
                 vr[u] = ld_stream(vc + (size_t)j * D);
+                if (FOX) fj[u] = fc[j];
             } else {
                 kr[u] = make_uint4(0, 0, 0, 0);
                 vr[u] = make_uint4(0, 0, 0, 0);
+                if (FOX) fj[u] = 0.f;
             }
         }
-        float s[kDecUnroll];
+        float s[UNROLL];
 #pragma unroll
-        for (int u = 0; u < kDecUnroll; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const int j = base + g + u * GROUPS;
             float k[8];
             unpack8(kr[u], k);
@@ -140,11 +158,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a)
 #pragma unroll
             for (int i = 0; i < 8; ++i) k[i] = fmaf(-ba, w[i], k[i]);
             if (j < j1) st_stream(kc + (size_t)j * D, pack8(k));
-            s[u] = (j < j1) ? sl2 * fmaf(-ba, qw, pb) : -INFINITY;
+            float sj = sl2 * fmaf(-ba, qw, pb);
+            if (FOX) sj = fmaf(Ft - fj[u], kLog2e, sj);  // difference first: no cancellation
+            s[u] = (j < j1) ? sj : -INFINITY;
         }
         float mnew = m;
 #pragma unroll
-        for (int u = 0; u < kDecUnroll; ++u) mnew = fmaxf(mnew, s[u]);
+        for (int u = 0; u < UNROLL; ++u) mnew = fmaxf(mnew, s[u]);
         // mref keeps exp2 finite while no valid key has been seen (then every
         // term is exp2(-inf) = 0 and the state stays empty).
         const float mref = (mnew == -INFINITY) ? 0.f : mnew;
@@ -153,7 +173,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] *= alpha;
 #pragma unroll
-        for (int u = 0; u < kDecUnroll; ++u) {
+        for (int u = 0; u < UNROLL; ++u) {
             const float p = exp2f(s[u] - mref);
             l += p;
             float v[8];
@@ -190,7 +210,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a)
     }
 }
 
-template <int D>
+template <int D, bool FOX>
 __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int nsplit) {
     __shared__ float red[D / 32];
     const int bh = blockIdx.x, dim = threadIdx.x;
@@ -222,6 +242,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a, int nsp
     const size_t slot = ((size_t)bh * a.cap + a.cache_len) * D + dim;
     static_cast<__nv_bfloat16 *>(a.k_cache)[slot] = kt[dim];
     static_cast<__nv_bfloat16 *>(a.v_cache)[slot] = vt[dim];
+    if (FOX && dim == 0) a.f_cache[(size_t)bh * a.cap + a.cache_len] = fox_prefix_now(a, bh);
 }
 
 // ------------------------------------------------------------ key-cache build
@@ -357,14 +378,21 @@ __global__ void __launch_bounds__(kThreads) kc_apply_kernel(KcacheArgs a) {
 
 int decode_keys_per_split() { return 1024; }
 
+template <int D, bool FOX>
+void launch_decode_t(const DecodeArgs &a, int nsplit, cudaStream_t st) {
+    if (nsplit > 0) decode_split_kernel<D, FOX><<<dim3(nsplit, a.BH), kDecThreads, 0, st>>>(a);
+    decode_combine_kernel<D, FOX><<<a.BH, D, 0, st>>>(a, nsplit);
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
     const int nsplit = (a.cache_len + a.keys_per_split - 1) / a.keys_per_split;
+    const bool fox = a.f_cache != nullptr;
     if (a.d == 128) {
-        if (nsplit > 0) decode_split_kernel<128><<<dim3(nsplit, a.BH), kDecThreads, 0, st>>>(a);
-        decode_combine_kernel<128><<<a.BH, 128, 0, st>>>(a, nsplit);
+        if (fox) launch_decode_t<128, true>(a, nsplit, st);
+        else launch_decode_t<128, false>(a, nsplit, st);
     } else {
-        if (nsplit > 0) decode_split_kernel<64><<<dim3(nsplit, a.BH), kDecThreads, 0, st>>>(a);
-        decode_combine_kernel<64><<<a.BH, 64, 0, st>>>(a, nsplit);
+        if (fox) launch_decode_t<64, true>(a, nsplit, st);
+        else launch_decode_t<64, false>(a, nsplit, st);
     }
     return cudaGetLastError();
 }

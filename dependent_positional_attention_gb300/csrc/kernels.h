@@ -48,6 +48,10 @@ struct DecodeArgs {
     float *partials;  // [BH][max_splits][d + 2]: m (log2 units), l, o[d]
     float scale;
     int BH, d, cap, cache_len, keys_per_split, max_splits;
+    // PaTH-FoX: f_cache [BH][cap] holds F_j = sum_{s<=j} log f_s of the cached
+    // tokens (slot cache_len is written by the step); log_f_t [BH].  Null for PaTH.
+    float *f_cache = nullptr;
+    const float *log_f_t = nullptr;
 };
 
 int decode_keys_per_split();

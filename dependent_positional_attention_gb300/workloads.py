@@ -89,9 +89,10 @@ def workload_inputs(wl: PrefillWorkload, seed=0, device="cpu"):
                           wl.beta_mu, wl.fox, device)
 
 
-def decode_token(batch, heads, head_dim, dtype="bf16", seed=0, device="cpu"):
-    """One decode step's q_t, k_t, v_t, w_t ([B,H,d]) and beta_t ([B,H])."""
-    d = prefill_inputs(batch, heads, 1, head_dim, dtype, seed, device=device)
+def decode_token(batch, heads, head_dim, dtype="bf16", seed=0, device="cpu", fox=False):
+    """One decode step's q_t, k_t, v_t, w_t ([B,H,d]), beta_t ([B,H]) and,
+    for PaTH-FoX, log_f_t ([B,H])."""
+    d = prefill_inputs(batch, heads, 1, head_dim, dtype, seed, fox=fox, device=device)
     return {n: t.squeeze(2).contiguous() for n, t in d.items()}
 
 

@@ -151,6 +151,41 @@ path_status_t path_attn_decode_step(const path_decode_desc_t *desc, void *k_cach
                                     size_t workspace_bytes, path_stream_t stream);
 
 /*
+ * One PaTH-FoX decode step: path_attn_decode_step with the forget-gate bias
+ * of the PaTH-FoX combination (section "2. 방법론: PaTH Attention", FoX; at
+ * inference, section "3. 효율적인 학습 및 추론").  The logit of cached key
+ * j < t gains sum_{s=j+1}^{t} log f_s; the new token's own logit gains
+ * nothing.  The bias is kept as a prefix per key:
+ *   f_cache    float32 [batch, heads, cache_capacity], f_cache[j] =
+ *              F_j = sum_{s<=j} log f_s for j < cache_len (read); the step
+ *              writes F_t = F_{t-1} + log_f_t at slot cache_len (F_{-1} = 0),
+ *              so the bias is F_t - F_j.  After a prefill, fill it with
+ *              path_attn_fox_prefix.
+ *   log_f_t    float32 [batch, heads]: log of the new token's forget gate.
+ * Every other argument, the layouts, ownership, errors and the in-place
+ * update are those of path_attn_decode_step.  f_cache and log_f_t need 4-byte
+ * alignment.
+ */
+path_status_t path_attn_decode_step_fox(const path_decode_desc_t *desc, void *k_cache,
+                                        void *v_cache, float *f_cache, int32_t cache_len,
+                                        const void *q_t, const void *k_t, const void *v_t,
+                                        const void *w_t, const float *beta_t,
+                                        const float *log_f_t, void *out, void *workspace,
+                                        size_t workspace_bytes, path_stream_t stream);
+
+/*
+ * Prefix sums of forget-gate logs for the PaTH-FoX decode cache:
+ *   f_out[h][i] = sum_{s<=i} log_f[h][s]   for i < len,
+ *   f_out[h][i] = f_out[h][len-1]          for len <= i < out_len,
+ * summed in fp64, stored as float32.  log_f: [heads_total][len], f_out:
+ * [heads_total][out_len] (heads_total = batch * heads), device pointers,
+ * caller-owned.  Asynchronous on `stream`.  PATH_ERR_INVALID_ARG for NULL
+ * pointers or sizes outside 1 <= len <= out_len, heads_total >= 1.
+ */
+path_status_t path_attn_fox_prefix(const float *log_f, float *f_out, int32_t heads_total,
+                                   int32_t len, int32_t out_len, path_stream_t stream);
+
+/*
  * path_attn_decode_step without a workspace, for callers that cannot
  * allocate device memory: plugins running inside a host framework that owns
  * all GPU memory and gives them no allocator, and token loops that must not

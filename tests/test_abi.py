@@ -98,3 +98,21 @@ def test_noalloc_decode_rejects_steps_beyond_its_fixed_scratch(lib):
     small = pa.DecodeDesc(1, 1, 128, 16, 1, 0.088)
     assert lib.path_attn_decode_step_noalloc(ctypes.byref(small), FAKE, FAKE, 16, FAKE, FAKE,
                                              FAKE, FAKE, FAKE, FAKE, None) == pa.PATH_ERR_INVALID_ARG
+
+
+def test_fox_decode_and_prefix_reject_bad_arguments(lib):
+    """Rejected before any CUDA call, so this runs without a GPU."""
+    desc = pa.DecodeDesc(1, 2, 128, 64, 1, 0.088)
+    ws = lib.path_attn_decode_workspace_size(ctypes.byref(desc))
+    args = [FAKE, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None]
+    for i, name in ((2, b"f_cache"), (9, b"log_f_t")):
+        bad = list(args)
+        bad[i] = None
+        assert lib.path_attn_decode_step_fox(ctypes.byref(desc), *bad) == pa.PATH_ERR_INVALID_ARG
+        assert name in lib.path_attn_last_error()
+    bad = list(args)
+    bad[3] = 64  # cache full: no slot for the new token
+    assert lib.path_attn_decode_step_fox(ctypes.byref(desc), *bad) == pa.PATH_ERR_INVALID_ARG
+    assert lib.path_attn_fox_prefix(FAKE, FAKE, 2, 10, 5, None) == pa.PATH_ERR_INVALID_ARG
+    assert lib.path_attn_fox_prefix(None, FAKE, 2, 10, 10, None) == pa.PATH_ERR_INVALID_ARG
+    assert lib.path_attn_fox_prefix(FAKE, FAKE, 0, 10, 10, None) == pa.PATH_ERR_INVALID_ARG
