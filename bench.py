@@ -352,6 +352,15 @@ class OracleSampler:
 
 # ----------------------------------------------------------------- main
 
+def workload_config(head, ws):
+    """The `config` object of the JSON line (both arms report the same one)."""
+    return {"workload": head.name, "batch_per_gpu": head.batch, "heads": head.heads,
+            "seq_len": head.seq_len, "head_dim": head.head_dim, "chunk": CHUNK,
+            "l2": "inputs larger than L2 (%.0f MB read per step)"
+                  % (5 * head.batch * head.heads * head.seq_len * head.head_dim * 2 / 1e6),
+            "parallelism": "replicas" if ws > 1 else "single"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,8 +402,7 @@ def main():
                 "n_gpus": args.gpus, "steps": steps, "warmup": warm,
                 "ms_per_step": 1e3 * t_tot / steps, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": head.name, "batch": head.batch, "heads": head.heads,
-                           "seq_len": head.seq_len, "head_dim": head.head_dim},
+                "config": workload_config(head, ws),
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
                                  "kind": "oracle",
                                  "sample": "%d uniformly sampled query rows of 2 heads per step"
@@ -445,11 +453,7 @@ def main():
         "n_gpus": ws, "steps": steps, "warmup": warmup, "ms_per_step": main_res["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": head.name, "batch_per_gpu": head.batch, "heads": head.heads,
-                   "seq_len": head.seq_len, "head_dim": head.head_dim, "chunk": CHUNK,
-                   "l2": "inputs larger than L2 (%.0f MB read per step)"
-                         % (5 * head.batch * head.heads * head.seq_len * head.head_dim * 2 / 1e6),
-                   "parallelism": "replicas" if ws > 1 else "single"},
+        "config": workload_config(head, ws),
         "tflops": main_res["tflops"], "prep_ms": main_res["prep_ms"],
         "scan_ms": main_res["scan_ms"], "roofline": main_res["roofline"],
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
