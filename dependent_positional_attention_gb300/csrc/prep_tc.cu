@@ -12,25 +12,29 @@
 //   Pm = I - W^T Wt                            (chunk product H_first...H_last,
 //                                               as the d x d matrix applied to
 //                                               carried query rows: q <- q Pm)
-// with M_le[r][s] = s <= r and M_gt[r][s] = s > r.  Nine 128 x 128 x 128
+// with M_le[r][s] = s <= r and M_gt[r][s] = s > r.  Eleven 128 x 128 x 128
 // contractions run as tcgen05 MMAs (bf16 operands, fp32 accumulation in
-// TMEM); T is solved in fp32 on the CUDA cores by forward substitution, two
-// threads per column.  Persistent CTAs, one chunk at a time.
+// TMEM).  T is solved blockwise in fp32: the 16 x 16 diagonal blocks by
+// forward substitution on the CUDA cores, their merges (T21 = -T22 G21 T11)
+// as TF32 mma.sync products with a hi/lo split (about fp32 accuracy).
+// Persistent CTAs, one chunk at a time.
 //
 // Phases per chunk (one thread issues TMA and MMAs; waits are bounded):
-//   P1 TMA Q,K,W; MMA G->cols 0, QW->128, KW->256, QK->384
-//   P2 G -> fp32 smem
+//   P1 TMA W, then Q and K; MMA G -> cols 0 alone (so the solve can start),
+//      then QW -> 128, KW -> 256, QK -> 384; the next chunk's boxes are
+//      prefetched into L2
+//   P2 G -> fp32 smem (swizzled)
 //   P3 solve T (fp32 smem)
 //   P4 T -> bf16 tile, -(M_le*QW) -> bf16 tile, (M_gt*KW) -> bf16 tile
 //   P5 MMA Wt = T W -> cols 0, Y = (M_gt*KW) T^T -> cols 256
 //   P6 Wt -> bf16 tile, Y -> bf16 tile
 //   P7 MMA -(M_le*QW) Wt -> cols 128, Y W -> cols 0, += -(M_le*QW) Y^T -> cols 384,
 //      W^T Wt -> cols 256   (the chunk's V is loaded meanwhile)
-//   P8 Qh, Kh, Pm -> workspace
+//   P8 Qh, Kh, Pm over their dead operand tiles, stored by TMA
 //   P9 causal softmax of the within-chunk logits (cols 384) -> P bf16 tile;
 //      MMA P V -> cols 256
-//   P10 the chunk's own attention output (normalised, bf16) and its log-sum-exp
-//      -> workspace; the scan starts every query tile from them
+//   P10 the chunk's own attention output (normalised, bf16, stored by TMA) and
+//      its log-sum-exp -> workspace; the scan starts every query tile from them
 
 #include "common.cuh"
 #include "kernels.h"
