@@ -63,7 +63,8 @@ int num_sms() {
 
 struct PrefillPlan {
     int BH, L, Lp, N, C, d;
-    bool bf16;
+    bool bf16;  // bf16 inputs and output
+    bool tc;    // the tensor-core route (bf16, head_dim 128, chunk 128); else CUDA cores
     size_t esize;
     size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, total;
 };
@@ -80,17 +81,18 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     if (BH > 65535) return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
     p->bf16 = desc->dtype == PATH_BF16;
     p->d = desc->head_dim;
-    if (p->bf16) {
-        if (p->d != 128) return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 needs head_dim == 128");
+    p->tc = p->bf16 && p->d == 128;
+    if (p->tc) {
         if (desc->chunk != 0 && desc->chunk != 128)
-            return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 needs chunk 0 or 128");
+            return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 with head_dim 128 needs chunk 0 or 128");
         p->C = 128;
     } else {
+        // CUDA-core route: fp32, or bf16 inputs/output with another head_dim
         if (p->d > 128 || p->d % 4)
-            return fail(PATH_ERR_UNSUPPORTED, "PATH_F32 needs head_dim <= 128, multiple of 4");
+            return fail(PATH_ERR_UNSUPPORTED, "head_dim must be 128, or <= 128 and a multiple of 4");
         int C = desc->chunk ? desc->chunk : 64;
         if (C != 16 && C != 32 && C != 64 && C != 128)
-            return fail(PATH_ERR_UNSUPPORTED, "PATH_F32 chunk must be 16, 32, 64 or 128");
+            return fail(PATH_ERR_UNSUPPORTED, "chunk must be 16, 32, 64 or 128");
         p->C = C;
     }
     p->BH = (int)BH;
@@ -98,7 +100,7 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     p->N = (p->L + p->C - 1) / p->C;
     if ((long long)p->N * p->C > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
     p->Lp = p->N * p->C;
-    p->esize = p->bf16 ? 2 : 4;
+    p->esize = p->tc ? 2 : 4;  // the CUDA-core route keeps an fp32 workspace
     const size_t rows = (size_t)p->BH * p->Lp;
     const size_t cc = (size_t)p->BH * p->N * p->C * p->C;
     size_t off = 0;
@@ -108,7 +110,7 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     p->off_Sd = off; off = align_up(off + cc * 4, 256);
     p->off_F = off; off = align_up(off + rows * 4, 256);
     // fp32 scratch of the SIMT prep (the tensor-core prep keeps it on chip)
-    p->off_scratch = off; off = align_up(off + (p->bf16 ? 0 : cc * 5 * 4), 256);
+    p->off_scratch = off; off = align_up(off + (p->tc ? 0 : cc * 5 * 4), 256);
     p->total = off;
     return ok();
 }
@@ -225,7 +227,7 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
             "fox prefix launch");
         if (s != PATH_OK) return s;
     }
-    if (p.bf16) {
+    if (p.tc) {
         PrepTcMaps maps;
         const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.L, p.BH, 64, 128) &&
                          encode_tmap_bf16_3d(&maps.k, k, 128, p.L, p.BH, 64, 128) &&
@@ -263,7 +265,7 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
     pa.scratch = at<float>(workspace, p.off_scratch);
     pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
     pa.keys_only = 0;
-    return cuda_status(launch_prep_simt(pa, false, false, st), "prep launch");
+    return cuda_status(launch_prep_simt(pa, p.bf16, false, st), "prep launch");
 }
 
 path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void *w,
@@ -289,7 +291,7 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
     const void *Wt = at<char>(workspace, p.off_Wt);
     const float *Sd = at<float>(workspace, p.off_Sd);
     const float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
-    if (p.bf16) {
+    if (p.tc) {
         FlashTcMaps maps;
         const bool enc =
             encode_tmap_bf16_3d(&maps.qh, Qh, 128, p.Lp, p.BH, 64, 128) &&
@@ -312,7 +314,7 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
     fa.Qh = Qh; fa.Kh = Kh; fa.Wt = Wt; fa.w = w; fa.v = v;
     fa.Sd = Sd; fa.F = F; fa.out = out; fa.lse = lse; fa.scale = desc->scale;
     fa.BH = p.BH; fa.L = p.L; fa.Lp = p.Lp; fa.N = p.N; fa.C = p.C; fa.d = p.d;
-    return cuda_status(launch_flash_simt(fa, st), "scan launch");
+    return cuda_status(launch_flash_simt(fa, p.bf16, st), "scan launch");
 }
 
 path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void *q,

@@ -38,7 +38,8 @@ cudaError_t launch_prep_simt(const PrepSimtArgs &a, bool bf16_in, bool bf16_out,
                              cudaStream_t st);
 cudaError_t launch_fox_prefix(const float *log_f, float *F, int L, int Lp, int BH,
                               cudaStream_t st);
-cudaError_t launch_flash_simt(const FlashSimtArgs &a, cudaStream_t st);
+// bf16_io: w, v and out in bf16 (the workspace stays fp32)
+cudaError_t launch_flash_simt(const FlashSimtArgs &a, bool bf16_io, cudaStream_t st);
 
 struct DecodeArgs {
     void *k_cache, *v_cache;

@@ -160,6 +160,9 @@ __global__ void fox_prefix_kernel(const float *log_f, float *F, int L, int Lp, i
 
 // ------------------------------------------------------------------ scan
 
+// TIO: element type of w, v and out (float, or bf16 for bf16 inputs whose head
+// dimension the tensor-core route does not take); Qh, Kh, Wt, Sd are fp32.
+template <class TIO>
 __global__ void __launch_bounds__(kThreads) flash_simt_kernel(FlashSimtArgs a) {
     extern __shared__ float smem[];
     const int C = a.C, d = a.d, L = a.L;
@@ -174,8 +177,8 @@ __global__ void __launch_bounds__(kThreads) flash_simt_kernel(FlashSimtArgs a) {
     const float *Qh = static_cast<const float *>(a.Qh) + ((size_t)bh * a.Lp + (size_t)b * C) * d;
     const float *Kh = static_cast<const float *>(a.Kh) + (size_t)bh * a.Lp * d;
     const float *Wt = static_cast<const float *>(a.Wt) + (size_t)bh * a.Lp * d;
-    const float *W = static_cast<const float *>(a.w) + (size_t)bh * L * d;
-    const float *V = static_cast<const float *>(a.v) + (size_t)bh * L * d;
+    const TIO *W = static_cast<const TIO *>(a.w) + (size_t)bh * L * d;
+    const TIO *V = static_cast<const TIO *>(a.v) + (size_t)bh * L * d;
     const float *Sd = a.Sd + ((size_t)bh * a.N + b) * C * C;
     const float *F = a.F ? a.F + (size_t)bh * a.Lp : nullptr;
 
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) flash_simt_kernel(FlashSimtArgs a) {
                 zero(acc);
                 block_gemm<false, true>(
                     acc, C, C, d, [&](int r, int m) { return Qt[r * d + m]; },
-                    [&](int m, int s) { return W[(size_t)(k0 + s) * d + m]; }, sA, sB);
+                    [&](int m, int s) { return to_f32(W[(size_t)(k0 + s) * d + m]); }, sA, sB);
                 for_owned(acc, C, C, [&](int r, int s, float v) { X[r * C + s] = v; });
             }
         }
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) flash_simt_kernel(FlashSimtArgs a) {
         }
         block_gemm<true, false>(
             o, C, d, C, [&](int r, int j) { return S[r * C + j]; },
-            [&](int j, int m) { return (k0 + j < L) ? V[(size_t)(k0 + j) * d + m] : 0.f; }, sA,
+            [&](int j, int m) { return (k0 + j < L) ? to_f32(V[(size_t)(k0 + j) * d + m]) : 0.f; }, sA,
             sB);
         if (c >= 1 && c < b) {
             zero(acc);
@@ -257,8 +260,9 @@ __global__ void __launch_bounds__(kThreads) flash_simt_kernel(FlashSimtArgs a) {
         }
         __syncthreads();
     }
-    float *out = static_cast<float *>(a.out) + ((size_t)bh * L + (size_t)b * C) * d;
-    for_owned(o, nq, d, [&](int r, int m, float v) { out[(size_t)r * d + m] = v / rowl[r]; });
+    TIO *out = static_cast<TIO *>(a.out) + ((size_t)bh * L + (size_t)b * C) * d;
+    for_owned(o, nq, d,
+              [&](int r, int m, float v) { out[(size_t)r * d + m] = from_f32<TIO>(v / rowl[r]); });
     if (a.lse)
         for (int r = threadIdx.x; r < nq; r += kThreads)
             a.lse[(size_t)bh * L + (size_t)b * C + r] = rowm[r] + logf(rowl[r]);
@@ -295,11 +299,13 @@ cudaError_t launch_fox_prefix(const float *log_f, float *F, int L, int Lp, int B
     return cudaGetLastError();
 }
 
-cudaError_t launch_flash_simt(const FlashSimtArgs &a, cudaStream_t st) {
+cudaError_t launch_flash_simt(const FlashSimtArgs &a, bool bf16_io, cudaStream_t st) {
     dim3 grid(a.N, a.BH);
     size_t sm = flash_simt_smem(a.C, a.d);
-    cudaFuncSetAttribute(flash_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    flash_simt_kernel<<<grid, kThreads, sm, st>>>(a);
+    void (*kern)(FlashSimtArgs) =
+        bf16_io ? flash_simt_kernel<__nv_bfloat16> : flash_simt_kernel<float>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    kern<<<grid, kThreads, sm, st>>>(a);
     return cudaGetLastError();
 }
 

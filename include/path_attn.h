@@ -57,8 +57,8 @@ typedef struct {
     int32_t batch, heads, seq_len, head_dim;
     int32_t dtype;  /* path_dtype_t */
     float scale;    /* multiplies k^T(...)q; usually 1/sqrt(head_dim) */
-    int32_t chunk;  /* 0 = default. PATH_F32: 16, 32, 64 or 128 (default 64).
-                       PATH_BF16: 128 only. */
+    int32_t chunk;  /* 0 = default. PATH_BF16 with head_dim 128: 128 only.
+                       Otherwise 16, 32, 64 or 128 (default 64). */
 } path_prefill_desc_t;
 
 /*
@@ -81,9 +81,11 @@ size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc);
  *                the causal row (logits include scale and FoX bias), or NULL.
  *   workspace  : device buffer of at least
  *                path_attn_prefill_workspace_size(desc) bytes.
- * Supported: PATH_F32 with head_dim <= 128 (multiple of 4); PATH_BF16 with
- * head_dim == 128.  seq_len may be any value >= 1 (the last chunk may be
- * partial).  Method: section 3 of the PaTH summary — a per-chunk UT
+ * Supported: head_dim <= 128 and a multiple of 4, PATH_F32 or PATH_BF16.
+ * PATH_BF16 with head_dim 128 runs on the tensor cores (chunk 128); every
+ * other case runs on the CUDA cores in fp32 (bf16 inputs and output are
+ * converted on load and store).  seq_len may be any value >= 1 (the last
+ * chunk may be partial).  Method: section 3 of the PaTH summary — a per-chunk UT
  * transform builds boundary-adjusted rows and the compact chunk product,
  * then a blockwise scan visits key chunks right to left, carrying the
  * accumulated product on the query side, with an online softmax.

@@ -55,7 +55,11 @@ def test_prefill_rejects_bad_descriptors(lib):
     assert prefill(lib, D(1, 1, 0, 64, 0, 0.1, 0)) == pa.PATH_ERR_INVALID_ARG
     assert prefill(lib, D(1, 1, 16, 64, 7, 0.1, 0)) == pa.PATH_ERR_INVALID_ARG
     assert prefill(lib, D(1, 1, 16, 64, 0, float("nan"), 0)) == pa.PATH_ERR_INVALID_ARG
-    assert prefill(lib, D(1, 1, 16, 64, 1, 0.1, 0)) == pa.PATH_ERR_UNSUPPORTED  # bf16 d=64
+    assert prefill(lib, D(1, 1, 16, 66, 1, 0.1, 0)) == pa.PATH_ERR_UNSUPPORTED  # bf16 d=66
+    # bf16 with a head_dim other than 128 takes the CUDA-core route: a valid
+    # descriptor, rejected here only for the (deliberately tiny) workspace
+    assert prefill(lib, D(1, 1, 16, 64, 1, 0.1, 0), ws_bytes=16) == pa.PATH_ERR_INVALID_ARG
+    assert b"workspace" in lib.path_attn_last_error()
     assert prefill(lib, D(1, 1, 16, 130, 0, 0.1, 0)) == pa.PATH_ERR_UNSUPPORTED
     assert prefill(lib, D(1, 1, 16, 64, 0, 0.1, 48)) == pa.PATH_ERR_UNSUPPORTED
     assert prefill(lib, D(1, 1, 16, 128, 1, 0.1, 64)) == pa.PATH_ERR_UNSUPPORTED

@@ -17,10 +17,10 @@ TOL_OUT, TOL_LSE = 2e-2, 1e-2
 DEV = torch.device("cuda:0")
 
 
-def run(x, rows=None):
+def run(x, rows=None, chunk=0):
     g = {n: t.to(DEV) for n, t in x.items()}
     out, lse = pa.path_attn_prefill_fwd(g["q"], g["k"], g["v"], g["w"], g["beta"],
-                                        log_f=g.get("log_f"))
+                                        log_f=g.get("log_f"), chunk=chunk)
     torch.cuda.synchronize()
     assert pa.path_attn_device_status() == 0
     B, H, L, d = x["q"].shape
@@ -83,4 +83,13 @@ def test_full_size_sampled_rows(wname):
     n = w.sampled_rows or 64
     rows = wl.sampled_rows(w.seq_len, n)
     eo, el = run(x, rows=rows)
+    assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
+
+
+@pytest.mark.parametrize("d,L,chunk,fox", [(64, 300, 0, False), (64, 257, 32, True),
+                                           (32, 190, 16, False), (96, 129, 128, False)])
+def test_cuda_core_route_other_head_dims(d, L, chunk, fox):
+    """bf16 inputs with a head_dim the tensor-core route does not take run on
+    the CUDA cores (fp32 inside, bf16 in and out); same tolerance."""
+    eo, el = run(wl.prefill_inputs(2, 2, L, d, "bf16", seed=d + L, fox=fox), chunk=chunk)
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
