@@ -93,3 +93,25 @@ def test_cuda_core_route_other_head_dims(d, L, chunk, fox):
     the CUDA cores (fp32 inside, bf16 in and out); same tolerance."""
     eo, el = run(wl.prefill_inputs(2, 2, L, d, "bf16", seed=d + L, fox=fox), chunk=chunk)
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
+
+
+def test_maximum_batch_heads():
+    """batch * heads at its limit of 65535, one token each: 65535 prep jobs
+    and scan tiles spread over the persistent grids (every tile is a first
+    chunk, whose result is the prep's own block)."""
+    L = 1
+    B, H = 65535 // 5, 5
+    x = wl.prefill_inputs(B, H, L, 128, "bf16", seed=40 + L)
+    g = {n: t.to(DEV) for n, t in x.items()}
+    out, lse = pa.path_attn_prefill_fwd(g["q"], g["k"], g["v"], g["w"], g["beta"])
+    torch.cuda.synchronize()
+    assert pa.path_attn_device_status() == 0
+    # every head is independent: check a spread of heads with the oracle
+    flat = lambda t: t.reshape((B * H,) + tuple(t.shape[2:]))
+    heads = [0, 1, 777, 32768, B * H - 2, B * H - 1]
+    args = [to64(flat(x[n])[heads]) for n in NAMES]
+    ro, rl = oracle.prefill(*args)
+    assert max_err(to64(flat(out)[heads]), ro) <= TOL_OUT
+    assert max_err(to64(flat(lse)[heads]), rl) <= TOL_LSE
+    too_many = pa.PrefillDesc(65536, 1, L, 128, pa.PATH_BF16, 0.088, 0)
+    assert pa.path_attn_prefill_workspace_size(too_many) == 0
