@@ -359,6 +359,17 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
     return res
 
 
+def autotune_block(wlk):
+    """Chunk-size autotune on the CUDA-core route: the chosen chunk and its
+    time against the default chunk."""
+    from dependent_positional_attention_gb300 import autotune
+    best, times = autotune.autotune_chunk(wlk.batch, wlk.heads, wlk.seq_len, wlk.head_dim,
+                                          wlk.dtype)
+    return {"workload": wlk.name, "best_chunk": best,
+            "ms_by_chunk": {str(c): t for c, t in sorted(times.items()) if c},
+            "ms_library_default": times[0], "speedup_vs_default": times[0] / times[best]}
+
+
 class OracleSampler:
     """fp64 oracle on uniformly sampled query rows of a few heads of a
     workload (inputs drawn once, with the workload's seeded generator)."""
@@ -469,6 +480,10 @@ def main():
         extra["decode_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws, peaks)
         extra["decode_fox_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws,
                                                peaks, fox=True)
+        extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
+        extra["chunk_autotune_bf16_d64"] = autotune_block(
+            wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (CUDA-core route)",
+                               8, 12, 4096, 64, "bf16"))
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle

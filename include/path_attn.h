@@ -58,7 +58,9 @@ typedef struct {
     int32_t dtype;  /* path_dtype_t */
     float scale;    /* multiplies k^T(...)q; usually 1/sqrt(head_dim) */
     int32_t chunk;  /* 0 = default. PATH_BF16 with head_dim 128: 128 only.
-                       Otherwise 16, 32, 64 or 128 (default 64). */
+                       Otherwise 16, 32, 64 or 128; the default is 64
+                       when batch*heads*seq_len <= 8192 and head_dim <= 64,
+                       else 128. */
 } path_prefill_desc_t;
 
 /*
