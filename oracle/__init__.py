@@ -56,7 +56,8 @@ def _declare(lib):
                                              _PD, ctypes.c_int]
     lib.path_oracle_boundary_rows.argtypes = [_I64, _I64, _I64, _PD, _PD, _PD, _PD,
                                               _PD, _PD]
-    for f in (lib.path_oracle_prefill, lib.path_oracle_logits,
+    lib.path_oracle_prefill_bwd.argtypes = [_I64, _I64, _I64, _DBL] + [_PD] * 14 + [ctypes.c_int]
+    for f in (lib.path_oracle_prefill, lib.path_oracle_prefill_bwd, lib.path_oracle_logits,
               lib.path_oracle_decode_step, lib.path_oracle_decode_step_fox,
               lib.path_oracle_build_kcache,
               lib.path_oracle_boundary_rows):
@@ -128,6 +129,39 @@ def prefill(q, k, v, w, beta, log_f=None, scale=None, rows=None, nthreads=0,
     if rc != 0:
         raise ValueError("path_oracle_prefill failed: %d" % rc)
     return out.reshape(lead + (nrows, d)), lse.reshape(lead + (nrows,))
+
+
+def prefill_bwd(q, k, v, w, beta, dout, log_f=None, dlse=None, scale=None, nthreads=0,
+                lib=None):
+    """Gradients of sum(dout * out) + sum(dlse * lse) of the PaTH (PaTH-FoX
+    with ``log_f``) forward with respect to every input, by reverse-mode
+    differentiation of the attention-logit equation (section 2, 핵심
+    메커니즘), one transition at a time.  Shapes as ``prefill``; dout:
+    [..., L, d], dlse: [..., L] or None.  Returns a dict with dq, dk, dv, dw,
+    dbeta and (PaTH-FoX) dlog_f."""
+    lib = lib or load()
+    qf, lead = _bh(q, 2)
+    kf, _ = _bh(k, 2)
+    vf, _ = _bh(v, 2)
+    wf, _ = _bh(w, 2)
+    bf, _ = _bh(beta, 1)
+    of, _ = _bh(dout, 2)
+    ff = _bh(log_f, 1)[0] if log_f is not None else None
+    lf = _bh(dlse, 1)[0] if dlse is not None else None
+    BH, L, d = qf.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    g = {n: np.empty((BH, L, d), dtype=np.float64) for n in ("dq", "dk", "dv", "dw")}
+    g["dbeta"] = np.empty((BH, L), dtype=np.float64)
+    if ff is not None:
+        g["dlog_f"] = np.empty((BH, L), dtype=np.float64)
+    rc = lib.path_oracle_prefill_bwd(BH, L, d, float(scale), _p(qf), _p(kf), _p(vf), _p(wf),
+                                     _p(bf), _p(ff), _p(of), _p(lf), _p(g["dq"]), _p(g["dk"]),
+                                     _p(g["dv"]), _p(g["dw"]), _p(g["dbeta"]),
+                                     _p(g.get("dlog_f")), int(nthreads))
+    if rc != 0:
+        raise ValueError("path_oracle_prefill_bwd failed: %d" % rc)
+    return {n: a.reshape(lead + a.shape[1:]) for n, a in g.items()}
 
 
 def logits(q, k, w, beta, log_f=None, scale=None, lib=None):

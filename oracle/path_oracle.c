@@ -25,6 +25,10 @@
  * transition, k_j <- H_t k_j (j < t), and the new key k_t is appended
  * untransformed; attention then reads the cache like ordinary attention.
  *
+ * Backward (path_oracle_prefill_bwd): reverse-mode differentiation of the
+ * same equation, one transition at a time (see row_backward); the pages give
+ * no gradient formulas of their own.
+ *
  * Everything below applies one reflection at a time to a vector.  It never
  * forms the UT / compact-WY representation and never blocks, fuses or
  * reorders the steps of the definition.  lse is the natural log of the sum of
@@ -62,15 +66,18 @@ static void apply_transition(double *u, const double *w, double beta, int64_t d)
  * Logits of query row i of one head, for keys j = 0..i.
  * Walk j from i down to 0.  At key j the running vector equals
  * (H_{j+1} ... H_i) q_i, so the logit is scale * k_j . u; then u moves past
- * position j (u <- H_j u) and the FoX bias picks up log f_j.
+ * position j (u <- H_j u) and the FoX bias picks up log f_j.  If B is not
+ * NULL, row j of B receives the running vector seen by key j.
  */
 static void row_logits(int64_t i, int64_t d, double scale, const double *q_i,
                        const double *k, const double *w, const double *beta,
-                       const double *log_f, double *u, double *logit)
+                       const double *log_f, double *u, double *logit, double *B)
 {
     memcpy(u, q_i, (size_t)d * sizeof(double));
     double bias = 0.0;
     for (int64_t j = i; j >= 0; --j) {
+        if (B)
+            memcpy(B + j * d, u, (size_t)d * sizeof(double));
         logit[j] = scale * dot(k + j * d, u, d) + bias;
         apply_transition(u, w + j * d, beta[j], d);
         if (log_f)
@@ -142,7 +149,7 @@ int path_oracle_prefill(int64_t BH, int64_t L, int64_t d, double scale,
                 const double *vh = v + bh * L * d, *wh = w + bh * L * d;
                 const double *bh_beta = beta + bh * L;
                 const double *bh_f = log_f ? log_f + bh * L : NULL;
-                row_logits(i, d, scale, qh + i * d, kh, wh, bh_beta, bh_f, u, logit);
+                row_logits(i, d, scale, qh + i * d, kh, wh, bh_beta, bh_f, u, logit, NULL);
                 softmax_rows(i + 1, d, logit, vh, out + t * d, lse ? lse + t : NULL);
             }
         }
@@ -167,7 +174,7 @@ int path_oracle_logits(int64_t L, int64_t d, double scale, const double *q,
         return -3;
     for (int64_t i = 0; i < L; ++i) {
         double *row = logits + i * L;
-        row_logits(i, d, scale, q + i * d, k, w, beta, log_f, u, row);
+        row_logits(i, d, scale, q + i * d, k, w, beta, log_f, u, row, NULL);
         for (int64_t j = i + 1; j < L; ++j)
             row[j] = -INFINITY;
     }
@@ -356,4 +363,157 @@ int path_oracle_boundary_rows(int64_t L, int64_t d, int64_t C, const double *q,
             apply_transition(x, w + s * d, beta[s], d);
     }
     return 0;
+}
+
+/*
+ * Gradients of one query row i of one head, added into the head's
+ * accumulators (dk, dv, dw, dbeta, dlog_f) and written to dq_i.
+ *
+ * The backward pass is not spelled out on the pages (the PaTH lecture notes,
+ * open questions, only remark that it costs more than the forward); this is
+ * reverse-mode differentiation of the attention-logit equation, one
+ * transition at a time.  With b_s = H_{s+1} ... H_i q_i (the running vector of
+ * row_logits at key s) and, for j < s, a_{j,s} = H_{s-1} ... H_{j+1} k_j, the
+ * logit is scale * a_{j,s}^T H_s b_s, so
+ *     dL/dH_s = scale * g_s b_s^T,  g_s = sum_{j<s} dlogit_j a_{j,s},
+ * and g obeys g_{s+1} = H_s g_s + dlogit_s k_s (g_0 = 0).  For
+ * H_s = I - beta_s w_s w_s^T that gives
+ *     dbeta_s = -w_s^T (dL/dH_s) w_s,
+ *     dw_s    = -beta_s (dL/dH_s + dL/dH_s^T) w_s,
+ * and dq_i = scale * g_{i+1}, dk_j = scale * dlogit_j b_j.  The softmax part
+ * is the usual one: dlogit_j = p_j (dout_i . v_j - dout_i . out_i + dlse_i).
+ * The FoX bias of logit j is sum_{s=j+1}^{i} log f_s, so
+ * dlog_f_s = sum_{j<s} dlogit_j.
+ */
+static void row_backward(int64_t i, int64_t d, double scale, const double *q_i,
+                         const double *k, const double *v, const double *w,
+                         const double *beta, const double *log_f, const double *dout_i,
+                         double dlse_i, double *B, double *logit, double *dl, double *g,
+                         double *dq_i, double *dk, double *dv, double *dw, double *dbeta,
+                         double *dlog_f)
+{
+    /* the logits, and b_j for j = i..0 */
+    row_logits(i, d, scale, q_i, k, w, beta, log_f, g, logit, B);
+    /* softmax and its gradient */
+    double mx = -INFINITY;
+    for (int64_t j = 0; j <= i; ++j)
+        if (logit[j] > mx)
+            mx = logit[j];
+    double sum = 0.0;
+    for (int64_t j = 0; j <= i; ++j)
+        sum += exp(logit[j] - mx);
+    const double lse = mx + log(sum);
+    double D = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+        double p = exp(logit[j] - lse);
+        double dp = dot(dout_i, v + j * d, d);
+        dl[j] = p * dp;   /* p_j (dout . v_j), finished below */
+        D += p * dp;
+        for (int64_t m = 0; m < d; ++m)
+            dv[j * d + m] += p * dout_i[m];
+    }
+    for (int64_t j = 0; j <= i; ++j) {
+        double p = exp(logit[j] - lse);
+        dl[j] -= p * (D - dlse_i);
+        for (int64_t m = 0; m < d; ++m)
+            dk[j * d + m] += scale * dl[j] * B[j * d + m];
+    }
+    /* left-to-right sweep over the transitions */
+    for (int64_t m = 0; m < d; ++m)
+        g[m] = 0.0;
+    double cum = 0.0;  /* sum_{j<s} dlogit_j */
+    for (int64_t s = 0; s <= i; ++s) {
+        if (s > 0) {
+            const double *ws = w + s * d, *bs = B + s * d;
+            double alpha = dot(ws, g, d), gamma = dot(ws, bs, d);
+            dbeta[s] -= scale * alpha * gamma;
+            for (int64_t m = 0; m < d; ++m)
+                dw[s * d + m] -= beta[s] * scale * (gamma * g[m] + alpha * bs[m]);
+        }
+        if (log_f)
+            dlog_f[s] += cum;
+        cum += dl[s];
+        apply_transition(g, w + s * d, beta[s], d);
+        for (int64_t m = 0; m < d; ++m)
+            g[m] += dl[s] * k[s * d + m];
+    }
+    for (int64_t m = 0; m < d; ++m)
+        dq_i[m] = scale * g[m];
+}
+
+/*
+ * Prefill backward: gradients of sum(dout * out) + sum(dlse * lse) with
+ * respect to q, k, v, w, beta and (PaTH-FoX) log_f.  Same layouts as
+ * path_oracle_prefill; dlse may be NULL (zero); dlog_f is written only when
+ * log_f is given.  Rows of one head run in parallel, each thread with its own
+ * accumulators, summed at the end of the head.
+ */
+int path_oracle_prefill_bwd(int64_t BH, int64_t L, int64_t d, double scale,
+                            const double *q, const double *k, const double *v,
+                            const double *w, const double *beta, const double *log_f,
+                            const double *dout, const double *dlse, double *dq,
+                            double *dk, double *dv, double *dw, double *dbeta,
+                            double *dlog_f, int nthreads)
+{
+    if (BH < 0 || L < 0 || d <= 0)
+        return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const size_t Ld = (size_t)L * d;
+    memset(dk, 0, BH * Ld * sizeof(double));
+    memset(dv, 0, BH * Ld * sizeof(double));
+    memset(dw, 0, BH * Ld * sizeof(double));
+    memset(dbeta, 0, (size_t)(BH * L) * sizeof(double));
+    if (log_f)
+        memset(dlog_f, 0, (size_t)(BH * L) * sizeof(double));
+    int err = 0;
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const double *qh = q + bh * Ld, *kh = k + bh * Ld, *vh = v + bh * Ld;
+        const double *wh = w + bh * Ld, *bb = beta + bh * L, *oh = dout + bh * Ld;
+        const double *fh = log_f ? log_f + bh * L : NULL;
+#pragma omp parallel
+        {
+            size_t n1 = L > 0 ? (size_t)L : 1;
+            double *B = (double *)malloc(n1 * d * sizeof(double));
+            double *logit = (double *)malloc(n1 * sizeof(double));
+            double *dl = (double *)malloc(n1 * sizeof(double));
+            double *g = (double *)malloc((size_t)d * sizeof(double));
+            double *acc = (double *)calloc(3 * n1 * d + 2 * n1, sizeof(double));
+            if (!B || !logit || !dl || !g || !acc) {
+#pragma omp atomic write
+                err = -3;
+            } else {
+                double *adk = acc, *adv = acc + n1 * d, *adw = acc + 2 * n1 * d;
+                double *adb = acc + 3 * n1 * d, *adf = adb + n1;
+#pragma omp for schedule(dynamic, 4)
+                for (int64_t i = 0; i < L; ++i)
+                    row_backward(i, d, scale, qh + i * d, kh, vh, wh, bb, fh, oh + i * d,
+                                 dlse ? dlse[bh * L + i] : 0.0, B, logit, dl, g,
+                                 dq + bh * Ld + i * d, adk, adv, adw, adb, adf);
+#pragma omp critical
+                {
+                    for (size_t e = 0; e < Ld; ++e) {
+                        dk[bh * Ld + e] += adk[e];
+                        dv[bh * Ld + e] += adv[e];
+                        dw[bh * Ld + e] += adw[e];
+                    }
+                    for (int64_t s = 0; s < L; ++s) {
+                        dbeta[bh * L + s] += adb[s];
+                        if (log_f)
+                            dlog_f[bh * L + s] += adf[s];
+                    }
+                }
+            }
+            free(B);
+            free(logit);
+            free(dl);
+            free(g);
+            free(acc);
+        }
+    }
+    return err;
 }

@@ -2,9 +2,9 @@
 
 Each case plants one plausible mistake in a copy of oracle/path_oracle.c
 (a dropped term, a wrong sign, an off-by-one, a misplaced scale), builds it,
-and runs the pin suite (tests/test_oracle.py) against that build.  Every
-mutant must make at least one pin fail; a surviving mutant means the pins
-do not constrain that part of the oracle.
+and runs the pin suites (tests/test_oracle.py, tests/test_oracle_bwd.py)
+against that build.  Every mutant must make at least one pin fail; a
+surviving mutant means the pins do not constrain that part of the oracle.
 """
 import os
 import subprocess
@@ -51,6 +51,27 @@ MUTANTS = {
     "kcache_transposed_update": ("M[r * d + c] -= bb[j] * Mw[r] * wh[j * d + c];",
                                  "M[c * d + r] -= bb[j] * Mw[r] * wh[j * d + c];"),
     "boundary_q_one_short": ("for (int64_t s = i; s >= s0; --s)", "for (int64_t s = i; s > s0; --s)"),
+    # backward
+    "bwd_dlse_dropped": ("dl[j] -= p * (D - dlse_i);", "dl[j] -= p * D;"),
+    "bwd_g_skips_transition": ("        apply_transition(g, w + s * d, beta[s], d);\n", ""),
+    "bwd_dw_one_sided": ("(gamma * g[m] + alpha * bs[m])", "(2.0 * gamma * g[m])"),
+    "bwd_dbeta_sign": ("dbeta[s] -= scale * alpha * gamma;", "dbeta[s] += scale * alpha * gamma;"),
+    "bwd_fox_cum_inclusive": ("            dlog_f[s] += cum;\n        cum += dl[s];",
+                              "            dlog_f[s] += cum + dl[s];\n        cum += dl[s];"),
+    "bwd_dk_unscaled": ("dk[j * d + m] += scale * dl[j] * B[j * d + m];",
+                        "dk[j * d + m] += dl[j] * B[j * d + m];"),
+    "bwd_b_after_transition": (
+        "        if (B)\n"
+        "            memcpy(B + j * d, u, (size_t)d * sizeof(double));\n"
+        "        logit[j] = scale * dot(k + j * d, u, d) + bias;\n"
+        "        apply_transition(u, w + j * d, beta[j], d);\n",
+        "        logit[j] = scale * dot(k + j * d, u, d) + bias;\n"
+        "        apply_transition(u, w + j * d, beta[j], d);\n"
+        "        if (B)\n"
+        "            memcpy(B + j * d, u, (size_t)d * sizeof(double));\n"),
+    "bwd_dq_before_own_key": (
+        "    for (int64_t m = 0; m < d; ++m)\n        dq_i[m] = scale * g[m];",
+        "    for (int64_t m = 0; m < d; ++m)\n        dq_i[m] = scale * (g[m] - dl[i] * k[i * d + m]);"),
 }
 
 
@@ -64,6 +85,7 @@ def test_pins_catch_mutant(name, tmp_path):
     lib = oracle.build(str(mut_src), str(tmp_path / "libmutant.so"), force=True)
     env = dict(os.environ, PATH_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                        os.path.join(ROOT, "tests", "test_oracle.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_bwd.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
