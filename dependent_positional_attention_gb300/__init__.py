@@ -14,7 +14,8 @@ import threading
 
 __all__ = [
     "PathAttnError", "load_library", "path_attn_prefill_fwd", "path_attn_prefill_prep",
-    "path_attn_prefill_scan", "path_attn_decode_step", "path_attn_decode_step_fox",
+    "path_attn_prefill_scan", "path_attn_prefill_bwd", "path_attn_prefill_bwd_workspace_size",
+    "path_attn_decode_step", "path_attn_decode_step_fox",
     "path_attn_fox_prefix",
     "path_attn_build_kcache", "path_attn_prefill_workspace_size",
     "path_attn_decode_workspace_size", "path_attn_build_kcache_workspace_size",
@@ -29,7 +30,7 @@ PATH_F32, PATH_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = (
     "path_attn_prefill_workspace_size", "path_attn_prefill_fwd", "path_attn_prefill_prep",
-    "path_attn_prefill_scan",
+    "path_attn_prefill_scan", "path_attn_prefill_bwd_workspace_size", "path_attn_prefill_bwd",
     "path_attn_decode_workspace_size", "path_attn_decode_step", "path_attn_decode_step_noalloc",
     "path_attn_decode_step_fox", "path_attn_fox_prefix",
     "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
@@ -86,6 +87,9 @@ def load_library(path: str | None = None):
                                               _VP, _SZ, _VP]
         lib.path_attn_prefill_prep.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
         lib.path_attn_prefill_scan.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
+        lib.path_attn_prefill_bwd_workspace_size.argtypes = [pd]
+        lib.path_attn_prefill_bwd_workspace_size.restype = _SZ
+        lib.path_attn_prefill_bwd.argtypes = [pd] + [_VP] * 17 + [_SZ, _VP]
         lib.path_attn_decode_workspace_size.argtypes = [dd]
         lib.path_attn_decode_workspace_size.restype = _SZ
         lib.path_attn_decode_step.argtypes = [dd, _VP, _VP, ctypes.c_int32, _VP, _VP, _VP,
@@ -106,6 +110,7 @@ def load_library(path: str | None = None):
         lib.path_attn_last_error.restype = ctypes.c_char_p
         lib.path_attn_version.restype = ctypes.c_int32
         for f in ("path_attn_prefill_fwd", "path_attn_prefill_prep", "path_attn_prefill_scan",
+                  "path_attn_prefill_bwd",
                   "path_attn_decode_step", "path_attn_decode_step_noalloc",
                   "path_attn_build_kcache",
                   "path_attn_device_status", "path_attn_selftest_bounded_wait"):
@@ -225,6 +230,45 @@ def path_attn_prefill_scan(q, w, v, workspace, log_f=None, out=None, lse=None, s
         ctypes.byref(desc), _ptr(w), _ptr(v), _ptr(log_f), _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
+
+
+def path_attn_prefill_bwd_workspace_size(desc: PrefillDesc) -> int:
+    return int(load_library().path_attn_prefill_bwd_workspace_size(ctypes.byref(desc)))
+
+
+def path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, log_f=None, dlse=None, scale=None,
+                          chunk=0, workspace=None, stream=None):
+    """Backward of path_attn_prefill_fwd (see path_attn_prefill_bwd in
+    include/path_attn.h): gradients of sum(dout * out) + sum(dlse * lse).
+    Tensors as for the forward; out and lse are the forward's outputs.
+    Returns a dict with dq, dk, dv, dw (dtype of q), dbeta and, for PaTH-FoX,
+    dlog_f (float32)."""
+    import torch
+    lib = load_library()
+    B, H, L, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (w, "w"), (out, "out"), (dout, "dout")):
+        _need(t, n, (B, H, L, d), q.dtype)
+    _need(beta, "beta", (B, H, L), torch.float32)
+    _need(lse, "lse", (B, H, L), torch.float32)
+    for t, n in ((log_f, "log_f"), (dlse, "dlse")):
+        if t is not None:
+            _need(t, n, (B, H, L), torch.float32)
+    desc = _prefill_desc(q, scale, chunk)
+    g = {n: torch.empty_like(q) for n in ("dq", "dk", "dv", "dw")}
+    g["dbeta"] = torch.empty((B, H, L), device=q.device, dtype=torch.float32)
+    if log_f is not None:
+        g["dlog_f"] = torch.empty((B, H, L), device=q.device, dtype=torch.float32)
+    ws_bytes = path_attn_prefill_bwd_workspace_size(desc)
+    if ws_bytes == 0:
+        _check(lib.path_attn_prefill_bwd(ctypes.byref(desc), *([None] * 17), 0, None))
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    _check(lib.path_attn_prefill_bwd(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
+        _ptr(out), _ptr(lse), _ptr(dout), _ptr(dlse), _ptr(g["dq"]), _ptr(g["dk"]),
+        _ptr(g["dv"]), _ptr(g["dw"]), _ptr(g["dbeta"]), _ptr(g.get("dlog_f")),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return g
 
 
 def path_attn_decode_workspace_size(desc: DecodeDesc) -> int:

@@ -69,7 +69,8 @@ struct PrefillPlan {
     size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, total;
 };
 
-path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
+// Checks shared by the prefill forward and backward descriptors.
+path_status_t check_prefill_desc(const path_prefill_desc_t *desc) {
     if (!desc) return fail(PATH_ERR_INVALID_ARG, "desc is NULL");
     if (desc->batch < 1 || desc->heads < 1 || desc->seq_len < 1 || desc->head_dim < 1)
         return fail(PATH_ERR_INVALID_ARG, "batch, heads, seq_len, head_dim must be >= 1");
@@ -77,8 +78,31 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
         return fail(PATH_ERR_INVALID_ARG, "dtype must be PATH_F32 or PATH_BF16");
     if (!(desc->scale == desc->scale) || isinf(desc->scale))
         return fail(PATH_ERR_INVALID_ARG, "scale must be finite");
+    if ((long long)desc->batch * desc->heads > 65535)
+        return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
+    return ok();
+}
+
+// Chunk of the CUDA-core route.  Default: 128 halves the per-step
+// chunk-product work of 64 (d^2 per query per key chunk), and wins on every
+// shape measured except small problems (batch*heads*seq_len <= 8192 with
+// head_dim <= 64), where 64 keeps more blocks busy.
+path_status_t cuda_core_chunk(const path_prefill_desc_t *desc, int *C) {
+    const int d = desc->head_dim;
+    if (d > 128 || d % 4)
+        return fail(PATH_ERR_UNSUPPORTED, "head_dim must be 128, or <= 128 and a multiple of 4");
+    const bool small = (long long)desc->batch * desc->heads * desc->seq_len <= 8192 && d <= 64;
+    const int c = desc->chunk ? desc->chunk : (small ? 64 : 128);
+    if (c != 16 && c != 32 && c != 64 && c != 128)
+        return fail(PATH_ERR_UNSUPPORTED, "chunk must be 16, 32, 64 or 128");
+    *C = c;
+    return ok();
+}
+
+path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
+    path_status_t st = check_prefill_desc(desc);
+    if (st != PATH_OK) return st;
     const long long BH = (long long)desc->batch * desc->heads;
-    if (BH > 65535) return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
     p->bf16 = desc->dtype == PATH_BF16;
     p->d = desc->head_dim;
     p->tc = p->bf16 && p->d == 128;
@@ -88,17 +112,8 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
         p->C = 128;
     } else {
         // CUDA-core route: fp32, or bf16 inputs/output with another head_dim
-        if (p->d > 128 || p->d % 4)
-            return fail(PATH_ERR_UNSUPPORTED, "head_dim must be 128, or <= 128 and a multiple of 4");
-        // Default chunk: 128 halves the per-step chunk-product work of 64
-        // (d^2 per query per key chunk), and wins on every shape measured
-        // except small problems (batch*heads*seq_len <= 8192 with head_dim
-        // <= 64), where 64 keeps more blocks busy.
-        const bool small = BH * desc->seq_len <= 8192 && p->d <= 64;
-        int C = desc->chunk ? desc->chunk : (small ? 64 : 128);
-        if (C != 16 && C != 32 && C != 64 && C != 128)
-            return fail(PATH_ERR_UNSUPPORTED, "chunk must be 16, 32, 64 or 128");
-        p->C = C;
+        st = cuda_core_chunk(desc, &p->C);
+        if (st != PATH_OK) return st;
     }
     p->BH = (int)BH;
     p->L = desc->seq_len;
@@ -116,6 +131,49 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     p->off_F = off; off = align_up(off + rows * 4, 256);
     // fp32 scratch of the SIMT prep (the tensor-core prep keeps it on chip)
     p->off_scratch = off; off = align_up(off + (p->tc ? 0 : cc * 5 * 4), 256);
+    p->total = off;
+    return ok();
+}
+
+// Backward workspace (all fp32): the forward prep's Qh, Kh, Wt, Sd, F and
+// its scratch (shared with the backward prep's), the carried query rows Qts
+// of every (query chunk, earlier key chunk) pair, dQh and dSd, then the
+// atomically accumulated dKh, dV, dA, dF, zeroed by one memset.
+struct BwdPlan {
+    int BH, L, Lp, N, C, d;
+    bool bf16;
+    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_dQh, off_dSd;
+    size_t off_dKh, off_dV, off_dA, off_dF, total;
+};
+
+path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
+    path_status_t st = check_prefill_desc(desc);
+    if (st != PATH_OK) return st;
+    st = cuda_core_chunk(desc, &p->C);
+    if (st != PATH_OK) return st;
+    p->bf16 = desc->dtype == PATH_BF16;
+    p->BH = desc->batch * desc->heads;
+    p->L = desc->seq_len;
+    p->d = desc->head_dim;
+    p->N = (p->L + p->C - 1) / p->C;
+    if ((long long)p->N * p->C > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
+    p->Lp = p->N * p->C;
+    const size_t BH = p->BH, N = p->N, C = p->C, d = p->d;
+    const size_t rows = BH * p->Lp, cc = BH * N * C * C;
+    size_t off = 0;
+    p->off_Qh = off; off = align_up(off + rows * d * 4, 256);
+    p->off_Kh = off; off = align_up(off + rows * d * 4, 256);
+    p->off_Wt = off; off = align_up(off + rows * d * 4, 256);
+    p->off_Sd = off; off = align_up(off + cc * 4, 256);
+    p->off_F = off; off = align_up(off + rows * 4, 256);
+    p->off_scratch = off; off = align_up(off + (cc * 10 + BH * N * C * d) * 4, 256);
+    p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * 4, 256);
+    p->off_dQh = off; off = align_up(off + rows * d * 4, 256);
+    p->off_dSd = off; off = align_up(off + cc * 4, 256);
+    p->off_dKh = off; off = align_up(off + rows * d * 4, 256);
+    p->off_dV = off; off = align_up(off + rows * d * 4, 256);
+    p->off_dA = off; off = align_up(off + BH * N * d * d * 4, 256);
+    p->off_dF = off; off = align_up(off + rows * 4, 256);
     p->total = off;
     return ok();
 }
@@ -336,6 +394,82 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
                                              workspace_bytes, stream);
     if (s != PATH_OK) return s;
     return path_attn_prefill_scan(desc, w, v, log_f, out, lse, workspace, workspace_bytes, stream);
+}
+
+size_t path_attn_prefill_bwd_workspace_size(const path_prefill_desc_t *desc) {
+    BwdPlan p;
+    if (plan_bwd(desc, &p) != PATH_OK) return 0;
+    return p.total;
+}
+
+path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void *q,
+                                    const void *k, const void *v, const void *w,
+                                    const float *beta, const float *log_f, const void *out,
+                                    const float *lse, const void *dout, const float *dlse,
+                                    void *dq, void *dk, void *dv, void *dw, float *dbeta,
+                                    float *dlog_f, void *workspace, size_t workspace_bytes,
+                                    path_stream_t stream) {
+    BwdPlan p;
+    path_status_t s = plan_bwd(desc, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {q, k, v, w, beta, out, lse, dout, dq, dk, dv, dw, dbeta, workspace};
+    const char *names[] = {"q", "k", "v", "w", "beta", "out", "lse", "dout", "dq", "dk",
+                           "dv", "dw", "dbeta", "workspace"};
+    for (int i = 0; i < 14; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    const void *opt[] = {log_f, dlse, dlog_f};
+    const char *onames[] = {"log_f", "dlse", "dlog_f"};
+    for (int i = 0; i < 3; ++i)
+        if (opt[i] && !aligned16(opt[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", onames[i]);
+    if (!log_f != !dlog_f)
+        return fail(PATH_ERR_INVALID_ARG, "dlog_f must be given exactly when log_f is");
+    if (workspace_bytes < p.total)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.total);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
+    if (log_f) {
+        s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
+        if (s != PATH_OK) return s;
+    }
+    PrepSimtArgs pa;
+    pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
+    pa.Qh = at<char>(workspace, p.off_Qh);
+    pa.Kh = at<char>(workspace, p.off_Kh);
+    pa.Wt = at<char>(workspace, p.off_Wt);
+    pa.Sd = at<float>(workspace, p.off_Sd);
+    pa.scratch = at<float>(workspace, p.off_scratch);
+    pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
+    pa.keys_only = 0;
+    s = cuda_status(launch_prep_simt(pa, p.bf16, false, st), "backward prep launch");
+    if (s != PATH_OK) return s;
+    s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dKh), 0, p.total - p.off_dKh, st),
+                    "accumulator clear");
+    if (s != PATH_OK) return s;
+    BwdArgs ba;
+    ba.q = q; ba.k = k; ba.v = v; ba.w = w; ba.out = out; ba.dout = dout;
+    ba.beta = beta; ba.lse = lse; ba.dlse = dlse;
+    ba.Qh = at<float>(workspace, p.off_Qh);
+    ba.Kh = at<float>(workspace, p.off_Kh);
+    ba.Wt = at<float>(workspace, p.off_Wt);
+    ba.Sd = at<float>(workspace, p.off_Sd);
+    ba.F = F;
+    ba.Qts = at<float>(workspace, p.off_Qts);
+    ba.dQh = at<float>(workspace, p.off_dQh);
+    ba.dSd = at<float>(workspace, p.off_dSd);
+    ba.dKh = at<float>(workspace, p.off_dKh);
+    ba.dV = at<float>(workspace, p.off_dV);
+    ba.dA = at<float>(workspace, p.off_dA);
+    ba.dF = log_f ? at<float>(workspace, p.off_dF) : nullptr;
+    ba.scratch = at<float>(workspace, p.off_scratch);
+    ba.dq = dq; ba.dk = dk; ba.dv = dv; ba.dw = dw; ba.dbeta = dbeta; ba.dlog_f = dlog_f;
+    ba.scale = desc->scale;
+    ba.BH = p.BH; ba.L = p.L; ba.Lp = p.Lp; ba.N = p.N; ba.C = p.C; ba.d = p.d;
+    return cuda_status(launch_bwd(ba, p.bf16, st), "backward launch");
 }
 
 size_t path_attn_decode_workspace_size(const path_decode_desc_t *desc) {

@@ -41,6 +41,32 @@ cudaError_t launch_fox_prefix(const float *log_f, float *F, int L, int Lp, int B
 // bf16_io: w, v and out in bf16 (the workspace stays fp32)
 cudaError_t launch_flash_simt(const FlashSimtArgs &a, bool bf16_io, cudaStream_t st);
 
+// Prefill backward (CUDA cores, fp32 arithmetic).  The forward prep's
+// outputs (Qh, Kh, Wt fp32, Sd, F) come from launch_prep_simt on the same
+// workspace.  Accumulators dKh, dV, dA, dF must be zero on entry.
+struct BwdArgs {
+    const void *q, *k, *v, *w, *out, *dout;  // [BH][L][d], element type of the call
+    const float *beta, *lse, *dlse;          // [BH][L]; dlse may be null (zero)
+    const float *Qh, *Kh, *Wt, *Sd, *F;      // forward prep; F null for PaTH
+    float *Qts;      // [BH][N(N-1)/2][C][d] carried query rows of every (b, c < b)
+    float *dQh;      // [BH][Lp][d]
+    float *dSd;      // [BH][N][C][C]
+    float *dKh, *dV; // [BH][Lp][d] (atomic)
+    float *dA;       // [BH][N][d][d] (atomic)
+    float *dF;       // [BH][Lp] (atomic; PaTH-FoX only, else null)
+    float *scratch;  // [BH][N][10][C][C] then [BH][N][C][d]
+    void *dq, *dk, *dv, *dw;  // [BH][L][d], element type of the call
+    float *dbeta;    // [BH][L]
+    float *dlog_f;   // [BH][L] (PaTH-FoX only)
+    float scale;
+    int BH, L, Lp, N, C, d;
+};
+
+size_t bwd_scan_smem(int C, int d);
+size_t bwd_prep_smem(int C);
+// bf16_io: q, k, v, w, out, dout and the gradients dq, dk, dv, dw in bf16
+cudaError_t launch_bwd(const BwdArgs &a, bool bf16_io, cudaStream_t st);
+
 struct DecodeArgs {
     void *k_cache, *v_cache;
     const void *q_t, *k_t, *v_t, *w_t;

@@ -73,26 +73,8 @@ __global__ void __launch_bounds__(kThreads) prep_simt_kernel(PrepSimtArgs a) {
     for_owned(acc, C, C, [&](int r, int c, float v) { KW[r * C + c] = v; });
     __syncthreads();
 
-    // S2: T = (I + strict_lower(diag(beta) G))^{-1} diag(beta), one column per
-    // thread by forward substitution: T[i][c] = beta_i ([i==c] - sum_{k<i} G[i][k] T[k][c]).
-    float *Gs = big, *Ts = big + C * (C + 1);
-    for (int e = threadIdx.x; e < C * C; e += kThreads) Gs[(e / C) * (C + 1) + e % C] = G[e];
-    __syncthreads();
-    if (threadIdx.x < C) {
-        const int c = threadIdx.x;
-        for (int i = 0; i < C; ++i) {
-            float t = 0.f;
-            if (i >= c) {
-                float s = (i == c) ? 1.f : 0.f;
-                for (int kk = c; kk < i; ++kk) s -= Gs[i * (C + 1) + kk] * Ts[kk * (C + 1) + c];
-                t = (i < n ? beta[i] : 0.f) * s;
-            }
-            Ts[i * (C + 1) + c] = t;
-        }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < C * C; e += kThreads) G[e] = Ts[(e / C) * (C + 1) + e % C];
-    __syncthreads();
+    // S2: T = (I + strict_lower(diag(beta) G))^{-1} diag(beta), in place of G.
+    ut_solve(G, beta, n, C, G, big);
     const float *Tm = G;
 
     // S3: Wt = T W, Z = (M_le * QW) T, Y = (M_gt * KW) T^T.

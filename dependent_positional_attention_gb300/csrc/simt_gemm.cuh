@@ -64,4 +64,31 @@ __device__ __forceinline__ void for_owned(const float (&acc)[8][8], int M, int N
         }
 }
 
+// T = (I + strict_lower(diag(beta) G))^{-1} diag(beta) of one chunk, one
+// column per thread by forward substitution:
+//   T[i][c] = beta_i ([i == c] - sum_{c <= k < i} G[i][k] T[k][c]).
+// G and T are row-major [C][C] (they may alias); rows >= n have beta = 0.
+// big: 2 C (C + 1) floats of shared memory.  Ends with __syncthreads().
+__device__ __forceinline__ void ut_solve(const float *G, const float *beta, int n, int C,
+                                         float *T, float *big) {
+    float *Gs = big, *Ts = big + C * (C + 1);
+    for (int e = threadIdx.x; e < C * C; e += kThreads) Gs[(e / C) * (C + 1) + e % C] = G[e];
+    __syncthreads();
+    if (threadIdx.x < C) {
+        const int c = threadIdx.x;
+        for (int i = 0; i < C; ++i) {
+            float t = 0.f;
+            if (i >= c) {
+                float s = (i == c) ? 1.f : 0.f;
+                for (int kk = c; kk < i; ++kk) s -= Gs[i * (C + 1) + kk] * Ts[kk * (C + 1) + c];
+                t = (i < n ? beta[i] : 0.f) * s;
+            }
+            Ts[i * (C + 1) + c] = t;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < C * C; e += kThreads) T[e] = Ts[(e / C) * (C + 1) + e % C];
+    __syncthreads();
+}
+
 }  // namespace path

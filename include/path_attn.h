@@ -121,6 +121,45 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
                                      void *workspace, size_t workspace_bytes,
                                      path_stream_t stream);
 
+/* ----------------------------------------------------------------- backward */
+
+/* Bytes of device workspace path_attn_prefill_bwd needs for `desc` (0 if the
+ * descriptor is invalid).  It grows as batch*heads*seq_len^2*head_dim/chunk:
+ * the backward keeps the carried query rows of every (query chunk, earlier
+ * key chunk) pair, in fp32. */
+size_t path_attn_prefill_bwd_workspace_size(const path_prefill_desc_t *desc);
+
+/*
+ * Backward of path_attn_prefill_fwd: the gradients of
+ *     sum(dout * out) + sum(dlse * lse)
+ * with respect to q, k, v, w, beta and (PaTH-FoX) log_f.  The pages give no
+ * backward algorithm; this one is reverse-mode differentiation of the
+ * forward's blockwise algorithm (section 3 of the PaTH summary), recomputing
+ * the per-chunk UT transform and re-walking the scan, with the per-key-chunk
+ * sums accumulated atomically across query chunks.
+ *   q, k, v, w   : the forward's inputs; beta, log_f likewise (log_f NULL for PaTH).
+ *   out, lse     : the forward's outputs for these inputs (lse is required).
+ *   dout         : [B][H][L][d], desc->dtype.
+ *   dlse         : float32 [B][H][L], or NULL for zero.
+ *   dq, dk, dv, dw : [B][H][L][d], desc->dtype, written.
+ *   dbeta        : float32 [B][H][L], written.
+ *   dlog_f       : float32 [B][H][L], written; required exactly when log_f is given.
+ *   workspace    : at least path_attn_prefill_bwd_workspace_size(desc) bytes.
+ * All arithmetic is fp32 on the CUDA cores for both dtypes (bf16 values are
+ * converted on load and store).  desc->chunk: 16, 32, 64 or 128, or 0 for the
+ * same default as the forward's CUDA-core route; it need not match the chunk
+ * the forward used.  Supported: head_dim <= 128 and a multiple of 4.
+ * Pointers must be 16-byte aligned.  Argument errors are returned before
+ * any launch; the call is asynchronous on `stream`.
+ */
+path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void *q,
+                                    const void *k, const void *v, const void *w,
+                                    const float *beta, const float *log_f, const void *out,
+                                    const float *lse, const void *dout, const float *dlse,
+                                    void *dq, void *dk, void *dv, void *dw, float *dbeta,
+                                    float *dlog_f, void *workspace, size_t workspace_bytes,
+                                    path_stream_t stream);
+
 /* ------------------------------------------------------------------- decode */
 
 typedef struct {

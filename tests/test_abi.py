@@ -120,3 +120,43 @@ def test_fox_decode_and_prefix_reject_bad_arguments(lib):
     assert lib.path_attn_fox_prefix(FAKE, FAKE, 2, 10, 5, None) == pa.PATH_ERR_INVALID_ARG
     assert lib.path_attn_fox_prefix(None, FAKE, 2, 10, 10, None) == pa.PATH_ERR_INVALID_ARG
     assert lib.path_attn_fox_prefix(FAKE, FAKE, 0, 10, 10, None) == pa.PATH_ERR_INVALID_ARG
+
+
+def bwd(lib, desc, ptrs, ws_bytes=1 << 40):
+    return lib.path_attn_prefill_bwd(ctypes.byref(desc), *ptrs, ws_bytes, None)
+
+
+def test_backward_rejects_bad_arguments(lib):
+    """Rejected before any CUDA call, so this runs without a GPU."""
+    D = pa.PrefillDesc
+    desc = D(2, 3, 100, 64, 0, 0.125, 0)
+    need = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(desc))
+    assert need > lib.path_attn_prefill_workspace_size(ctypes.byref(desc)) > 0
+    # q k v w beta log_f out lse dout dlse dq dk dv dw dbeta dlog_f workspace
+    good = [FAKE] * 5 + [None] + [FAKE] * 3 + [None] + [FAKE] * 5 + [None, FAKE]
+    assert bwd(lib, desc, good, ws_bytes=need - 1) == pa.PATH_ERR_INVALID_ARG
+    assert b"workspace" in lib.path_attn_last_error()
+    required = [0, 1, 2, 3, 4, 6, 7, 8, 10, 11, 12, 13, 14, 16]
+    for i in required:
+        for bad in (None, ODD):
+            p = list(good)
+            p[i] = bad
+            assert bwd(lib, desc, p) == pa.PATH_ERR_INVALID_ARG, i
+    p = list(good)
+    p[5] = FAKE  # log_f without dlog_f
+    assert bwd(lib, desc, p) == pa.PATH_ERR_INVALID_ARG
+    assert b"dlog_f" in lib.path_attn_last_error()
+    p[5], p[15] = None, FAKE  # dlog_f without log_f
+    assert bwd(lib, desc, p) == pa.PATH_ERR_INVALID_ARG
+    p = list(good)
+    p[9] = ODD
+    assert bwd(lib, desc, p) == pa.PATH_ERR_INVALID_ARG
+    assert bwd(lib, D(1, 1, 16, 130, 0, 0.1, 0), good) == pa.PATH_ERR_UNSUPPORTED
+    assert bwd(lib, D(1, 1, 16, 64, 0, 0.1, 48), good) == pa.PATH_ERR_UNSUPPORTED
+    # bf16 with head_dim 128 accepts any chunk here (the CUDA-core route)
+    d128 = D(1, 1, 300, 128, 1, 0.1, 32)
+    assert lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(d128)) > 0
+    # the carried-row store grows as L^2: doubling L roughly quadruples it
+    a = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(D(1, 1, 4096, 64, 0, 0.1, 64)))
+    b = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(D(1, 1, 8192, 64, 0, 0.1, 64)))
+    assert 3.0 < b / a < 4.2

@@ -1,0 +1,108 @@
+"""Parity of the prefill backward (path_attn_prefill_bwd, CUDA cores, fp32
+arithmetic) with the fp64 oracle's reverse-mode gradients, on the same
+seeded inputs (the oracle sees exactly the values the GPU receives).
+
+Tolerance: every gradient G is compared as max|G_gpu - G_ref| / max(1, max|G_ref|).
+fp32 outputs: 1e-4 (fp32 accumulation over at most a few thousand terms,
+relative error ~1e-6 per term).  bf16 outputs: 2e-2, from the bf16 rounding
+of the output itself (2^-9 relative) plus the rounding of the forward's bf16
+`out` that enters D = dout . out, whose error reaches every dlogit through
+P (D + ...) and is then amplified by at most the row length's worth of
+cancellation in the key-side sums; measured errors sit well inside it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dependent_positional_attention_gb300 as pa
+from dependent_positional_attention_gb300 import workloads as wl
+from helpers import to64
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dq", "dk", "dv", "dw", "dbeta")
+
+
+def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None):
+    dev = torch.device("cuda:0")
+    g = {n: t.to(dev) for n, t in x.items()}
+    gen = torch.Generator().manual_seed(1234)
+    dout = torch.randn(g["q"].shape, generator=gen).to(g["q"].dtype)
+    dlse = torch.randn(g["beta"].shape, generator=gen) if use_dlse else None
+    out, lse = pa.path_attn_prefill_fwd(g["q"], g["k"], g["v"], g["w"], g["beta"],
+                                        log_f=g.get("log_f"), chunk=fwd_chunk)
+    got = pa.path_attn_prefill_bwd(g["q"], g["k"], g["v"], g["w"], g["beta"], out, lse,
+                                   dout.to(dev), log_f=g.get("log_f"),
+                                   dlse=dlse.to(dev) if dlse is not None else None, chunk=chunk)
+    torch.cuda.synchronize()
+    assert pa.path_attn_device_status() == 0
+    sel = slice(None) if heads is None else heads
+
+    def pick(t):
+        B, H = t.shape[:2]
+        return to64(t.reshape((B * H,) + tuple(t.shape[2:]))[sel])
+
+    args = [pick(x[n]) for n in ("q", "k", "v", "w", "beta")]
+    ref = oracle.prefill_bwd(*args, pick(dout), log_f=pick(x["log_f"]) if "log_f" in x else None,
+                             dlse=pick(dlse) if dlse is not None else None)
+    return {n: pick(t) for n, t in got.items()}, ref
+
+
+def check(got, ref, tol):
+    assert set(got) == set(ref)
+    for n in ref:
+        err = float(np.max(np.abs(got[n] - ref[n]))) / max(1.0, float(np.max(np.abs(ref[n]))))
+        assert err <= tol, "%s: normalised error %.3g > %.3g" % (n, err, tol)
+
+
+def test_tiny_fp32():
+    got, ref = run(wl.prefill_inputs(1, 1, 256, 64, "f32", seed=0))
+    check(got, ref, 1e-4)
+
+
+def test_tiny_fp32_with_dlse_and_fox():
+    got, ref = run(wl.prefill_inputs(1, 2, 256, 64, "f32", seed=2, fox=True), use_dlse=True)
+    assert "dlog_f" in got
+    check(got, ref, 1e-4)
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128])
+@pytest.mark.parametrize("L", [1, 100, 300])
+def test_chunks_and_ragged_tails(chunk, L):
+    got, ref = run(wl.prefill_inputs(2, 2, L, 32, "f32", seed=L + chunk), chunk=chunk,
+                   use_dlse=True)
+    check(got, ref, 1e-4)
+
+
+@pytest.mark.parametrize("d", [4, 96, 128])
+def test_head_dims(d):
+    got, ref = run(wl.prefill_inputs(1, 2, 200, d, "f32", seed=d), chunk=64)
+    check(got, ref, 1e-4)
+
+
+def test_beta_near_two_fox():
+    x = wl.prefill_inputs(1, 2, 384, 64, "f32", seed=8, beta_mu=2.0, fox=True)
+    got, ref = run(x, chunk=128, use_dlse=True)
+    check(got, ref, 1e-4)
+
+
+def test_bf16_inputs_tensor_core_forward():
+    """bf16, head_dim 128: the forward runs on the tensor cores, the backward
+    (chunk 128) on the CUDA cores."""
+    got, ref = run(wl.prefill_inputs(1, 2, 520, 128, "bf16", seed=4))
+    check(got, ref, 2e-2)
+
+
+def test_bf16_fox_other_chunk():
+    got, ref = run(wl.prefill_inputs(1, 2, 300, 64, "bf16", seed=6, fox=True), chunk=32,
+                   use_dlse=True)
+    check(got, ref, 2e-2)
+
+
+def test_headline_shape_sampled_heads():
+    """B8 H12 L4096 d128 bf16, the shape of the forward benchmark; two heads
+    (first and last) checked in full against the oracle."""
+    x = wl.prefill_inputs(8, 12, 4096, 128, "bf16", seed=0)
+    got, ref = run(x, heads=[0, 95])
+    check(got, ref, 2e-2)
