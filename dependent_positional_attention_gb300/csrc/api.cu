@@ -137,12 +137,12 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
 
 // Backward workspace (all fp32): the forward prep's Qh, Kh, Wt, Sd, F and
 // its scratch (shared with the backward prep's), the carried query rows Qts
-// of every (query chunk, earlier key chunk) pair, dQh and dSd, then the
-// atomically accumulated dKh, dV, dA, dF, zeroed by one memset.
+// of every (query chunk, earlier key chunk) pair, dQh, then the atomically
+// accumulated dKh, dV, dA, dF, zeroed by one memset.
 struct BwdPlan {
     int BH, L, Lp, N, C, d;
     bool bf16;
-    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_dQh, off_dSd;
+    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_dQh;
     size_t off_dKh, off_dV, off_dA, off_dF, total;
 };
 
@@ -166,10 +166,9 @@ path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
     p->off_Wt = off; off = align_up(off + rows * d * 4, 256);
     p->off_Sd = off; off = align_up(off + cc * 4, 256);
     p->off_F = off; off = align_up(off + rows * 4, 256);
-    p->off_scratch = off; off = align_up(off + (cc * 10 + BH * N * C * d) * 4, 256);
+    p->off_scratch = off; off = align_up(off + (cc * kBwdPrepCC + BH * N * 2 * C * d) * 4, 256);
     p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * 4, 256);
     p->off_dQh = off; off = align_up(off + rows * d * 4, 256);
-    p->off_dSd = off; off = align_up(off + cc * 4, 256);
     p->off_dKh = off; off = align_up(off + rows * d * 4, 256);
     p->off_dV = off; off = align_up(off + rows * d * 4, 256);
     p->off_dA = off; off = align_up(off + BH * N * d * d * 4, 256);
@@ -456,11 +455,9 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
     ba.Qh = at<float>(workspace, p.off_Qh);
     ba.Kh = at<float>(workspace, p.off_Kh);
     ba.Wt = at<float>(workspace, p.off_Wt);
-    ba.Sd = at<float>(workspace, p.off_Sd);
     ba.F = F;
     ba.Qts = at<float>(workspace, p.off_Qts);
     ba.dQh = at<float>(workspace, p.off_dQh);
-    ba.dSd = at<float>(workspace, p.off_dSd);
     ba.dKh = at<float>(workspace, p.off_dKh);
     ba.dV = at<float>(workspace, p.off_dV);
     ba.dA = at<float>(workspace, p.off_dA);

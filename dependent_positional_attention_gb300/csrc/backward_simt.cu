@@ -9,21 +9,24 @@
 // Sd = Q K^T - a T b^T, and the chunk product A_c = I - W_c^T Wt_c that the
 // carried query rows take after key chunk c: Qt_{c-1} = Qt_c A_c.
 //
-//   bwd_scan_kernel (one block per query chunk b):
+//   bwd_scan_kernel (one block per query chunk b, key chunks c < b):
 //     (R) the forward's right-to-left chain Qt_{b-1} = Qh_b, Qt_{c-1} = Qt_c A_c,
 //         every Qt_c stored;
-//     (L) c = 0 .. b: probabilities from the saved lse, dP = dout V_c^T,
+//     (L) c = 0 .. b-1: probabilities from the saved lse, dP = dout V_c^T,
 //         dlogit = P * (dP - D + dlse) with D = dout . out; then
 //           dV_c  += P^T dout                     (atomic, over query chunks)
 //           dKh_c += scale dlogit^T Qt_c          (atomic)
 //           dA_c  += Qt_c^T G_{c-1}               (atomic)
 //           G_c    = scale dlogit Kh_c + G_{c-1} A_c^T,  G_{-1} = 0,
-//         and, for the chunk's own block, dSd_b = scale dlogit.  dQh_b = G_{b-1}.
+//         and dQh_b = G_{b-1}.
 //         The pages remark that the backward pays for atomic accumulation;
 //         these three sums are where it does.
-//   bwd_prep_kernel (one block per chunk): from dQh, dKh, dSd and dA back
-//     through the boundary adjustment, Wt = T W and the UT transform to dq,
-//     dk, dw, dbeta (the derivation is written out step by step below).
+//   bwd_prep_kernel (one block per chunk): the chunk's own causal block
+//     (its logits Sd recomputed, dSd = scale dlogit, dV's diagonal part),
+//     then from dQh, dKh, dSd and dA back through the boundary adjustment,
+//     Wt = T W and the UT transform to dq, dk, dw, dbeta (the derivation is
+//     written out step by step below).  It recomputes everything it needs
+//     from the inputs, so it serves the CUDA-core and the tensor-core scans.
 //   fox_suffix_kernel: with the FoX bias F_i - F_j (F the inclusive prefix of
 //     log f), dF_i = sum_j dlogit_ij - sum_i' dlogit_i'i and
 //     dlog f_s = sum_{i >= s} dF_i.
@@ -102,23 +105,17 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
         }
     }
 
-    // (L) c = 0 .. b
+    // (L) c = 0 .. b-1
     for (int e = threadIdx.x; e < C * d; e += kThreads) Gs[e] = 0.f;
     __syncthreads();
-    for (int c = 0; c <= b; ++c) {
+    for (int c = 0; c < b; ++c) {
         const int k0 = c * C;
-        const bool diag = (c == b);
-        const float *Qt = Qts + (size_t)c * C * d;  // valid for c < b
-        if (diag) {
-            const float *Sd = a.Sd + ((size_t)bh * a.N + b) * C * C;
-            for (int e = threadIdx.x; e < C * C; e += kThreads) S[e] = Sd[e];
-        } else {
-            zero(acc);
-            block_gemm<true, true>(
-                acc, C, C, d, [&](int r, int m) { return Qt[(size_t)r * d + m]; },
-                [&](int m, int j) { return Kh[(size_t)(k0 + j) * d + m]; }, sA, sB);
-            for_owned(acc, C, C, [&](int r, int j, float v) { S[r * C + j] = v; });
-        }
+        const float *Qt = Qts + (size_t)c * C * d;
+        zero(acc);
+        block_gemm<true, true>(
+            acc, C, C, d, [&](int r, int m) { return Qt[(size_t)r * d + m]; },
+            [&](int m, int j) { return Kh[(size_t)(k0 + j) * d + m]; }, sA, sB);
+        for_owned(acc, C, C, [&](int r, int j, float v) { S[r * C + j] = v; });
         zero(acc);
         block_gemm<true, true>(
             acc, C, C, d, dO_,
@@ -128,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
         __syncthreads();
         for (int e = threadIdx.x; e < C * C; e += kThreads) {
             const int r = e / C, j = e - r * C;
-            const bool valid = r < nq && k0 + j < L && (!diag || j <= r);
+            const bool valid = r < nq;  // key chunk c < b is full
             float p = 0.f;
             if (valid) {
                 float l = a.scale * S[e] + (F ? rF[r] - F[k0 + j] : 0.f);
@@ -157,11 +154,6 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
         for_owned(acc, C, d, [&](int j, int m, float v) {
             if (k0 + j < L) atomicAdd(dV + (size_t)(k0 + j) * d + m, v);
         });
-        if (diag) {
-            float *dSd = a.dSd + ((size_t)bh * a.N + b) * C * C;
-            for (int e = threadIdx.x; e < C * C; e += kThreads) dSd[e] = a.scale * X[e];
-            break;
-        }
         // dKh_c += scale dlogit^T Qt_c
         zero(acc);
         block_gemm<false, false>(
@@ -206,8 +198,10 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(BwdArgs a) {
         for (int r = threadIdx.x; r < nq; r += kThreads) atomicAdd(dF + b * C + r, rR[r]);
 }
 
-// Gradient through one chunk's prep.  With dQh, dKh, dSd from the scan and
-// dA (the chunk product's gradient):
+// One chunk's own causal block and the gradient through its prep.  The block:
+//   Sd = Q K^T - a Y^T, P = exp(scale Sd + F_i - F_j - lse_i) (j <= i),
+//   dlogit = P (dout V^T - D + dlse), dSd = scale dlogit, dV += P^T dout.
+// Then, with dQh, dKh from the scan and dA (the chunk product's gradient):
 //   dWt  = -W dA                     dW  = -Wt dA^T + ...
 //   da   = -(dSd b T^T + dQh Wt^T)   (a = M_le * Q W^T)
 //   db   = -(dSd^T a + dKh W^T) T    (b = M_gt * K W^T)
@@ -235,16 +229,22 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(BwdArgs a) {
     const TIO *w = static_cast<const TIO *>(a.w) + in_base;
     const float *beta = a.beta + (size_t)bh * L + c0;
     const size_t ws_rows = ((size_t)bh * a.Lp + c0) * d;
-    const float *Wt = a.Wt + ws_rows;
     const float *dQh = a.dQh + ws_rows, *dKh = a.dKh + ws_rows, *dVa = a.dV + ws_rows;
     const size_t chunk_id = (size_t)bh * a.N + chunk;
-    const float *dSd = a.dSd + chunk_id * C * C;
     const float *dA = a.dA + chunk_id * d * d;
     const size_t cc = (size_t)C * C;
-    float *G = a.scratch + chunk_id * 10 * cc;
+    float *G = a.scratch + chunk_id * kBwdPrepCC * cc;
     float *Tm = G + cc, *QW = G + 2 * cc, *KW = G + 3 * cc, *Z = G + 4 * cc, *Y = G + 5 * cc;
     float *R = G + 6 * cc, *dam = G + 7 * cc, *dbm = G + 8 * cc, *dT = G + 9 * cc;
-    float *dWt = a.scratch + (size_t)a.BH * a.N * 10 * cc + chunk_id * C * d;
+    float *dSd = G + 10 * cc;
+    float *dWt = a.scratch + (size_t)a.BH * a.N * kBwdPrepCC * cc + chunk_id * 2 * C * d;
+    float *Wt = dWt + C * d;
+    const size_t io_rows = (size_t)bh * L + c0;
+    const TIO *v = static_cast<const TIO *>(a.v) + in_base;
+    const TIO *dO = static_cast<const TIO *>(a.dout) + in_base;
+    const TIO *O = static_cast<const TIO *>(a.out) + in_base;
+    const float *F = a.F ? a.F + (size_t)bh * a.Lp + c0 : nullptr;
+    float *dF = a.dF ? a.dF + (size_t)bh * a.Lp + c0 : nullptr;
 
     auto W_ = [&](int r, int m) { return r < n ? to_f32(w[(size_t)r * d + m]) : 0.f; };
     auto Q_ = [&](int r, int m) { return r < n ? to_f32(q[(size_t)r * d + m]) : 0.f; };
@@ -271,6 +271,64 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(BwdArgs a) {
     zero(acc);
     block_gemm<true, true>(acc, C, C, C, bm, [&](int s, int t) { return Tm[t * C + s]; }, sA, sB);
     for_owned(acc, C, C, [&](int r, int c, float v) { Y[r * C + c] = v; });
+    // Wt = T W
+    zero(acc);
+    block_gemm<true, false>(acc, C, d, C, [&](int r, int s) { return Tm[r * C + s]; }, W_, sA, sB);
+    for_owned(acc, C, d, [&](int r, int m, float v) { Wt[r * d + m] = v; });
+
+    // The chunk's own block.  Row constants in the (idle) solve area.
+    float *rD = big, *rL = big + C, *rF = big + 2 * C;
+    for (int r = threadIdx.x; r < C; r += kThreads) {
+        float D = 0.f, l = 0.f, f = 0.f;
+        if (r < n) {
+            for (int m = 0; m < d; ++m)
+                D = fmaf(to_f32(dO[(size_t)r * d + m]), to_f32(O[(size_t)r * d + m]), D);
+            if (a.dlse) D -= a.dlse[io_rows + r];
+            l = a.lse[io_rows + r];
+            f = F ? F[r] : 0.f;
+        }
+        rD[r] = D; rL[r] = l; rF[r] = f;
+    }
+    auto dO_ = [&](int r, int m) { return r < n ? to_f32(dO[(size_t)r * d + m]) : 0.f; };
+    // Sd = Q K^T - a Y^T into R; dP = dout V^T into dam
+    zero(acc);
+    block_gemm<true, true>(acc, C, C, d, Q_, [&](int m, int j) { return K_(j, m); }, sA, sB);
+    block_gemm<true, true>(acc, C, C, C, [&](int r, int s) { return -am(r, s); },
+                           [&](int s, int j) { return Y[j * C + s]; }, sA, sB);
+    for_owned(acc, C, C, [&](int r, int j, float v) { R[r * C + j] = v; });
+    zero(acc);
+    block_gemm<true, true>(acc, C, C, d, dO_,
+                           [&](int m, int j) { return j < n ? to_f32(v[(size_t)j * d + m]) : 0.f; },
+                           sA, sB);
+    for_owned(acc, C, C, [&](int r, int j, float x) { dam[r * C + j] = x; });
+    __syncthreads();
+    for (int e = threadIdx.x; e < C * C; e += kThreads) {
+        const int r = e / C, j = e - r * C;
+        float p = 0.f;
+        if (r < n && j <= r) p = expf(a.scale * R[e] + (F ? rF[r] - F[j] : 0.f) - rL[r]);
+        const float dl = p * (dam[e] - rD[r]);
+        R[e] = p;
+        dam[e] = dl;
+        dSd[e] = a.scale * dl;
+    }
+    __syncthreads();
+    if (dF) {
+        // FoX: dF_i += sum_j dlogit_ij, dF_j -= sum_i dlogit_ij
+        for (int r = threadIdx.x; r < n; r += kThreads) {
+            float srow = 0.f, scol = 0.f;
+            for (int j = 0; j < C; ++j) srow += dam[r * C + j];
+            for (int i = 0; i < C; ++i) scol += dam[i * C + r];
+            atomicAdd(dF + r, srow - scol);
+        }
+    }
+    // dv = dV (scan) + P^T dout
+    zero(acc);
+    block_gemm<false, false>(acc, C, d, C, [&](int j, int r) { return R[r * C + j]; }, dO_, sA, sB);
+    TIO *dv = static_cast<TIO *>(a.dv) + in_base;
+    for_owned(acc, n, d, [&](int r, int m, float x) {
+        dv[(size_t)r * d + m] = from_f32<TIO>(x + dVa[(size_t)r * d + m]);
+    });
+    __syncthreads();
 
     // dWt = -W dA
     zero(acc);
@@ -393,9 +451,6 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(BwdArgs a) {
     for_owned(acc, n, d, [&](int r, int m, float v) {
         dk[(size_t)r * d + m] = from_f32<TIO>(v + dKh[(size_t)r * d + m]);
     });
-    // dv
-    TIO *dv = static_cast<TIO *>(a.dv) + in_base;
-    for (int e = threadIdx.x; e < n * d; e += kThreads) dv[e] = from_f32<TIO>(dVa[e]);
 }
 
 // dlog f_s = sum_{i >= s} dF_i (fp64 running sum from the right), one warp per head.

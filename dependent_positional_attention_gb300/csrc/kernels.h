@@ -47,14 +47,14 @@ cudaError_t launch_flash_simt(const FlashSimtArgs &a, bool bf16_io, cudaStream_t
 struct BwdArgs {
     const void *q, *k, *v, *w, *out, *dout;  // [BH][L][d], element type of the call
     const float *beta, *lse, *dlse;          // [BH][L]; dlse may be null (zero)
-    const float *Qh, *Kh, *Wt, *Sd, *F;      // forward prep; F null for PaTH
+    const float *Qh, *Kh, *Wt;               // forward prep (CUDA-core scan only)
+    const float *F;                          // FoX prefix sums [BH][Lp], null for PaTH
     float *Qts;      // [BH][N(N-1)/2][C][d] carried query rows of every (b, c < b)
     float *dQh;      // [BH][Lp][d]
-    float *dSd;      // [BH][N][C][C]
     float *dKh, *dV; // [BH][Lp][d] (atomic)
     float *dA;       // [BH][N][d][d] (atomic)
     float *dF;       // [BH][Lp] (atomic; PaTH-FoX only, else null)
-    float *scratch;  // [BH][N][10][C][C] then [BH][N][C][d]
+    float *scratch;  // [BH][N][kBwdPrepCC][C][C] then [BH][N][2][C][d]
     void *dq, *dk, *dv, *dw;  // [BH][L][d], element type of the call
     float *dbeta;    // [BH][L]
     float *dlog_f;   // [BH][L] (PaTH-FoX only)
@@ -62,6 +62,7 @@ struct BwdArgs {
     int BH, L, Lp, N, C, d;
 };
 
+constexpr int kBwdPrepCC = 11;  // C x C scratch matrices per chunk of the backward prep
 size_t bwd_scan_smem(int C, int d);
 size_t bwd_prep_smem(int C);
 // bf16_io: q, k, v, w, out, dout and the gradients dq, dk, dv, dw in bf16
