@@ -142,6 +142,7 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
 struct BwdPlan {
     int BH, L, Lp, N, C, d;
     bool bf16;
+    bool tc;  // bf16, head_dim 128, chunk 128: the tensor-core scan (PaTH calls)
     size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_dQh;
     size_t off_dKh, off_dV, off_dA, off_dF, total;
 };
@@ -155,6 +156,7 @@ path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
     p->BH = desc->batch * desc->heads;
     p->L = desc->seq_len;
     p->d = desc->head_dim;
+    p->tc = p->bf16 && p->d == 128 && p->C == 128;
     p->N = (p->L + p->C - 1) / p->C;
     if ((long long)p->N * p->C > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
     p->Lp = p->N * p->C;
@@ -168,6 +170,7 @@ path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
     p->off_F = off; off = align_up(off + rows * 4, 256);
     p->off_scratch = off; off = align_up(off + (cc * kBwdPrepCC + BH * N * 2 * C * d) * 4, 256);
     p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * 4, 256);
+    // zeroed from here on
     p->off_dQh = off; off = align_up(off + rows * d * 4, 256);
     p->off_dKh = off; off = align_up(off + rows * d * 4, 256);
     p->off_dV = off; off = align_up(off + rows * d * 4, 256);
@@ -435,20 +438,6 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
         if (s != PATH_OK) return s;
     }
-    PrepSimtArgs pa;
-    pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
-    pa.Qh = at<char>(workspace, p.off_Qh);
-    pa.Kh = at<char>(workspace, p.off_Kh);
-    pa.Wt = at<char>(workspace, p.off_Wt);
-    pa.Sd = at<float>(workspace, p.off_Sd);
-    pa.scratch = at<float>(workspace, p.off_scratch);
-    pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
-    pa.keys_only = 0;
-    s = cuda_status(launch_prep_simt(pa, p.bf16, false, st), "backward prep launch");
-    if (s != PATH_OK) return s;
-    s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dKh), 0, p.total - p.off_dKh, st),
-                    "accumulator clear");
-    if (s != PATH_OK) return s;
     BwdArgs ba;
     ba.q = q; ba.k = k; ba.v = v; ba.w = w; ba.out = out; ba.dout = dout;
     ba.beta = beta; ba.lse = lse; ba.dlse = dlse;
@@ -466,6 +455,72 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
     ba.dq = dq; ba.dk = dk; ba.dv = dv; ba.dw = dw; ba.dbeta = dbeta; ba.dlog_f = dlog_f;
     ba.scale = desc->scale;
     ba.BH = p.BH; ba.L = p.L; ba.Lp = p.Lp; ba.N = p.N; ba.C = p.C; ba.d = p.d;
+    if (p.tc && !log_f) {
+        // tensor-core prep (bf16 Qh, Kh, Pm; its chunk outputs OD/LSD unused
+        // here), then the tensor-core scan, then the CUDA-core backward prep
+        char *qh = at<char>(workspace, p.off_Qh), *kh = at<char>(workspace, p.off_Kh);
+        char *pm = at<char>(workspace, p.off_Wt), *od = at<char>(workspace, p.off_Sd);
+        char *qts = at<char>(workspace, p.off_Qts);
+        const uint64_t npairs = (uint64_t)p.N * (p.N - 1) / 2;
+        PrepTcMaps pm_maps;
+        BwdTcMaps bm;
+        const bool enc =
+            encode_tmap_bf16_3d(&pm_maps.q, q, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.k, k, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.w, w, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.v, v, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.qh, qh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.kh, kh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.pm, pm, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.od, od, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.qh, qh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.kh, kh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.pm, pm, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.v, v, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.dout, dout, 128, p.L, p.BH, 64, 128) &&
+            (npairs == 0 ||
+             encode_tmap_bf16_3d(&bm.qts, qts, 128, npairs * 128, p.BH, 64, 128));
+        if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+        const int sms = num_sms();
+        if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+        PrepTcArgs ta;
+        ta.beta = beta;
+        ta.F = nullptr;
+        ta.scale = desc->scale;
+        ta.LSD = reinterpret_cast<float *>(od + (size_t)p.BH * p.Lp * 128 * 2);
+        ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        ta.err = error_flag_ptr();
+        s = cuda_status(launch_prep_tc(pm_maps, ta, sms, st), "tensor-core prep launch");
+        if (s != PATH_OK) return s;
+        s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dQh), 0, p.total - p.off_dQh, st),
+                        "accumulator clear");
+        if (s != PATH_OK) return s;
+        BwdTcArgs tb;
+        tb.out = static_cast<const __nv_bfloat16 *>(out);
+        tb.dout = static_cast<const __nv_bfloat16 *>(dout);
+        tb.lse = lse; tb.dlse = dlse;
+        tb.dQh = ba.dQh; tb.dKh = ba.dKh; tb.dV = ba.dV; tb.dA = ba.dA;
+        tb.scale = desc->scale;
+        tb.BH = p.BH; tb.L = p.L; tb.Lp = p.Lp; tb.N = p.N;
+        tb.err = error_flag_ptr();
+        s = cuda_status(launch_bwd_scan_tc(bm, tb, sms, st), "tensor-core backward scan launch");
+        if (s != PATH_OK) return s;
+        return cuda_status(launch_bwd_prep(ba, true, st), "backward prep launch");
+    }
+    PrepSimtArgs pa;
+    pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
+    pa.Qh = at<char>(workspace, p.off_Qh);
+    pa.Kh = at<char>(workspace, p.off_Kh);
+    pa.Wt = at<char>(workspace, p.off_Wt);
+    pa.Sd = at<float>(workspace, p.off_Sd);
+    pa.scratch = at<float>(workspace, p.off_scratch);
+    pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
+    pa.keys_only = 0;
+    s = cuda_status(launch_prep_simt(pa, p.bf16, false, st), "backward prep launch");
+    if (s != PATH_OK) return s;
+    s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dQh), 0, p.total - p.off_dQh, st),
+                    "accumulator clear");
+    if (s != PATH_OK) return s;
     return cuda_status(launch_bwd(ba, p.bf16, st), "backward launch");
 }
 

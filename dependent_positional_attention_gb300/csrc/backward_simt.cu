@@ -488,14 +488,17 @@ size_t bwd_prep_smem(int C) {
 
 cudaError_t launch_bwd(const BwdArgs &a, bool bf16_io, cudaStream_t st) {
     dim3 grid(a.N, a.BH);
-    {
-        const size_t sm = bwd_scan_smem(a.C, a.d);
-        void (*kern)(BwdArgs) = bf16_io ? bwd_scan_kernel<__nv_bfloat16> : bwd_scan_kernel<float>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        kern<<<grid, kThreads, sm, st>>>(a);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+    const size_t sm = bwd_scan_smem(a.C, a.d);
+    void (*kern)(BwdArgs) = bf16_io ? bwd_scan_kernel<__nv_bfloat16> : bwd_scan_kernel<float>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    kern<<<grid, kThreads, sm, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_bwd_prep(a, bf16_io, st);
+}
+
+cudaError_t launch_bwd_prep(const BwdArgs &a, bool bf16_io, cudaStream_t st) {
+    dim3 grid(a.N, a.BH);
     {
         const size_t sm = bwd_prep_smem(a.C);
         void (*kern)(BwdArgs) = bf16_io ? bwd_prep_kernel<__nv_bfloat16> : bwd_prep_kernel<float>;

@@ -1,0 +1,346 @@
+// PaTH prefill backward scan on tensor cores (bf16, head_dim 128, chunk 128).
+//
+// The off-diagonal part of the backward of the blockwise forward (PaTH
+// Attention summary, section "3. 효율적인 학습 및 추론"); the chunk's own
+// block and the gradient through the UT transform follow in
+// bwd_prep_kernel.  Per query chunk b, with the tensor-core prep's bf16 Qh,
+// Kh and chunk products Pm_c (the carried rows take Qt <- Qt Pm_c after key
+// chunk c):
+//   (R) Qt_{b-1} = Qh_b, Qt_{c-1} = Qt_c Pm_c: the forward's right-to-left
+//       chain, recomputed exactly as the forward scan forms it (bf16 rows,
+//       fp32 product, re-rounded per chunk), every Qt_c stored by TMA;
+//   (L) c = 0 .. b-1, with D = dout . out - dlse per row:
+//         S  = Qt_c Kh_c^T,  dP = dout V_c^T,  P = 2^(S scale log2e - lse log2e)
+//         dl = scale P (dP - D)                     (bf16 tile; P likewise)
+//         dV_c  += P^T dout,  dKh_c += dl^T Qt_c,  dA_c += Qt_c^T G  (c >= 1)
+//         G     <- G Pm_c^T + dl Kh_c                (G = 0 before c = 0)
+//       and dQh_b = G.  The three sums over query chunks are vector fp32
+//       reductions into HBM (the pages remark that the backward pays for
+//       atomic accumulation; these are where it does).
+// Nine 128 x 128 x 128 MMAs per (b, c) pair: S, dP, dV, dKh, dA, G Pm^T, dl Kh
+// and the chain product of (R).  One thread issues TMA and MMAs; 256 threads
+// run the epilogues (thread = TMEM lane / tile row, half of the columns).
+// Persistent CTAs, query chunks in decreasing order of work.  Every wait is
+// bounded; on timeout the kernel sets the device error flag and stops.
+//
+// Shared memory: seven 32 KB bf16 operand tiles (dout_b, Qt, Kh_c, V_c / P,
+// Pm_c, dl, G).  TMEM columns: [0,128) S then dV, [128,256) dP then dKh,
+// [256,384) G, [384,512) the chain product U then dA.
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace path {
+namespace {
+
+constexpr int kC = 128;
+constexpr int kTile = kC * kC * 2;
+constexpr int kThreadsB = 256;
+constexpr uint32_t kColS = 0, kColDP = 128, kColG = 256, kColU = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+enum { kDO = 0, kQt, kKh, kVP, kPm, kDL, kGs, kSlots };
+
+struct BBars {
+    uint64_t tma, mma;
+    uint32_t tmem_base;
+    int ok;
+    float rD[kC];  // dout . out - dlse
+    float rL[kC];  // lse * log2e
+};
+constexpr int kSmemB = (int)sizeof(BBars) + 1023 + kSlots * kTile;
+static_assert(kSmemB <= 232448, "shared memory budget exceeded");
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_scan_tc_kernel(const __grid_constant__ BwdTcMaps maps, BwdTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    BBars &bars = *reinterpret_cast<BBars *>(smem_raw);
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(BBars) + 1023) &
+        ~static_cast<uintptr_t>(1023));
+    const uint32_t s0 = smem_u32(tiles);
+    auto slot = [&](int s) { return s0 + (uint32_t)(s * kTile); };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int T = (a.N - 1) * a.BH;
+    const float sl2 = a.scale * kLog2e;
+
+    if (tid == 0) {
+        mbar_init(&bars.tma, 1);
+        mbar_init(&bars.mma, 1);
+        bars.ok = 1;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&bars.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars.tmem_base;
+    uint32_t ph_tma = 0, ph_mma = 0;
+
+    // Thread 0 waits for the MMAs issued so far; the result is shared by the block.
+    auto mma_sync = [&]() {
+        if (tid == 0) {
+            tc::mma_commit(&bars.mma);
+            if (!mbar_wait(&bars.mma, ph_mma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
+        }
+        ph_mma ^= 1;
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        return bars.ok != 0;
+    };
+    // Thread 0 waits for the TMA loads issued against `bytes`; shared result.
+    auto tma_sync = [&]() {
+        if (tid == 0) {
+            if (!mbar_wait(&bars.tma, ph_tma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
+            tc::fence_after_sync();
+        }
+        ph_tma ^= 1;
+        __syncthreads();
+        return bars.ok != 0;
+    };
+    auto load_tile = [&](int s, const CUtensorMap *map, int y, int z) {
+        tc::tma_load_3d(tiles + s * kTile, map, 0, y, z, &bars.tma);
+        tc::tma_load_3d(tiles + s * kTile + kTile / 2, map, 64, y, z, &bars.tma);
+    };
+    // 64 fp32 TMEM values (this thread's row, columns half*64 ..) -> bf16 tile row
+    auto store_row = [&](uint32_t tile, const uint32_t (&v)[64]) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            tc::sts128(tile + tc::swz_off(r, half * 8 + q, kC),
+                       tc::pack2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1])),
+                       tc::pack2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3])),
+                       tc::pack2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5])),
+                       tc::pack2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7])));
+    };
+    // 64 fp32 TMEM values added into 64 consecutive floats of global memory
+    auto red_row = [&](float *dst, const uint32_t (&v)[64]) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            tc::red_add_v4(dst + 4 * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    };
+
+    for (int job = blockIdx.x; job < T && bars.ok; job += gridDim.x) {
+        const int b = a.N - 1 - job / a.BH, bh = job % a.BH;  // b >= 1
+        const int nq = min(kC, a.L - b * kC);
+        const int pair0 = b * (b - 1) / 2;  // first (b, c) pair of this chunk in the head
+        const size_t head_rows = (size_t)bh * a.Lp;
+
+        // row constants; partial dot products in the (idle) dl tile
+        {
+            float s = 0.f;
+            if (r < nq) {
+                const size_t off = ((size_t)bh * a.L + (size_t)b * kC + r) * kC + half * 64;
+                const uint4 *po = reinterpret_cast<const uint4 *>(a.out + off);
+                const uint4 *pd = reinterpret_cast<const uint4 *>(a.dout + off);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 x = po[i], y = pd[i];
+                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xs[e]));
+                        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ys[e]));
+                        s = fmaf(fx.x, fy.x, fmaf(fx.y, fy.y, s));
+                    }
+                }
+            }
+            float *part = reinterpret_cast<float *>(tiles + kDL * kTile);
+            part[half * kC + r] = s;
+            __syncthreads();
+            if (half == 0) {
+                float D = 0.f, l = 0.f;
+                if (r < nq) {
+                    const size_t row = (size_t)bh * a.L + (size_t)b * kC + r;
+                    D = part[r] + part[kC + r] - (a.dlse ? a.dlse[row] : 0.f);
+                    l = a.lse[row] * kLog2e;
+                }
+                bars.rD[r] = D;
+                bars.rL[r] = l;
+            }
+        }
+        // (R) dout_b and Qh_b, then the chain
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bars.tma, 2 * kTile);
+            load_tile(kDO, &maps.dout, b * kC, bh);
+            load_tile(kQt, &maps.qh, b * kC, bh);
+        }
+        if (!tma_sync()) break;
+        bool ok = true;
+        for (int c = b - 1; c >= 0; --c) {
+            if (tid == 0) {
+                tc::tma_store_3d(&maps.qts, tiles + kQt * kTile, 0, (pair0 + c) * kC, bh);
+                tc::tma_store_3d(&maps.qts, tiles + kQt * kTile + kTile / 2, 64, (pair0 + c) * kC, bh);
+                tc::bulk_commit();
+            }
+            if (c == 0) break;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bars.tma, kTile);
+                load_tile(kPm, &maps.pm, c * kC, bh);
+            }
+            if (!(ok = tma_sync())) break;
+            if (tid == 0)
+                tc::gemm128_lo<true>(tmem + kColU, tc::desc_lo(slot(kQt), false),
+                                     tc::desc_lo(slot(kPm), true), false);
+            if (tid == 0) tc::bulk_wait_read();  // the store of Qt_c has read the tile
+            if (!(ok = mma_sync())) break;
+            {
+                uint32_t v[64];
+                tc::tmem_ld64(tmem + lane_off + kColU + half * 64, v);
+                store_row(slot(kQt), v);
+            }
+            tc::fence_proxy_async();
+            __syncthreads();
+        }
+        if (!ok) break;
+        if (tid == 0) {
+            tc::bulk_wait();  // every Qt_c is in HBM before it is loaded back
+            tc::fence_proxy_async_global();
+        }
+        __syncthreads();
+
+        // (L)
+        for (int c = 0; c < b; ++c) {
+            const int k0 = c * kC;
+            if (tid == 0) {
+                // Qt_0 is still in its tile from the end of (R)
+                mbar_arrive_expect_tx(&bars.tma, (c > 0 ? 4 : 2) * kTile);
+                if (c > 0) load_tile(kQt, &maps.qts, (pair0 + c) * kC, bh);
+                load_tile(kKh, &maps.kh, k0, bh);
+                load_tile(kVP, &maps.v, k0, bh);
+                if (c > 0) load_tile(kPm, &maps.pm, k0, bh);
+                if (c + 1 < b) {
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        tc::tma_prefetch_3d(&maps.qts, 64 * x, (pair0 + c + 1) * kC, bh);
+                        tc::tma_prefetch_3d(&maps.kh, 64 * x, k0 + kC, bh);
+                        tc::tma_prefetch_3d(&maps.v, 64 * x, k0 + kC, bh);
+                        tc::tma_prefetch_3d(&maps.pm, 64 * x, k0 + kC, bh);
+                    }
+                }
+            }
+            if (!(ok = tma_sync())) break;
+            if (tid == 0) {
+                tc::gemm128_lo<false>(tmem + kColS, tc::desc_lo(slot(kQt), false),
+                                      tc::desc_lo(slot(kKh), false), false);  // S = Qt Kh^T
+                tc::gemm128_lo<false>(tmem + kColDP, tc::desc_lo(slot(kDO), false),
+                                      tc::desc_lo(slot(kVP), false), false);  // dP = dout V^T
+            }
+            if (!(ok = mma_sync())) break;
+            // P and dl (scaled) as bf16 tiles; V's tile takes P
+            {
+                uint32_t sv[64], pv[64];
+                tc::tmem_ld64(tmem + lane_off + kColS + half * 64, sv);
+                tc::tmem_ld64(tmem + lane_off + kColDP + half * 64, pv);
+                const float lr = bars.rL[r], dr = bars.rD[r];
+                const bool live = r < nq;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float p[8], g[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float x = __uint_as_float(sv[q * 8 + e]);
+                        p[e] = live ? ex2(fmaf(x, sl2, -lr)) : 0.f;
+                        g[e] = a.scale * p[e] * (__uint_as_float(pv[q * 8 + e]) - dr);
+                    }
+                    const uint32_t off = tc::swz_off(r, half * 8 + q, kC);
+                    tc::sts128(slot(kVP) + off, tc::pack2(p[0], p[1]), tc::pack2(p[2], p[3]),
+                               tc::pack2(p[4], p[5]), tc::pack2(p[6], p[7]));
+                    tc::sts128(slot(kDL) + off, tc::pack2(g[0], g[1]), tc::pack2(g[2], g[3]),
+                               tc::pack2(g[4], g[5]), tc::pack2(g[6], g[7]));
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+            if (tid == 0) {
+                // dV = P^T dout, dKh = dl^T Qt
+                tc::gemm128_lo2<true, true>(tmem + kColS, tc::desc_lo(slot(kVP), true),
+                                            tc::desc_lo(slot(kDO), true), false);
+                tc::gemm128_lo2<true, true>(tmem + kColDP, tc::desc_lo(slot(kDL), true),
+                                            tc::desc_lo(slot(kQt), true), false);
+                if (c > 0) {
+                    // dA = Qt^T G, then G <- G Pm^T
+                    tc::gemm128_lo2<true, true>(tmem + kColU, tc::desc_lo(slot(kQt), true),
+                                                tc::desc_lo(slot(kGs), true), false);
+                    tc::gemm128_lo<false>(tmem + kColG, tc::desc_lo(slot(kGs), false),
+                                          tc::desc_lo(slot(kPm), false), false);
+                }
+                // G += dl Kh
+                tc::gemm128_lo<true>(tmem + kColG, tc::desc_lo(slot(kDL), false),
+                                     tc::desc_lo(slot(kKh), true), c > 0);
+            }
+            if (!(ok = mma_sync())) break;
+            {
+                uint32_t v[64];
+                const size_t krow = (head_rows + k0 + r) * kC + half * 64;
+                tc::tmem_ld64(tmem + lane_off + kColS + half * 64, v);
+                red_row(a.dV + krow, v);
+                tc::tmem_ld64(tmem + lane_off + kColDP + half * 64, v);
+                red_row(a.dKh + krow, v);
+                if (c > 0) {
+                    tc::tmem_ld64(tmem + lane_off + kColU + half * 64, v);
+                    red_row(a.dA + (((size_t)bh * a.N + c) * kC + r) * kC + half * 64, v);
+                }
+                tc::tmem_ld64(tmem + lane_off + kColG + half * 64, v);
+                store_row(slot(kGs), v);
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+        }
+        if (!ok) break;
+        // dQh_b = G (fp32)
+        {
+            uint32_t v[64];
+            tc::tmem_ld64(tmem + lane_off + kColG + half * 64, v);
+            float4 *dst = reinterpret_cast<float4 *>(a.dQh + (head_rows + (size_t)b * kC + r) * kC +
+                                                     half * 64);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    if (tid == 0) tc::bulk_wait();  // no store may outlive the CTA's shared memory
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_scan_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_sms,
+                               cudaStream_t st) {
+    const int total = (a.N - 1) * a.BH;
+    if (total <= 0) return cudaSuccess;
+    const int grid = total < num_sms ? total : num_sms;
+    cudaError_t e = cudaFuncSetAttribute(bwd_scan_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemB);
+    if (e != cudaSuccess) return e;
+    bwd_scan_tc_kernel<<<grid, kThreadsB, kSmemB, st>>>(maps, a);
+    return cudaGetLastError();
+}
+
+}  // namespace path

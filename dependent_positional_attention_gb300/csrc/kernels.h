@@ -68,6 +68,30 @@ size_t bwd_prep_smem(int C);
 // bf16_io: q, k, v, w, out, dout and the gradients dq, dk, dv, dw in bf16
 cudaError_t launch_bwd(const BwdArgs &a, bool bf16_io, cudaStream_t st);
 
+// Tensor-core backward scan (bf16, head_dim 128, chunk 128, PaTH without the
+// forget gate).  Maps: 3-D bf16 tensors [BH][rows][128] in 64 x 128 boxes
+// with the 128-byte swizzle: qh, kh, pm from the tensor-core prep (rows =
+// Lp), v and dout (rows = L), qts the carried-row store (rows = 128 times
+// the number of (query chunk, earlier key chunk) pairs of a head).
+struct BwdTcMaps {
+    CUtensorMap qh, kh, pm, v, dout, qts;
+};
+
+struct BwdTcArgs {
+    const __nv_bfloat16 *out, *dout;  // [BH][L][128]
+    const float *lse, *dlse;          // [BH][L]; dlse may be null
+    float *dQh, *dKh, *dV;            // [BH][Lp][128] fp32 (dKh, dV accumulated)
+    float *dA;                        // [BH][N][128][128] fp32 (accumulated)
+    float scale;
+    int BH, L, Lp, N;
+    uint32_t *err;
+};
+
+cudaError_t launch_bwd_scan_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_sms,
+                               cudaStream_t st);
+// The CUDA-core backward prep alone (after a tensor-core scan).
+cudaError_t launch_bwd_prep(const BwdArgs &a, bool bf16_io, cudaStream_t st);
+
 struct DecodeArgs {
     void *k_cache, *v_cache;
     const void *q_t, *k_t, *v_t, *w_t;

@@ -106,3 +106,17 @@ def test_headline_shape_sampled_heads():
     x = wl.prefill_inputs(8, 12, 4096, 128, "bf16", seed=0)
     got, ref = run(x, heads=[0, 95])
     check(got, ref, 2e-2)
+
+
+@pytest.mark.parametrize("L", [1, 128, 129, 700])
+def test_tensor_core_scan_ragged(L):
+    """bf16, head_dim 128, chunk 128: the backward scan on the tensor cores
+    (L <= 128 has no earlier key chunk and skips it)."""
+    got, ref = run(wl.prefill_inputs(1, 3, L, 128, "bf16", seed=L), use_dlse=True)
+    check(got, ref, 2e-2)
+
+
+def test_bf16_d128_cuda_core_route():
+    """chunk 64 keeps bf16 head_dim 128 on the CUDA-core scan."""
+    got, ref = run(wl.prefill_inputs(1, 2, 300, 128, "bf16", seed=12), chunk=64)
+    check(got, ref, 2e-2)
