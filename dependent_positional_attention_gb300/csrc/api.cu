@@ -168,7 +168,11 @@ path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
     p->off_Wt = off; off = align_up(off + rows * d * 4, 256);
     p->off_Sd = off; off = align_up(off + cc * 4, 256);
     p->off_F = off; off = align_up(off + rows * 4, 256);
-    p->off_scratch = off; off = align_up(off + (cc * kBwdPrepCC + BH * N * 2 * C * d) * 4, 256);
+    // the CUDA-core backward prep's scratch, or the tensor-core one's tiles
+    const size_t simt_scratch = (cc * kBwdPrepCC + BH * N * 2 * C * d) * 4;
+    const size_t tc_tiles = p->tc ? rows * 128 * (kBwdBf16Tiles * 2 + kBwdF32Tiles * 4) : 0;
+    p->off_scratch = off;
+    off = align_up(off + (simt_scratch > tc_tiles ? simt_scratch : tc_tiles), 256);
     p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * 4, 256);
     // zeroed from here on
     p->off_dQh = off; off = align_up(off + rows * d * 4, 256);
@@ -246,6 +250,198 @@ template <class T> T *at(void *base, size_t off) {
 path_status_t cuda_status(cudaError_t e, const char *what) {
     if (e != cudaSuccess) return fail(PATH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
     return ok();
+}
+
+// Builds one batched chunk contraction: operands are registered by map, up
+// to eight distinct maps and six products.
+struct GemmBuilder {
+    ChunkGemmMaps maps;
+    ChunkGemmArgs args;
+    const CUtensorMap *ids[8];
+    int nm = 0;
+    explicit GemmBuilder(const ChunkGemmArgs &base) : args(base) {
+        args.np = 0;
+        args.alpha = 1.f;
+        args.E = nullptr;
+        args.rowscale = nullptr;
+        args.mask = 0;
+        args.out_f32 = nullptr;
+        args.out_bf16 = nullptr;
+        args.out_final = 0;
+    }
+    int map_of(const CUtensorMap *m) {
+        for (int i = 0; i < nm; ++i)
+            if (ids[i] == m) return i;
+        ids[nm] = m;
+        maps.m[nm] = *m;
+        return nm++;
+    }
+    // D += (neg ? -1 : 1) * op(A) op(B), op = transpose when at / bt
+    GemmBuilder &prod(const CUtensorMap *A, bool at, const CUtensorMap *B, bool bt,
+                      bool neg = false) {
+        ChunkGemmProd &p = args.prod[args.np++];
+        p.a = (int8_t)map_of(A);
+        p.b = (int8_t)map_of(B);
+        p.at = at;
+        p.bt = bt;
+        p.neg = neg;
+        return *this;
+    }
+};
+
+// The backward prep of the tensor-core route (formulas: backward_simt.cu,
+// bwd_prep_kernel; Ti as in backward_prep_tc.cu).  X^T is written Xt.
+path_status_t run_bwd_prep_tc(const path_prefill_desc_t *desc, const BwdPlan &p,
+                              const BwdArgs &ba, void *workspace, cudaStream_t st) {
+    const size_t rows = (size_t)p.BH * p.Lp;
+    char *u = at<char>(workspace, p.off_scratch);
+    __nv_bfloat16 *bt[kBwdBf16Tiles];
+    float *ft[kBwdF32Tiles];
+    for (int i = 0; i < kBwdBf16Tiles; ++i)
+        bt[i] = reinterpret_cast<__nv_bfloat16 *>(u + (size_t)i * rows * 256);
+    for (int i = 0; i < kBwdF32Tiles; ++i)
+        ft[i] = reinterpret_cast<float *>(u + (size_t)kBwdBf16Tiles * rows * 256 +
+                                          (size_t)i * rows * 512);
+    enum { a_, b_, T_, Ti_, Z_, Y_, Wt_, P_, dSd_, dQh_, dKh_, dA_, dWt_, R1_, da_, R2_, db_,
+           R3_, R4_, dT_, dX_, dG_ };
+    enum { G_, Sd_, dP_, dXf_, dLo_, dwp_ };
+    static_assert(dG_ + 1 == kBwdBf16Tiles && dwp_ + 1 == kBwdF32Tiles, "tile counts");
+    CUtensorMap mq, mk, mv, mw, mdo, mt[kBwdBf16Tiles];
+    bool enc = encode_tmap_bf16_3d(&mq, ba.q, 128, p.L, p.BH, 64, 128) &&
+               encode_tmap_bf16_3d(&mk, ba.k, 128, p.L, p.BH, 64, 128) &&
+               encode_tmap_bf16_3d(&mv, ba.v, 128, p.L, p.BH, 64, 128) &&
+               encode_tmap_bf16_3d(&mw, ba.w, 128, p.L, p.BH, 64, 128) &&
+               encode_tmap_bf16_3d(&mdo, ba.dout, 128, p.L, p.BH, 64, 128);
+    for (int i = 0; i < kBwdBf16Tiles && enc; ++i)
+        enc = encode_tmap_bf16_3d(&mt[i], bt[i], 128, p.Lp, p.BH, 64, 128);
+    if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+    ChunkGemmArgs base;
+    base.BH = p.BH; base.L = p.L; base.Lp = p.Lp; base.N = p.N;
+    base.err = error_flag_ptr();
+    path_status_t s = ok();
+    auto run = [&](GemmBuilder &g, const char *what) {
+        if (s == PATH_OK) s = cuda_status(launch_chunk_gemm_tc(g.maps, g.args, st), what);
+    };
+    const float *dQh = ba.dQh, *dKh = ba.dKh;
+    {   // G = W Wt (fp32, for the solve and dbeta)
+        GemmBuilder g(base); g.prod(&mw, false, &mw, true); g.args.out_f32 = ft[G_]; run(g, "G");
+    }
+    {   // a = M_le * (Q Wt)
+        GemmBuilder g(base); g.prod(&mq, false, &mw, true); g.args.mask = 1;
+        g.args.out_bf16 = bt[a_]; run(g, "a");
+    }
+    {   // b = M_gt * (K Wt)
+        GemmBuilder g(base); g.prod(&mk, false, &mw, true); g.args.mask = 2;
+        g.args.out_bf16 = bt[b_]; run(g, "b");
+    }
+    if (s != PATH_OK) return s;
+    s = cuda_status(launch_bwd_solve(ft[G_], ba.beta, bt[T_], bt[Ti_], p.BH, p.L, p.Lp, p.N, st),
+                    "solve");
+    {   // Z = a T
+        GemmBuilder g(base); g.prod(&mt[a_], false, &mt[T_], false); g.args.out_bf16 = bt[Z_];
+        run(g, "Z");
+    }
+    {   // Y = b Tt
+        GemmBuilder g(base); g.prod(&mt[b_], false, &mt[T_], true); g.args.out_bf16 = bt[Y_];
+        run(g, "Y");
+    }
+    {   // Wt = T W
+        GemmBuilder g(base); g.prod(&mt[T_], false, &mw, false); g.args.out_bf16 = bt[Wt_];
+        run(g, "Wt");
+    }
+    {   // Sd = Q Kt - a Yt
+        GemmBuilder g(base); g.prod(&mq, false, &mk, true).prod(&mt[a_], false, &mt[Y_], true, true);
+        g.args.out_f32 = ft[Sd_]; run(g, "Sd");
+    }
+    {   // dP = dout Vt
+        GemmBuilder g(base); g.prod(&mdo, false, &mv, true); g.args.out_f32 = ft[dP_];
+        run(g, "dP");
+    }
+    if (s != PATH_OK) return s;
+    BwdDiagArgs da;
+    da.out = static_cast<const __nv_bfloat16 *>(ba.out);
+    da.dout = static_cast<const __nv_bfloat16 *>(ba.dout);
+    da.lse = ba.lse; da.dlse = ba.dlse; da.Sd = ft[Sd_]; da.dP = ft[dP_];
+    da.P = bt[P_]; da.dSd = bt[dSd_]; da.scale = desc->scale;
+    da.BH = p.BH; da.L = p.L; da.Lp = p.Lp; da.N = p.N;
+    s = cuda_status(launch_bwd_diag(da, st), "diagonal block");
+    if (s == PATH_OK) s = cuda_status(launch_bwd_cvt(dQh, bt[dQh_], rows * 128, st), "cvt");
+    if (s == PATH_OK) s = cuda_status(launch_bwd_cvt(dKh, bt[dKh_], rows * 128, st), "cvt");
+    if (s == PATH_OK) s = cuda_status(launch_bwd_cvt(ba.dA, bt[dA_], rows * 128, st), "cvt");
+    {   // dv = dV (scan) + Pt dout
+        GemmBuilder g(base); g.prod(&mt[P_], true, &mdo, false); g.args.E = ba.dV;
+        g.args.out_bf16 = static_cast<__nv_bfloat16 *>(ba.dv); g.args.out_final = 1; run(g, "dv");
+    }
+    {   // dWt = -W dA
+        GemmBuilder g(base); g.prod(&mw, false, &mt[dA_], false); g.args.alpha = -1.f;
+        g.args.out_bf16 = bt[dWt_]; run(g, "dWt");
+    }
+    {   // R1 = dSd b
+        GemmBuilder g(base); g.prod(&mt[dSd_], false, &mt[b_], false); g.args.out_bf16 = bt[R1_];
+        run(g, "R1");
+    }
+    {   // da = M_le * -(R1 Tt + dQh Wtt)
+        GemmBuilder g(base); g.prod(&mt[R1_], false, &mt[T_], true).prod(&mt[dQh_], false, &mt[Wt_], true);
+        g.args.alpha = -1.f; g.args.mask = 1; g.args.out_bf16 = bt[da_]; run(g, "da");
+    }
+    {   // R2 = dSdt a + dKh Wt
+        GemmBuilder g(base); g.prod(&mt[dSd_], true, &mt[a_], false).prod(&mt[dKh_], false, &mw, true);
+        g.args.out_bf16 = bt[R2_]; run(g, "R2");
+    }
+    {   // db = M_gt * -(R2 T)
+        GemmBuilder g(base); g.prod(&mt[R2_], false, &mt[T_], false); g.args.alpha = -1.f;
+        g.args.mask = 2; g.args.out_bf16 = bt[db_]; run(g, "db");
+    }
+    {   // R3 = dSd b + dQh Wt
+        GemmBuilder g(base); g.prod(&mt[dSd_], false, &mt[b_], false).prod(&mt[dQh_], false, &mw, true);
+        g.args.out_bf16 = bt[R3_]; run(g, "R3");
+    }
+    {   // R4 = W dKht
+        GemmBuilder g(base); g.prod(&mw, false, &mt[dKh_], true); g.args.out_bf16 = bt[R4_];
+        run(g, "R4");
+    }
+    {   // dT = -at R3 - R4 b + dWt Wt
+        GemmBuilder g(base);
+        g.prod(&mt[a_], true, &mt[R3_], false, true).prod(&mt[R4_], false, &mt[b_], false, true)
+            .prod(&mt[dWt_], false, &mw, true);
+        g.args.out_bf16 = bt[dT_]; run(g, "dT");
+    }
+    {   // dX = Tit dT
+        GemmBuilder g(base); g.prod(&mt[Ti_], true, &mt[dT_], false); g.args.out_f32 = ft[dXf_];
+        g.args.out_bf16 = bt[dX_]; run(g, "dX");
+    }
+    {   // dLo = strict_lower(-dX Tt); dG = diag(beta) dLo
+        GemmBuilder g(base); g.prod(&mt[dX_], false, &mt[T_], true); g.args.alpha = -1.f;
+        g.args.mask = 3; g.args.out_f32 = ft[dLo_]; g.args.rowscale = ba.beta;
+        g.args.out_bf16 = bt[dG_]; run(g, "dLo");
+    }
+    if (s != PATH_OK) return s;
+    s = cuda_status(launch_bwd_dbeta(ft[dXf_], ft[dLo_], ft[G_], ba.dbeta, p.BH, p.L, p.Lp, p.N, st),
+                    "dbeta");
+    {   // dw (first half) = -Wt dAt - Zt dQh - Yt dKh + Tt dWt
+        GemmBuilder g(base);
+        g.prod(&mt[Wt_], false, &mt[dA_], true, true).prod(&mt[Z_], true, &mt[dQh_], false, true)
+            .prod(&mt[Y_], true, &mt[dKh_], false, true).prod(&mt[T_], true, &mt[dWt_], false);
+        g.args.out_f32 = ft[dwp_]; run(g, "dw1");
+    }
+    {   // dw = (first half) + dat Q + dbt K + dG W + dGt W
+        GemmBuilder g(base);
+        g.prod(&mt[da_], true, &mq, false).prod(&mt[db_], true, &mk, false)
+            .prod(&mt[dG_], false, &mw, false).prod(&mt[dG_], true, &mw, false);
+        g.args.E = ft[dwp_]; g.args.out_bf16 = static_cast<__nv_bfloat16 *>(ba.dw);
+        g.args.out_final = 1; run(g, "dw");
+    }
+    {   // dq = dQh + dSd K + da W
+        GemmBuilder g(base); g.prod(&mt[dSd_], false, &mk, false).prod(&mt[da_], false, &mw, false);
+        g.args.E = dQh; g.args.out_bf16 = static_cast<__nv_bfloat16 *>(ba.dq); g.args.out_final = 1;
+        run(g, "dq");
+    }
+    {   // dk = dKh + dSdt Q + db W
+        GemmBuilder g(base); g.prod(&mt[dSd_], true, &mq, false).prod(&mt[db_], false, &mw, false);
+        g.args.E = dKh; g.args.out_bf16 = static_cast<__nv_bfloat16 *>(ba.dk); g.args.out_final = 1;
+        run(g, "dk");
+    }
+    return s;
 }
 
 }  // namespace
@@ -505,7 +701,7 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         tb.err = error_flag_ptr();
         s = cuda_status(launch_bwd_scan_tc(bm, tb, sms, st), "tensor-core backward scan launch");
         if (s != PATH_OK) return s;
-        return cuda_status(launch_bwd_prep(ba, true, st), "backward prep launch");
+        return run_bwd_prep_tc(desc, p, ba, workspace, st);
     }
     PrepSimtArgs pa;
     pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;

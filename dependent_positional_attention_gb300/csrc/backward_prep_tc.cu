@@ -1,0 +1,265 @@
+// Backward prep on tensor cores (bf16, head_dim 128, chunk 128, PaTH without
+// the forget gate): the chunk's own causal block and the gradient through
+// the boundary adjustment and the UT transform, as a sequence of batched
+// 128 x 128 x 128 contractions over all chunks (bf16 operands, fp32
+// accumulation in TMEM) plus four small CUDA-core steps.  The formulas are
+// those of bwd_prep_kernel (backward_simt.cu); here
+//   T = Ti diag(beta),  Ti = (I + strict_lower(diag(beta) G))^{-1},
+// so that the solve dX = (I + Lo)^{-T} dT becomes the product Ti^T dT.
+// Intermediate tiles live in the workspace as [BH][Lp][128] arrays.
+
+#include "common.cuh"
+#include "kernels.h"
+#include "simt_gemm.cuh"
+#include "tc.cuh"
+
+namespace path {
+namespace {
+
+constexpr int kC = 128;
+constexpr int kTile = kC * kC * 2;
+constexpr int kThreadsG = 128;
+
+struct GBars {
+    uint64_t tma, mma;
+    uint32_t tmem_base;
+    int ok;
+};
+constexpr int kSmemG = (int)sizeof(GBars) + 1023 + 2 * kTile;
+
+// D = alpha * sum_p (+/-) op(A_p) op(B_p) (+ E), masked, per chunk.
+__global__ void __launch_bounds__(kThreadsG)
+    chunk_gemm_tc_kernel(const __grid_constant__ ChunkGemmMaps maps, ChunkGemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    GBars &bars = *reinterpret_cast<GBars *>(smem_raw);
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(GBars) + 1023) &
+        ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = smem_u32(tiles), sB = sA + kTile;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chunk = blockIdx.x % a.N, bh = blockIdx.x / a.N;
+    const int c0 = chunk * kC;
+    const int n = min(kC, a.L - c0);
+
+    if (tid == 0) {
+        mbar_init(&bars.tma, 1);
+        mbar_init(&bars.mma, 1);
+        bars.ok = 1;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&bars.tmem_base, 128);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (tid == 0) {
+        for (int p = 0; p < a.np && bars.ok; ++p) {
+            const ChunkGemmProd &pr = a.prod[p];
+            mbar_arrive_expect_tx(&bars.tma, 2 * kTile);
+            tc::tma_load_3d(tiles, &maps.m[pr.a], 0, c0, bh, &bars.tma);
+            tc::tma_load_3d(tiles + kTile / 2, &maps.m[pr.a], 64, c0, bh, &bars.tma);
+            tc::tma_load_3d(tiles + kTile, &maps.m[pr.b], 0, c0, bh, &bars.tma);
+            tc::tma_load_3d(tiles + kTile + kTile / 2, &maps.m[pr.b], 64, c0, bh, &bars.tma);
+            if (!mbar_wait(&bars.tma, p & 1, a.err, nullptr, kWaitLimitNs)) {
+                bars.ok = 0;
+                break;
+            }
+            tc::fence_after_sync();
+            // A: op = X (K-major) or X^T (MN-major).  B: op = X is MN-major
+            // (rows of X along K), X^T is K-major.
+            const bool a_mn = pr.at, b_mn = !pr.bt;
+            const uint32_t idesc = tc::idesc_bf16(128, 128, a_mn, b_mn) | (pr.neg ? (1u << 13) : 0u);
+            const uint32_t a_lo = tc::desc_lo(sA, a_mn), b_lo = tc::desc_lo(sB, b_mn);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+                tc::mma_bf16_lohi(tmem, a_lo + (a_mn ? (uint32_t)(kk * 128) : koff),
+                                  b_lo + (b_mn ? (uint32_t)(kk * 128) : koff), idesc,
+                                  (p > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&bars.mma);
+            // the tiles are reloaded for the next product only after this one read them
+            if (!mbar_wait(&bars.mma, p & 1, a.err, nullptr, kWaitLimitNs)) {
+                bars.ok = 0;
+                break;
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (bars.ok) {
+        const int r = tid;
+        const size_t ws_row = ((size_t)bh * a.Lp + c0 + r) * kC;
+        const size_t io_row = ((size_t)bh * a.L + c0 + r) * kC;
+        const bool live = r < n;
+        const float rs = (a.rowscale && live) ? a.rowscale[(size_t)bh * a.L + c0 + r] : 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc * 32, v);
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int j = cc * 32 + e;
+                float y = a.alpha * __uint_as_float(v[e]);
+                if (a.E) y += a.E[ws_row + j];
+                const bool keep = live && (a.mask == 0 || (a.mask == 1 && j <= r) ||
+                                           (a.mask == 2 && j > r) || (a.mask == 3 && j < r));
+                x[e] = keep ? y : 0.f;
+            }
+            if (a.out_f32) {
+                float4 *dst = reinterpret_cast<float4 *>(a.out_f32 + ws_row + cc * 32);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            }
+            if (a.out_bf16 && (!a.out_final || live)) {
+                const float s = a.rowscale ? rs : 1.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out_bf16 + (a.out_final ? io_row : ws_row) +
+                                                       cc * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(tc::pack2(s * x[8 * q], s * x[8 * q + 1]),
+                                        tc::pack2(s * x[8 * q + 2], s * x[8 * q + 3]),
+                                        tc::pack2(s * x[8 * q + 4], s * x[8 * q + 5]),
+                                        tc::pack2(s * x[8 * q + 6], s * x[8 * q + 7]));
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 128);
+    }
+}
+
+// Ti = (I + strict_lower(diag(beta) G))^{-1} (fp32 solve, as the forward's
+// CUDA-core prep, with the rows of G scaled by beta and unit coefficients),
+// written as bf16 Ti and T = Ti diag(beta).  One block per chunk.
+__global__ void __launch_bounds__(kThreads) bwd_solve_kernel(const float *G, const float *beta,
+                                                             __nv_bfloat16 *T, __nv_bfloat16 *Ti,
+                                                             int L, int Lp, int N) {
+    extern __shared__ float smem[];
+    float *big = smem;                      // 2 C (C + 1)
+    float *Gs = smem + 2 * kC * (kC + 1);   // C x C: beta-scaled G, then Ti
+    float *bs = Gs + kC * kC, *ones = bs + kC;
+    const int chunk = blockIdx.x, bh = blockIdx.y;
+    const int c0 = chunk * kC, n = min(kC, L - c0);
+    const size_t base = ((size_t)bh * Lp + c0) * kC;
+    for (int r = threadIdx.x; r < kC; r += kThreads) {
+        bs[r] = r < n ? beta[(size_t)bh * L + c0 + r] : 0.f;
+        ones[r] = 1.f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * kC; e += kThreads) Gs[e] = bs[e / kC] * G[base + e];
+    __syncthreads();
+    ut_solve(Gs, ones, kC, kC, Gs, big);
+    for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+        const float t = Gs[e];
+        Ti[base + e] = __float2bfloat16_rn(t);
+        T[base + e] = __float2bfloat16_rn(t * bs[e % kC]);
+    }
+}
+
+// The chunk's own block: P = exp(scale Sd - lse) (j <= i), dSd = scale P (dP -
+// dout . out + dlse), as bf16 tiles.  One block per chunk.
+__global__ void __launch_bounds__(kThreads) bwd_diag_kernel(BwdDiagArgs a) {
+    __shared__ float rD[kC], rL[kC];
+    const int chunk = blockIdx.x, bh = blockIdx.y;
+    const int c0 = chunk * kC, n = min(kC, a.L - c0);
+    const size_t base = ((size_t)bh * a.Lp + c0) * kC;
+    for (int r = threadIdx.x; r < kC; r += kThreads) {
+        float D = 0.f, l = 0.f;
+        if (r < n) {
+            const size_t row = (size_t)bh * a.L + c0 + r;
+            const __nv_bfloat16 *o = a.out + row * kC, *g = a.dout + row * kC;
+            for (int m = 0; m < kC; ++m) D = fmaf(__bfloat162float(o[m]), __bfloat162float(g[m]), D);
+            if (a.dlse) D -= a.dlse[row];
+            l = a.lse[row];
+        }
+        rD[r] = D;
+        rL[r] = l;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+        const int r = e / kC, j = e - r * kC;
+        float p = 0.f;
+        if (r < n && j <= r) p = expf(a.scale * a.Sd[base + e] - rL[r]);
+        a.P[base + e] = __float2bfloat16_rn(p);
+        a.dSd[base + e] = __float2bfloat16_rn(a.scale * p * (a.dP[base + e] - rD[r]));
+    }
+}
+
+__global__ void bwd_cvt_kernel(const float *x, __nv_bfloat16 *y, size_t n4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = reinterpret_cast<const float4 *>(x)[i];
+        reinterpret_cast<uint2 *>(y)[i] = make_uint2(tc::pack2(v.x, v.y), tc::pack2(v.z, v.w));
+    }
+}
+
+// dbeta_s = dX_ss + sum_{t<s} dLo_st G_st, one thread per row.
+__global__ void bwd_dbeta_kernel(const float *dX, const float *dLo, const float *G, float *dbeta,
+                                 int L, int Lp, int N, int BH) {
+    const int row = blockIdx.x * blockDim.x + threadIdx.x;  // over BH * Lp
+    if (row >= BH * Lp) return;
+    const int bh = row / Lp, i = row % Lp;
+    if (i >= L) return;
+    const int s = i % kC;
+    const size_t base = (size_t)row * kC;
+    float v = dX[base + s];
+    for (int t = 0; t < s; ++t) v = fmaf(dLo[base + t], G[base + t], v);
+    dbeta[(size_t)bh * L + i] = v;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs &a,
+                                 cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_gemm_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemG);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    chunk_gemm_tc_kernel<<<a.N * a.BH, kThreadsG, kSmemG, st>>>(maps, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_solve(const float *G, const float *beta, __nv_bfloat16 *T,
+                             __nv_bfloat16 *Ti, int BH, int L, int Lp, int N, cudaStream_t st) {
+    const size_t sm = sizeof(float) * (2 * kC * (kC + 1) + kC * kC + 2 * kC);
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    bwd_solve_kernel<<<dim3(N, BH), kThreads, sm, st>>>(G, beta, T, Ti, L, Lp, N);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_diag(const BwdDiagArgs &a, cudaStream_t st) {
+    bwd_diag_kernel<<<dim3(a.N, a.BH), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_cvt(const float *x, __nv_bfloat16 *y, size_t n, cudaStream_t st) {
+    const size_t n4 = n / 4;
+    const int blocks = (int)((n4 + 255) / 256 < 4096 ? (n4 + 255) / 256 : 4096);
+    bwd_cvt_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(x, y, n4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dbeta(const float *dX, const float *dLo, const float *G, float *dbeta,
+                             int BH, int L, int Lp, int N, cudaStream_t st) {
+    const int rows = BH * Lp;
+    bwd_dbeta_kernel<<<(rows + 127) / 128, 128, 0, st>>>(dX, dLo, G, dbeta, L, Lp, N, BH);
+    return cudaGetLastError();
+}
+
+}  // namespace path

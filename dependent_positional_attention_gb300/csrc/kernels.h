@@ -63,6 +63,7 @@ struct BwdArgs {
 };
 
 constexpr int kBwdPrepCC = 11;  // C x C scratch matrices per chunk of the backward prep
+constexpr int kBwdBf16Tiles = 22, kBwdF32Tiles = 6;  // tensor-core backward prep intermediates
 size_t bwd_scan_smem(int C, int d);
 size_t bwd_prep_smem(int C);
 // bf16_io: q, k, v, w, out, dout and the gradients dq, dk, dv, dw in bf16
@@ -91,6 +92,47 @@ cudaError_t launch_bwd_scan_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int nu
                                cudaStream_t st);
 // The CUDA-core backward prep alone (after a tensor-core scan).
 cudaError_t launch_bwd_prep(const BwdArgs &a, bool bf16_io, cudaStream_t st);
+
+// Batched 128 x 128 x 128 contraction over all chunks of all heads (tensor
+// cores): per chunk, D = alpha * sum_p (+/-) op(A_p) op(B_p) (+ E), then an
+// optional mask, written as fp32 and/or bf16.  Operands are bf16 tensors
+// [BH][rows][128] through maps[a], maps[b] (the chunk's 128 rows); at / bt
+// select the transposed operand.
+struct ChunkGemmProd {
+    int8_t a, b, at, bt, neg;
+};
+struct ChunkGemmMaps {
+    CUtensorMap m[8];
+};
+struct ChunkGemmArgs {
+    int np;
+    ChunkGemmProd prod[6];
+    float alpha;
+    const float *E;            // [BH][Lp][128] added to the result, or null
+    const float *rowscale;     // [BH][L]: bf16 output rows scaled by it, or null
+    int mask;                  // 0 none, 1 keep j <= r, 2 keep j > r, 3 keep j < r
+    float *out_f32;            // [BH][Lp][128] or null
+    __nv_bfloat16 *out_bf16;   // [BH][Lp][128], or [BH][L][128] if out_final; or null
+    int out_final;
+    int BH, L, Lp, N;
+    uint32_t *err;
+};
+cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs &a,
+                                 cudaStream_t st);
+
+struct BwdDiagArgs {
+    const __nv_bfloat16 *out, *dout;
+    const float *lse, *dlse, *Sd, *dP;
+    __nv_bfloat16 *P, *dSd;
+    float scale;
+    int BH, L, Lp, N;
+};
+cudaError_t launch_bwd_solve(const float *G, const float *beta, __nv_bfloat16 *T,
+                             __nv_bfloat16 *Ti, int BH, int L, int Lp, int N, cudaStream_t st);
+cudaError_t launch_bwd_diag(const BwdDiagArgs &a, cudaStream_t st);
+cudaError_t launch_bwd_cvt(const float *x, __nv_bfloat16 *y, size_t n, cudaStream_t st);
+cudaError_t launch_bwd_dbeta(const float *dX, const float *dLo, const float *G, float *dbeta,
+                             int BH, int L, int Lp, int N, cudaStream_t st);
 
 struct DecodeArgs {
     void *k_cache, *v_cache;
