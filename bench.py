@@ -53,22 +53,15 @@ def prefill_flops(B, H, L, d, C=CHUNK):
 
 
 def backward_flops(B, H, L, d, C=CHUNK):
-    """FLOPs the CUDA-core backward executes (2 per multiply-add), per call.
-    Per (query chunk, earlier key chunk) pair: the stored carried-row chain
-    (2 C^2 d MACs), then S, dP, dV, dKh (4 C^2 d), dA (C d^2), E = G Wt^T
-    (C^2 d) and the G update (2 C^2 d): 9 C^2 d + C d^2 MACs.  Per chunk:
-    its own block (dP, dV: 2 C^2 d), the recomputed forward prep
-    (7 C^2 d + 3 C^3) and the prep backward (18 C^2 d + 9 C^3 + 2 C d^2)."""
+    """MMA FLOPs of one backward call on the tensor-core route (bf16,
+    d = C = 128), 2 C^2 d per 128 x 128 x 128 contraction.  Per (query chunk,
+    earlier key chunk) pair the scan runs nine: the carried-row chain product,
+    S, dP, dV, dKh, dA and the two of the carried-gradient update.  Per chunk
+    the recomputed prep runs twelve (its eleven plus P V) and the backward
+    prep thirty-seven (the products of its 22 batched contractions)."""
     N = math.ceil(L / C)
     pairs = N * (N - 1) / 2
-    macs = pairs * (9 * C * C * d + C * d * d) + N * (27 * C * C * d + 12 * C ** 3 + 2 * C * d * d)
-    return 2 * macs * B * H
-
-
-def fp32_alu_peak_tflops():
-    """FP32 CUDA-core peak: SMs x 128 FP32 lanes x 2 FLOPs (FMA) x 2070 MHz
-    (the maximum SM clock)."""
-    return torch.cuda.get_device_properties(0).multi_processor_count * 128 * 2 * 2070e6 / 1e12
+    return 2 * C * C * d * (9 * pairs + 49 * N) * B * H
 
 
 # DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
@@ -378,7 +371,7 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
     return res
 
 
-def backward_block(wlk, steps, warmup, ws):
+def backward_block(wlk, steps, warmup, ws, peaks):
     """path_attn_prefill_bwd on the forward's inputs and outputs, device-timed
     with CUDA events; the four launches of one call form one step."""
     x = wl.workload_inputs(wlk, seed=0, device="cuda")
@@ -405,15 +398,17 @@ def backward_block(wlk, steps, warmup, ws):
     B, H, L, d = wlk.batch, wlk.heads, wlk.seq_len, wlk.head_dim
     flops = backward_flops(B, H, L, d)
     tf = flops / (ms * 1e-3) / 1e12
-    peak = fp32_alu_peak_tflops()
+    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     res = {"workload": "PaTH prefill backward (dq, dk, dv, dw, dbeta) B%d H%d L%d d%d %s"
                        % (B, H, L, d, wlk.dtype),
            "tokens_per_s": job_throughput(B * L, ms, ws), "ms_per_step": ms,
            "flops_per_step": flops, "tflops": tf, "workspace_bytes": ws_t.numel(),
-           "roofline": {"kernel": "bwd_scan_kernel + bwd_prep_kernel + prep (CUDA cores, fp32)",
-                        "bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+           "roofline": {"kernel": "whole backward call: prep_tc_kernel + bwd_scan_tc_kernel + "
+                                  "chunk_gemm_tc_kernel x23 + solve/diag/cvt/dbeta",
+                        "bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                         "frac": tf / peak, "traffic": None,
-                        "peak_source": "derived: SMs x 128 FP32 lanes x 2 x 2070 MHz"}}
+                        "peak_source": peaks["source"] + " bf16 dense (sustained: a step of "
+                                       "about 30 launches)"}}
     del x, out, lse, dout, ws_t
     torch.cuda.empty_cache()
     return res
@@ -540,7 +535,7 @@ def main():
         extra["decode_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws, peaks)
         extra["decode_fox_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws,
                                                peaks, fox=True)
-        extra["backward_4k"] = backward_block(head, max(3, steps // 4), 3, ws)
+        extra["backward_4k"] = backward_block(head, max(3, steps // 2), 3, ws, peaks)
         extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
         extra["chunk_autotune_bf16_d64"] = autotune_block(
             wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (CUDA-core route)",

@@ -12,6 +12,7 @@
 #include "kernels.h"
 #include "simt_gemm.cuh"
 #include "tc.cuh"
+#include "ut_solve_tc.cuh"
 
 namespace path {
 namespace {
@@ -139,31 +140,33 @@ __global__ void __launch_bounds__(kThreadsG)
     }
 }
 
-// Ti = (I + strict_lower(diag(beta) G))^{-1} (fp32 solve, as the forward's
-// CUDA-core prep, with the rows of G scaled by beta and unit coefficients),
-// written as bf16 Ti and T = Ti diag(beta).  One block per chunk.
-__global__ void __launch_bounds__(kThreads) bwd_solve_kernel(const float *G, const float *beta,
-                                                             __nv_bfloat16 *T, __nv_bfloat16 *Ti,
-                                                             int L, int Lp, int N) {
-    extern __shared__ float smem[];
-    float *big = smem;                      // 2 C (C + 1)
-    float *Gs = smem + 2 * kC * (kC + 1);   // C x C: beta-scaled G, then Ti
-    float *bs = Gs + kC * kC, *ones = bs + kC;
-    const int chunk = blockIdx.x, bh = blockIdx.y;
+// Ti = (I + strict_lower(diag(beta) G))^{-1} by the tensor-core prep's blocked
+// solve in inverse mode, written as bf16 Ti and T = Ti diag(beta).  One block
+// of 256 threads per chunk.
+__global__ void __launch_bounds__(utc::kThr) bwd_solve_kernel(const float *G, const float *beta,
+                                                               __nv_bfloat16 *T, __nv_bfloat16 *Ti,
+                                                               int L, int Lp, int N) {
+    extern __shared__ uint8_t smem_raw[];
+    float *Gs = reinterpret_cast<float *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
+    float *Tf = Gs + kC * kC;
+    float *bs = Tf + kC * kC;
+    const int chunk = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const int c0 = chunk * kC, n = min(kC, L - c0);
     const size_t base = ((size_t)bh * Lp + c0) * kC;
-    for (int r = threadIdx.x; r < kC; r += kThreads) {
-        bs[r] = r < n ? beta[(size_t)bh * L + c0 + r] : 0.f;
-        ones[r] = 1.f;
+    if (tid < kC) bs[tid] = tid < n ? beta[(size_t)bh * L + c0 + tid] : 0.f;
+    for (int e = tid; e < kC * kC / 4; e += utc::kThr) {
+        const int r = e / (kC / 4), c = (e % (kC / 4)) * 4;
+        *reinterpret_cast<float4 *>(Gs + utc::sw(r, c)) = reinterpret_cast<const float4 *>(G + base)[e];
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < kC * kC; e += kThreads) Gs[e] = bs[e / kC] * G[base + e];
+    utc::ut_solve<true>(Gs, Tf, bs, tid);
     __syncthreads();
-    ut_solve(Gs, ones, kC, kC, Gs, big);
-    for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
-        const float t = Gs[e];
+    for (int e = tid; e < kC * kC; e += utc::kThr) {
+        const int r = e / kC, c = e % kC;
+        const float t = Tf[utc::sw(r, c)];
         Ti[base + e] = __float2bfloat16_rn(t);
-        T[base + e] = __float2bfloat16_rn(t * bs[e % kC]);
+        T[base + e] = __float2bfloat16_rn(t * bs[c]);
     }
 }
 
@@ -235,11 +238,11 @@ cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs 
 
 cudaError_t launch_bwd_solve(const float *G, const float *beta, __nv_bfloat16 *T,
                              __nv_bfloat16 *Ti, int BH, int L, int Lp, int N, cudaStream_t st) {
-    const size_t sm = sizeof(float) * (2 * kC * (kC + 1) + kC * kC + 2 * kC);
+    const size_t sm = sizeof(float) * (2 * kC * kC + kC) + 16;
     cudaError_t e =
         cudaFuncSetAttribute(bwd_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    bwd_solve_kernel<<<dim3(N, BH), kThreads, sm, st>>>(G, beta, T, Ti, L, Lp, N);
+    bwd_solve_kernel<<<dim3(N, BH), utc::kThr, sm, st>>>(G, beta, T, Ti, L, Lp, N);
     return cudaGetLastError();
 }
 
