@@ -143,7 +143,7 @@ struct BwdPlan {
     int BH, L, Lp, N, C, d;
     bool bf16;
     bool tc;  // bf16, head_dim 128, chunk 128: the tensor-core scan (PaTH calls)
-    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_dQh;
+    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_Dg, off_dQh;
     size_t off_dKh, off_dV, off_dA, off_dF, total;
 };
 
@@ -174,6 +174,7 @@ path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
     p->off_scratch = off;
     off = align_up(off + (simt_scratch > tc_tiles ? simt_scratch : tc_tiles), 256);
     p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * 4, 256);
+    p->off_Dg = off; off = align_up(off + rows * 4, 256);
     // zeroed from here on
     p->off_dQh = off; off = align_up(off + rows * d * 4, 256);
     p->off_dKh = off; off = align_up(off + rows * d * 4, 256);
@@ -696,10 +697,13 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         tb.dout = static_cast<const __nv_bfloat16 *>(dout);
         tb.lse = lse; tb.dlse = dlse;
         tb.dQh = ba.dQh; tb.dKh = ba.dKh; tb.dV = ba.dV; tb.dA = ba.dA;
+        tb.Dg = at<float>(workspace, p.off_Dg);
         tb.scale = desc->scale;
         tb.BH = p.BH; tb.L = p.L; tb.Lp = p.Lp; tb.N = p.N;
         tb.err = error_flag_ptr();
         s = cuda_status(launch_bwd_scan_tc(bm, tb, sms, st), "tensor-core backward scan launch");
+        if (s != PATH_OK) return s;
+        s = cuda_status(launch_bwd_kv_tc(bm, tb, sms, st), "tensor-core backward key-side launch");
         if (s != PATH_OK) return s;
         return run_bwd_prep_tc(desc, p, ba, workspace, st);
     }

@@ -9,23 +9,30 @@
 //   (R) Qt_{b-1} = Qh_b, Qt_{c-1} = Qt_c Pm_c: the forward's right-to-left
 //       chain, recomputed exactly as the forward scan forms it (bf16 rows,
 //       fp32 product, re-rounded per chunk), every Qt_c stored by TMA;
-//   (L) c = 0 .. b-1, with D = dout . out - dlse per row:
+//   (L) c = 0 .. b-1, with D = dout . out - dlse per row (saved for the
+//       key-side kernel):
 //         S  = Qt_c Kh_c^T,  dP = dout V_c^T,  P = 2^(S scale log2e - lse log2e)
-//         dl = scale P (dP - D)                     (bf16 tile; P likewise)
-//         dV_c  += P^T dout,  dKh_c += dl^T Qt_c,  dA_c += Qt_c^T G  (c >= 1)
-//         G     <- G Pm_c^T + dl Kh_c                (G = 0 before c = 0)
-//       and dQh_b = G.  The three sums over query chunks are vector fp32
-//       reductions into HBM (the pages remark that the backward pays for
-//       atomic accumulation; these are where it does).
-// Nine 128 x 128 x 128 MMAs per (b, c) pair: S, dP, dV, dKh, dA, G Pm^T, dl Kh
-// and the chain product of (R).  One thread issues TMA and MMAs; 256 threads
-// run the epilogues (thread = TMEM lane / tile row, half of the columns).
-// Persistent CTAs, query chunks in decreasing order of work.  Every wait is
-// bounded; on timeout the kernel sets the device error flag and stops.
+//         dl = scale P (dP - D)                     (bf16 tile)
+//         dA_c += Qt_c^T G  (c >= 1),  G <- G Pm_c^T + dl Kh_c  (G = 0 before c = 0)
+//       and dQh_b = G.  dA's sum over query chunks is a vector fp32
+//       reduction into HBM (the pages remark that the backward pays for
+//       atomic accumulation; this is where it does).
+// Six 128 x 128 x 128 MMAs per (b, c) pair: S, dP, dA, G Pm^T, dl Kh and the
+// chain product of (R).
 //
-// Shared memory: seven 32 KB bf16 operand tiles (dout_b, Qt, Kh_c, V_c / P,
-// Pm_c, dl, G).  TMEM columns: [0,128) S then dV, [128,256) dP then dKh,
-// [256,384) G, [384,512) the chain product U then dA.
+// bwd_kv_tc_kernel, one key chunk c per job: for every later query chunk b it
+// reloads the stored Qt_c (of that b) and dout_b, recomputes S, dP, P and dl
+// as above, and accumulates dV_c = sum_b P^T dout_b and dKh_c = sum_b dl^T
+// Qt_c in TMEM, written once at the end (four MMAs per pair, no reductions).
+//
+// One thread issues TMA and MMAs; 256 threads run the epilogues (thread =
+// TMEM lane / tile row, half of the columns).  Persistent CTAs, jobs in
+// decreasing order of work.  Every wait is bounded; on timeout a kernel sets
+// the device error flag and stops.
+//
+// Query-side shared memory: seven 32 KB bf16 tiles (dout_b, Qt, Kh_c, V_c /
+// P, Pm_c, dl, G).  TMEM columns: [0,128) S, [128,256) dP, [256,384) G,
+// [384,512) the chain product U then dA.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -170,6 +177,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 }
                 bars.rD[r] = D;
                 bars.rL[r] = l;
+                a.Dg[head_rows + (size_t)b * kC + r] = D;
             }
         }
         // (R) dout_b and Qh_b, then the chain
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                       tc::desc_lo(slot(kVP), false), false);  // dP = dout V^T
             }
             if (!(ok = mma_sync())) break;
-            // P and dl (scaled) as bf16 tiles; V's tile takes P
+            // dl (scaled) as a bf16 tile
             {
                 uint32_t sv[64], pv[64];
                 tc::tmem_ld64(tmem + lane_off + kColS + half * 64, sv);
@@ -257,8 +265,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                         g[e] = a.scale * p[e] * (__uint_as_float(pv[q * 8 + e]) - dr);
                     }
                     const uint32_t off = tc::swz_off(r, half * 8 + q, kC);
-                    tc::sts128(slot(kVP) + off, tc::pack2(p[0], p[1]), tc::pack2(p[2], p[3]),
-                               tc::pack2(p[4], p[5]), tc::pack2(p[6], p[7]));
                     tc::sts128(slot(kDL) + off, tc::pack2(g[0], g[1]), tc::pack2(g[2], g[3]),
                                tc::pack2(g[4], g[5]), tc::pack2(g[6], g[7]));
                 }
@@ -268,11 +274,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             __syncthreads();
             tc::fence_after_sync();
             if (tid == 0) {
-                // dV = P^T dout, dKh = dl^T Qt
-                tc::gemm128_lo2<true, true>(tmem + kColS, tc::desc_lo(slot(kVP), true),
-                                            tc::desc_lo(slot(kDO), true), false);
-                tc::gemm128_lo2<true, true>(tmem + kColDP, tc::desc_lo(slot(kDL), true),
-                                            tc::desc_lo(slot(kQt), true), false);
                 if (c > 0) {
                     // dA = Qt^T G, then G <- G Pm^T
                     tc::gemm128_lo2<true, true>(tmem + kColU, tc::desc_lo(slot(kQt), true),
@@ -287,11 +288,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             if (!(ok = mma_sync())) break;
             {
                 uint32_t v[64];
-                const size_t krow = (head_rows + k0 + r) * kC + half * 64;
-                tc::tmem_ld64(tmem + lane_off + kColS + half * 64, v);
-                red_row(a.dV + krow, v);
-                tc::tmem_ld64(tmem + lane_off + kColDP + half * 64, v);
-                red_row(a.dKh + krow, v);
                 if (c > 0) {
                     tc::tmem_ld64(tmem + lane_off + kColU + half * 64, v);
                     red_row(a.dA + (((size_t)bh * a.N + c) * kC + r) * kC + half * 64, v);
@@ -329,7 +325,181 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
 }
 
+// Key side: dV_c and dKh_c of key chunk c from every later query chunk.
+// Shared memory: six 32 KB tiles (Kh_c, V_c resident; Qt_c of b, dout_b, P,
+// dl per step).  TMEM columns: [0,128) S, [128,256) dP, [256,384) dV,
+// [384,512) dKh.
+enum { kvKh = 0, kvV, kvQt, kvDO, kvP, kvDL, kvSlots };
+constexpr int kSmemKV = (int)sizeof(BBars) + 1023 + kvSlots * kTile;
+static_assert(kSmemKV <= 232448, "shared memory budget exceeded");
+constexpr uint32_t kColDV = 256, kColDK = 384;
+
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_kv_tc_kernel(const __grid_constant__ BwdTcMaps maps, BwdTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    BBars &bars = *reinterpret_cast<BBars *>(smem_raw);
+    uint8_t *tiles = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(BBars) + 1023) &
+        ~static_cast<uintptr_t>(1023));
+    const uint32_t s0 = smem_u32(tiles);
+    auto slot = [&](int s) { return s0 + (uint32_t)(s * kTile); };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int T = (a.N - 1) * a.BH;
+    const float sl2 = a.scale * kLog2e;
+
+    if (tid == 0) {
+        mbar_init(&bars.tma, 1);
+        mbar_init(&bars.mma, 1);
+        bars.ok = 1;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&bars.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars.tmem_base;
+    uint32_t ph_tma = 0, ph_mma = 0;
+    auto mma_sync = [&]() {
+        if (tid == 0) {
+            tc::mma_commit(&bars.mma);
+            if (!mbar_wait(&bars.mma, ph_mma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
+        }
+        ph_mma ^= 1;
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        return bars.ok != 0;
+    };
+    auto tma_sync = [&]() {
+        if (tid == 0) {
+            if (!mbar_wait(&bars.tma, ph_tma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
+            tc::fence_after_sync();
+        }
+        ph_tma ^= 1;
+        __syncthreads();
+        return bars.ok != 0;
+    };
+    auto load_tile = [&](int s, const CUtensorMap *map, int y, int z) {
+        tc::tma_load_3d(tiles + s * kTile, map, 0, y, z, &bars.tma);
+        tc::tma_load_3d(tiles + s * kTile + kTile / 2, map, 64, y, z, &bars.tma);
+    };
+
+    for (int job = blockIdx.x; job < T && bars.ok; job += gridDim.x) {
+        const int c = job / a.BH, bh = job % a.BH;  // c <= N - 2, heaviest first
+        const int k0 = c * kC;
+        const size_t head_rows = (size_t)bh * a.Lp;
+        bool ok = true;
+        for (int b = c + 1; b < a.N; ++b) {
+            const int nq = min(kC, a.L - b * kC);
+            if (half == 0) {
+                const size_t row = head_rows + (size_t)b * kC + r;
+                bars.rD[r] = a.Dg[row];
+                bars.rL[r] = r < nq ? a.lse[(size_t)bh * a.L + (size_t)b * kC + r] * kLog2e : 0.f;
+            }
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bars.tma, (b == c + 1 ? 4 : 2) * kTile);
+                if (b == c + 1) {
+                    load_tile(kvKh, &maps.kh, k0, bh);
+                    load_tile(kvV, &maps.v, k0, bh);
+                }
+                load_tile(kvQt, &maps.qts, (b * (b - 1) / 2 + c) * kC, bh);
+                load_tile(kvDO, &maps.dout, b * kC, bh);
+                if (b + 1 < a.N) {
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        tc::tma_prefetch_3d(&maps.qts, 64 * x, ((b + 1) * b / 2 + c) * kC, bh);
+                        tc::tma_prefetch_3d(&maps.dout, 64 * x, (b + 1) * kC, bh);
+                    }
+                }
+            }
+            if (!(ok = tma_sync())) break;
+            if (tid == 0) {
+                tc::gemm128_lo<false>(tmem + kColS, tc::desc_lo(slot(kvQt), false),
+                                      tc::desc_lo(slot(kvKh), false), false);  // S = Qt Kh^T
+                tc::gemm128_lo<false>(tmem + kColDP, tc::desc_lo(slot(kvDO), false),
+                                      tc::desc_lo(slot(kvV), false), false);   // dP = dout V^T
+            }
+            if (!(ok = mma_sync())) break;
+            {
+                uint32_t sv[64], pv[64];
+                tc::tmem_ld64(tmem + lane_off + kColS + half * 64, sv);
+                tc::tmem_ld64(tmem + lane_off + kColDP + half * 64, pv);
+                const float lr = bars.rL[r], dr = bars.rD[r];
+                const bool live = r < nq;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float p[8], g[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float x = __uint_as_float(sv[q * 8 + e]);
+                        p[e] = live ? ex2(fmaf(x, sl2, -lr)) : 0.f;
+                        g[e] = a.scale * p[e] * (__uint_as_float(pv[q * 8 + e]) - dr);
+                    }
+                    const uint32_t off = tc::swz_off(r, half * 8 + q, kC);
+                    tc::sts128(slot(kvP) + off, tc::pack2(p[0], p[1]), tc::pack2(p[2], p[3]),
+                               tc::pack2(p[4], p[5]), tc::pack2(p[6], p[7]));
+                    tc::sts128(slot(kvDL) + off, tc::pack2(g[0], g[1]), tc::pack2(g[2], g[3]),
+                               tc::pack2(g[4], g[5]), tc::pack2(g[6], g[7]));
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+            if (tid == 0) {
+                // dV += P^T dout, dKh += dl^T Qt
+                tc::gemm128_lo2<true, true>(tmem + kColDV, tc::desc_lo(slot(kvP), true),
+                                            tc::desc_lo(slot(kvDO), true), b > c + 1);
+                tc::gemm128_lo2<true, true>(tmem + kColDK, tc::desc_lo(slot(kvDL), true),
+                                            tc::desc_lo(slot(kvQt), true), b > c + 1);
+            }
+            if (!(ok = mma_sync())) break;
+        }
+        if (!ok) break;
+        {
+            uint32_t v[64];
+            const size_t krow = (head_rows + k0 + r) * kC + half * 64;
+#pragma unroll 1
+            for (int w = 0; w < 2; ++w) {
+                tc::tmem_ld64(tmem + lane_off + (w ? kColDK : kColDV) + half * 64, v);
+                float4 *dst = reinterpret_cast<float4 *>((w ? a.dKh : a.dV) + krow);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_kv_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_sms,
+                             cudaStream_t st) {
+    const int total = (a.N - 1) * a.BH;
+    if (total <= 0) return cudaSuccess;
+    const int grid = total < num_sms ? total : num_sms;
+    cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV);
+    if (e != cudaSuccess) return e;
+    bwd_kv_tc_kernel<<<grid, kThreadsB, kSmemKV, st>>>(maps, a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_scan_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_sms,
                                cudaStream_t st) {

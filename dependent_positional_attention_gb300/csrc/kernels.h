@@ -81,8 +81,9 @@ struct BwdTcMaps {
 struct BwdTcArgs {
     const __nv_bfloat16 *out, *dout;  // [BH][L][128]
     const float *lse, *dlse;          // [BH][L]; dlse may be null
-    float *dQh, *dKh, *dV;            // [BH][Lp][128] fp32 (dKh, dV accumulated)
+    float *dQh, *dKh, *dV;            // [BH][Lp][128] fp32
     float *dA;                        // [BH][N][128][128] fp32 (accumulated)
+    float *Dg;                        // [BH][Lp] dout . out - dlse per query row
     float scale;
     int BH, L, Lp, N;
     uint32_t *err;
@@ -90,6 +91,9 @@ struct BwdTcArgs {
 
 cudaError_t launch_bwd_scan_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_sms,
                                cudaStream_t st);
+// Key side of the tensor-core backward (after launch_bwd_scan_tc): dV, dKh.
+cudaError_t launch_bwd_kv_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_sms,
+                             cudaStream_t st);
 // The CUDA-core backward prep alone (after a tensor-core scan).
 cudaError_t launch_bwd_prep(const BwdArgs &a, bool bf16_io, cudaStream_t st);
 
