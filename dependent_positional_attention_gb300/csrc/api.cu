@@ -319,9 +319,11 @@ path_status_t run_bwd_prep_tc(const path_prefill_desc_t *desc, const BwdPlan &p,
     ChunkGemmArgs base;
     base.BH = p.BH; base.L = p.L; base.Lp = p.Lp; base.N = p.N;
     base.err = error_flag_ptr();
+    const int sms = num_sms();
+    if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
     path_status_t s = ok();
     auto run = [&](GemmBuilder &g, const char *what) {
-        if (s == PATH_OK) s = cuda_status(launch_chunk_gemm_tc(g.maps, g.args, st), what);
+        if (s == PATH_OK) s = cuda_status(launch_chunk_gemm_tc(g.maps, g.args, sms, st), what);
     };
     const float *dQh = ba.dQh, *dKh = ba.dKh;
     {   // G = W Wt (fp32, for the solve and dbeta)

@@ -19,37 +19,51 @@ namespace {
 
 constexpr int kC = 128;
 constexpr int kTile = kC * kC * 2;
-constexpr int kThreadsG = 128;
+constexpr int kStages = 3;      // (A, B) tile pairs in flight
+constexpr int kThreadsG = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 
 struct GBars {
-    uint64_t tma, mma;
+    uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
     uint32_t tmem_base;
-    int ok;
+    int abort_word;
 };
-constexpr int kSmemG = (int)sizeof(GBars) + 1023 + 2 * kTile;
+constexpr int kSmemG = (int)sizeof(GBars) + 1023 + kStages * 2 * kTile;
+static_assert(kSmemG <= 232448, "shared memory budget exceeded");
 
-// D = alpha * sum_p (+/-) op(A_p) op(B_p) (+ E), masked, per chunk.
-__global__ void __launch_bounds__(kThreadsG)
+// D = alpha * sum_p (+/-) op(A_p) op(B_p) (+ E), masked, for every chunk.
+// Persistent and warp-specialised: a three-stage TMA ring of operand pairs,
+// one MMA thread accumulating into two TMEM buffers (128 columns each) so
+// that the epilogue of one chunk overlaps the products of the next, and eight
+// epilogue warps (two per TMEM lane quadrant, thread = chunk row, one half of
+// the columns each).  Staging the rows through shared memory for contiguous
+// global stores was tried and was slower: it left room for only two stages.
+__global__ void __launch_bounds__(kThreadsG, 1)
     chunk_gemm_tc_kernel(const __grid_constant__ ChunkGemmMaps maps, ChunkGemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     GBars &bars = *reinterpret_cast<GBars *>(smem_raw);
     uint8_t *tiles = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(GBars) + 1023) &
         ~static_cast<uintptr_t>(1023));
-    const uint32_t sA = smem_u32(tiles), sB = sA + kTile;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int chunk = blockIdx.x % a.N, bh = blockIdx.x / a.N;
-    const int c0 = chunk * kC;
-    const int n = min(kC, a.L - c0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int jobs = a.N * a.BH;
+    volatile int *abort_word = &bars.abort_word;
+    const uint64_t lim = kWaitLimitNs;
 
     if (tid == 0) {
-        mbar_init(&bars.tma, 1);
-        mbar_init(&bars.mma, 1);
-        bars.ok = 1;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.acc_full[b], 1);
+            mbar_init(&bars.acc_empty[b], 8);
+        }
+        mbar_init(&bars.drain, 1);
+        bars.abort_word = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
-        tc::tmem_alloc(&bars.tmem_base, 128);
+    if (warp == 1) {
+        tc::tmem_alloc(&bars.tmem_base, 256);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -57,86 +71,153 @@ __global__ void __launch_bounds__(kThreadsG)
     tc::fence_after_sync();
     const uint32_t tmem = bars.tmem_base;
 
-    if (tid == 0) {
-        for (int p = 0; p < a.np && bars.ok; ++p) {
-            const ChunkGemmProd &pr = a.prod[p];
-            mbar_arrive_expect_tx(&bars.tma, 2 * kTile);
-            tc::tma_load_3d(tiles, &maps.m[pr.a], 0, c0, bh, &bars.tma);
-            tc::tma_load_3d(tiles + kTile / 2, &maps.m[pr.a], 64, c0, bh, &bars.tma);
-            tc::tma_load_3d(tiles + kTile, &maps.m[pr.b], 0, c0, bh, &bars.tma);
-            tc::tma_load_3d(tiles + kTile + kTile / 2, &maps.m[pr.b], 64, c0, bh, &bars.tma);
-            if (!mbar_wait(&bars.tma, p & 1, a.err, nullptr, kWaitLimitNs)) {
-                bars.ok = 0;
-                break;
-            }
-            tc::fence_after_sync();
-            // A: op = X (K-major) or X^T (MN-major).  B: op = X is MN-major
-            // (rows of X along K), X^T is K-major.
-            const bool a_mn = pr.at, b_mn = !pr.bt;
-            const uint32_t idesc = tc::idesc_bf16(128, 128, a_mn, b_mn) | (pr.neg ? (1u << 13) : 0u);
-            const uint32_t a_lo = tc::desc_lo(sA, a_mn), b_lo = tc::desc_lo(sB, b_mn);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2);
-                tc::mma_bf16_lohi(tmem, a_lo + (a_mn ? (uint32_t)(kk * 128) : koff),
-                                  b_lo + (b_mn ? (uint32_t)(kk * 128) : koff), idesc,
-                                  (p > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc::mma_commit(&bars.mma);
-            // the tiles are reloaded for the next product only after this one read them
-            if (!mbar_wait(&bars.mma, p & 1, a.err, nullptr, kWaitLimitNs)) {
-                bars.ok = 0;
-                break;
-            }
-        }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (bars.ok) {
-        const int r = tid;
-        const size_t ws_row = ((size_t)bh * a.Lp + c0 + r) * kC;
-        const size_t io_row = ((size_t)bh * a.L + c0 + r) * kC;
-        const bool live = r < n;
-        const float rs = (a.rowscale && live) ? a.rowscale[(size_t)bh * a.L + c0 + r] : 0.f;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t v[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc * 32, v);
-            float x[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int j = cc * 32 + e;
-                float y = a.alpha * __uint_as_float(v[e]);
-                if (a.E) y += a.E[ws_row + j];
-                const bool keep = live && (a.mask == 0 || (a.mask == 1 && j <= r) ||
-                                           (a.mask == 2 && j > r) || (a.mask == 3 && j < r));
-                x[e] = keep ? y : 0.f;
-            }
-            if (a.out_f32) {
-                float4 *dst = reinterpret_cast<float4 *>(a.out_f32 + ws_row + cc * 32);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-            }
-            if (a.out_bf16 && (!a.out_final || live)) {
-                const float s = a.rowscale ? rs : 1.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(a.out_bf16 + (a.out_final ? io_row : ws_row) +
-                                                       cc * 32);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(tc::pack2(s * x[8 * q], s * x[8 * q + 1]),
-                                        tc::pack2(s * x[8 * q + 2], s * x[8 * q + 3]),
-                                        tc::pack2(s * x[8 * q + 4], s * x[8 * q + 5]),
-                                        tc::pack2(s * x[8 * q + 6], s * x[8 * q + 7]));
-            }
-        }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
     if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int par[kStages];
+            for (int i = 0; i < kStages; ++i) par[i] = -1;
+            bool ok = true;
+            for (int job = blockIdx.x; job < jobs && ok; job += gridDim.x) {
+                const int c0 = (job % a.N) * kC, bh = job / a.N;
+                for (int p = 0; p < a.np; ++p) {
+                    if (!mbar_wait(&bars.empty[s], ph ^ 1, a.err, abort_word, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const ChunkGemmProd &pr = a.prod[p];
+                    uint8_t *dst = tiles + s * 2 * kTile;
+                    mbar_arrive_expect_tx(&bars.full[s], 2 * kTile);
+                    tc::tma_load_3d(dst, &maps.m[pr.a], 0, c0, bh, &bars.full[s]);
+                    tc::tma_load_3d(dst + kTile / 2, &maps.m[pr.a], 64, c0, bh, &bars.full[s]);
+                    tc::tma_load_3d(dst + kTile, &maps.m[pr.b], 0, c0, bh, &bars.full[s]);
+                    tc::tma_load_3d(dst + kTile + kTile / 2, &maps.m[pr.b], 64, c0, bh,
+                                    &bars.full[s]);
+                    par[s] = (int)ph;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok)  // let the copies in flight land before the CTA's memory goes away
+                for (int i = 0; i < kStages; ++i)
+                    if (par[i] >= 0) mbar_wait(&bars.full[i], (uint32_t)par[i], nullptr, nullptr, lim);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int s = 0, it = 0;
+            uint32_t ph = 0, ae_ph[2] = {0, 0};
+            bool ok = true, issued = false;
+            for (int job = blockIdx.x; job < jobs && ok; job += gridDim.x, ++it) {
+                const int buf = it & 1;
+                if (!mbar_wait(&bars.acc_empty[buf], ae_ph[buf] ^ 1, a.err, abort_word, lim)) {
+                    ok = false;
+                    break;
+                }
+                ae_ph[buf] ^= 1;
+                tc::fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(buf * 128);
+                for (int p = 0; p < a.np; ++p) {
+                    if (!mbar_wait(&bars.full[s], ph, a.err, abort_word, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const ChunkGemmProd &pr = a.prod[p];
+                    // A: op = X (K-major) or X^T (MN-major).  B: op = X is
+                    // MN-major (rows of X along K), X^T is K-major.
+                    const bool a_mn = pr.at, b_mn = !pr.bt;
+                    const uint32_t idesc =
+                        tc::idesc_bf16(128, 128, a_mn, b_mn) | (pr.neg ? (1u << 13) : 0u);
+                    const uint32_t sA = smem_u32(tiles + s * 2 * kTile), sB = sA + kTile;
+                    const uint32_t a_lo = tc::desc_lo(sA, a_mn), b_lo = tc::desc_lo(sB, b_mn);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2);
+                        tc::mma_bf16_lohi(d, a_lo + (a_mn ? (uint32_t)(kk * 128) : koff),
+                                          b_lo + (b_mn ? (uint32_t)(kk * 128) : koff), idesc,
+                                          (p > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc::mma_commit(&bars.empty[s]);  // frees the stage once read
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc::mma_commit(&bars.acc_full[buf]);
+            }
+            if (!ok && issued) {  // every issued MMA completes before TMEM is freed
+                tc::mma_commit(&bars.drain);
+                mbar_wait(&bars.drain, 0, nullptr, nullptr, lim);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3, hcol = (warp - 2) >> 2;
+        const int r = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        uint32_t af_ph[2] = {0, 0};
+        int it = 0;
+        for (int job = blockIdx.x; job < jobs; job += gridDim.x, ++it) {
+            const int buf = it & 1;
+            bool ok = mbar_wait(&bars.acc_full[buf], af_ph[buf], a.err, abort_word, lim);
+            af_ph[buf] ^= 1;
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc::fence_after_sync();
+            const int chunk = job % a.N, bh = job / a.N;
+            const int c0 = chunk * kC;
+            const int n = min(kC, a.L - c0);
+            const size_t ws_row = ((size_t)bh * a.Lp + c0 + r) * kC;
+            const size_t io_row = ((size_t)bh * a.L + c0 + r) * kC;
+            const bool live = r < n;
+            const float rs = (a.rowscale && live) ? a.rowscale[(size_t)bh * a.L + c0 + r] : 0.f;
+#pragma unroll 1
+            for (int cc = 2 * hcol; cc < 2 * hcol + 2; ++cc) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + lane_off + (uint32_t)(buf * 128 + cc * 32), v);
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = cc * 32 + e;
+                    float y = a.alpha * __uint_as_float(v[e]);
+                    if (a.E) y += a.E[ws_row + j];
+                    const bool keep = live && (a.mask == 0 || (a.mask == 1 && j <= r) ||
+                                               (a.mask == 2 && j > r) || (a.mask == 3 && j < r));
+                    x[e] = keep ? y : 0.f;
+                }
+                if (a.out_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.out_f32 + ws_row + cc * 32);
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4)
+                        dst[k4] = make_float4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+                }
+                if (a.out_bf16 && (!a.out_final || live)) {
+                    const float sc = a.rowscale ? rs : 1.f;
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        a.out_bf16 + (a.out_final ? io_row : ws_row) + cc * 32);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        dst[k4] = make_uint4(tc::pack2(sc * x[8 * k4], sc * x[8 * k4 + 1]),
+                                             tc::pack2(sc * x[8 * k4 + 2], sc * x[8 * k4 + 3]),
+                                             tc::pack2(sc * x[8 * k4 + 4], sc * x[8 * k4 + 5]),
+                                             tc::pack2(sc * x[8 * k4 + 6], sc * x[8 * k4 + 7]));
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.acc_empty[buf]);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, 128);
+        tc::tmem_dealloc(tmem, 256);
     }
 }
 
@@ -224,7 +305,7 @@ __global__ void bwd_dbeta_kernel(const float *dX, const float *dLo, const float 
 }  // namespace
 
 cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs &a,
-                                 cudaStream_t st) {
+                                 int num_sms, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(chunk_gemm_tc_kernel,
@@ -232,7 +313,8 @@ cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs 
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    chunk_gemm_tc_kernel<<<a.N * a.BH, kThreadsG, kSmemG, st>>>(maps, a);
+    const int jobs = a.N * a.BH;
+    chunk_gemm_tc_kernel<<<jobs < num_sms ? jobs : num_sms, kThreadsG, kSmemG, st>>>(maps, a);
     return cudaGetLastError();
 }
 

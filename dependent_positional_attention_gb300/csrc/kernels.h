@@ -122,7 +122,7 @@ struct ChunkGemmArgs {
     uint32_t *err;
 };
 cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs &a,
-                                 cudaStream_t st);
+                                 int num_sms, cudaStream_t st);
 
 struct BwdDiagArgs {
     const __nv_bfloat16 *out, *dout;
