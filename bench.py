@@ -473,6 +473,9 @@ def main():
     ap.add_argument("--skip-extra", action="store_true",
                     help="headline workload only (no FoX / long / decode objects)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the prefill backward on the headline shape and print its "
+                         "object (for profiler captures; not the bench line)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the headline workload's batch (smaller cases for "
                          "profiler captures; the default is the headline B8)")
@@ -525,6 +528,13 @@ def main():
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
 
+    if args.backward_only:
+        res = backward_block(head, steps, warmup, ws, peaks)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
     sampler = ClockSampler() if rank == 0 else None
     main_res, clocks = prefill_block(head, steps, warmup, ws, peaks, sampler=sampler)
     e2e = e2e_prefill(head, max(3, steps // 2), 2, ws)
