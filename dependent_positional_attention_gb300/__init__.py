@@ -15,6 +15,7 @@ import threading
 __all__ = [
     "PathAttnError", "load_library", "path_attn_prefill_fwd", "path_attn_prefill_prep",
     "path_attn_prefill_scan", "path_attn_prefill_bwd", "path_attn_prefill_bwd_workspace_size",
+    "path_attention",
     "path_attn_decode_step", "path_attn_decode_step_fox",
     "path_attn_fox_prefix",
     "path_attn_build_kcache", "path_attn_prefill_workspace_size",
@@ -269,6 +270,50 @@ def path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, log_f=None, dlse=Non
         _ptr(g["dv"]), _ptr(g["dw"]), _ptr(g["dbeta"]), _ptr(g.get("dlog_f")),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return g
+
+
+def path_attention(q, k, v, w, beta, log_f=None, scale=None):
+    """Differentiable PaTH / PaTH-FoX prefill for torch autograd: forward by
+    path_attn_prefill_fwd, backward by path_attn_prefill_bwd (both in the
+    library).  Returns out; gradients flow to q, k, v, w, beta and log_f."""
+    return _PathAttentionFn.apply(q, k, v, w, beta, log_f, scale)
+
+
+def _autograd_fn():
+    import torch
+
+    class PathAttentionFn(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, w, beta, log_f, scale):
+            q, k, v, w, beta = (t.contiguous() for t in (q, k, v, w, beta))
+            log_f = log_f.contiguous() if log_f is not None else None
+            out, lse = path_attn_prefill_fwd(q, k, v, w, beta, log_f=log_f, scale=scale)
+            ctx.save_for_backward(q, k, v, w, beta, out, lse,
+                                  log_f if log_f is not None else torch.empty(0))
+            ctx.fox = log_f is not None
+            ctx.scale = scale
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, w, beta, out, lse, log_f = ctx.saved_tensors
+            g = path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout.contiguous(),
+                                      log_f=log_f if ctx.fox else None, scale=ctx.scale)
+            return (g["dq"], g["dk"], g["dv"], g["dw"], g["dbeta"], g.get("dlog_f"), None)
+
+    return PathAttentionFn
+
+
+class _LazyFn:
+    _fn = None
+
+    def apply(self, *args):
+        if _LazyFn._fn is None:
+            _LazyFn._fn = _autograd_fn()
+        return _LazyFn._fn.apply(*args)
+
+
+_PathAttentionFn = _LazyFn()
 
 
 def path_attn_decode_workspace_size(desc: DecodeDesc) -> int:

@@ -362,9 +362,8 @@ path_status_t run_bwd_prep_tc(const path_prefill_desc_t *desc, const BwdPlan &p,
     }
     if (s != PATH_OK) return s;
     BwdDiagArgs da;
-    da.out = static_cast<const __nv_bfloat16 *>(ba.out);
-    da.dout = static_cast<const __nv_bfloat16 *>(ba.dout);
-    da.lse = ba.lse; da.dlse = ba.dlse; da.Sd = ft[Sd_]; da.dP = ft[dP_];
+    da.Dg = at<float>(workspace, p.off_Dg);
+    da.lse = ba.lse; da.Sd = ft[Sd_]; da.dP = ft[dP_];
     da.P = bt[P_]; da.dSd = bt[dSd_]; da.scale = desc->scale;
     da.BH = p.BH; da.L = p.L; da.Lp = p.Lp; da.N = p.N;
     s = cuda_status(launch_bwd_diag(da, st), "diagonal block");
@@ -703,6 +702,10 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         tb.scale = desc->scale;
         tb.BH = p.BH; tb.L = p.L; tb.Lp = p.Lp; tb.N = p.N;
         tb.err = error_flag_ptr();
+        s = cuda_status(launch_bwd_rowdot(tb.out, tb.dout, dlse, at<float>(workspace, p.off_Dg),
+                                          p.BH, p.L, p.Lp, st),
+                        "row dot launch");
+        if (s != PATH_OK) return s;
         s = cuda_status(launch_bwd_scan_tc(bm, tb, sms, st), "tensor-core backward scan launch");
         if (s != PATH_OK) return s;
         s = cuda_status(launch_bwd_kv_tc(bm, tb, sms, st), "tensor-core backward key-side launch");

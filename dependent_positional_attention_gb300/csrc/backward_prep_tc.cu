@@ -251,24 +251,40 @@ __global__ void __launch_bounds__(utc::kThr) bwd_solve_kernel(const float *G, co
     }
 }
 
+// D = dout . out - dlse for every row of the padded layout [BH][Lp] (0 on the
+// padding), one warp per row.
+__global__ void bwd_rowdot_kernel(const __nv_bfloat16 *out, const __nv_bfloat16 *dout,
+                                  const float *dlse, float *Dg, int BH, int L, int Lp) {
+    const size_t row = (size_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= (size_t)BH * Lp) return;
+    const int bh = (int)(row / Lp), i = (int)(row % Lp);
+    float s = 0.f;
+    if (i < L) {
+        const size_t off = ((size_t)bh * L + i) * kC + 4 * lane;
+        const uint2 x = *reinterpret_cast<const uint2 *>(out + off);
+        const uint2 y = *reinterpret_cast<const uint2 *>(dout + off);
+        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.x));
+        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x.y));
+        const float2 y0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&y.x));
+        const float2 y1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&y.y));
+        s = x0.x * y0.x + x0.y * y0.y + x1.x * y1.x + x1.y * y1.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) Dg[row] = (i < L) ? s - (dlse ? dlse[(size_t)bh * L + i] : 0.f) : 0.f;
+}
+
 // The chunk's own block: P = exp(scale Sd - lse) (j <= i), dSd = scale P (dP -
-// dout . out + dlse), as bf16 tiles.  One block per chunk.
+// D), as bf16 tiles.  One block per chunk.
 __global__ void __launch_bounds__(kThreads) bwd_diag_kernel(BwdDiagArgs a) {
     __shared__ float rD[kC], rL[kC];
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int c0 = chunk * kC, n = min(kC, a.L - c0);
     const size_t base = ((size_t)bh * a.Lp + c0) * kC;
     for (int r = threadIdx.x; r < kC; r += kThreads) {
-        float D = 0.f, l = 0.f;
-        if (r < n) {
-            const size_t row = (size_t)bh * a.L + c0 + r;
-            const __nv_bfloat16 *o = a.out + row * kC, *g = a.dout + row * kC;
-            for (int m = 0; m < kC; ++m) D = fmaf(__bfloat162float(o[m]), __bfloat162float(g[m]), D);
-            if (a.dlse) D -= a.dlse[row];
-            l = a.lse[row];
-        }
-        rD[r] = D;
-        rL[r] = l;
+        rD[r] = a.Dg[(size_t)bh * a.Lp + c0 + r];
+        rL[r] = r < n ? a.lse[(size_t)bh * a.L + c0 + r] : 0.f;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
@@ -325,6 +341,14 @@ cudaError_t launch_bwd_solve(const float *G, const float *beta, __nv_bfloat16 *T
         cudaFuncSetAttribute(bwd_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     bwd_solve_kernel<<<dim3(N, BH), utc::kThr, sm, st>>>(G, beta, T, Ti, L, Lp, N);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_rowdot(const __nv_bfloat16 *out, const __nv_bfloat16 *dout,
+                              const float *dlse, float *Dg, int BH, int L, int Lp,
+                              cudaStream_t st) {
+    const size_t rows = (size_t)BH * Lp;
+    bwd_rowdot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, dout, dlse, Dg, BH, L, Lp);
     return cudaGetLastError();
 }
 

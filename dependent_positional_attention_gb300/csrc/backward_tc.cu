@@ -9,8 +9,7 @@
 //   (R) Qt_{b-1} = Qh_b, Qt_{c-1} = Qt_c Pm_c: the forward's right-to-left
 //       chain, recomputed exactly as the forward scan forms it (bf16 rows,
 //       fp32 product, re-rounded per chunk), every Qt_c stored by TMA;
-//   (L) c = 0 .. b-1, with D = dout . out - dlse per row (saved for the
-//       key-side kernel):
+//   (L) c = 0 .. b-1, with D = dout . out - dlse per row (bwd_rowdot_kernel):
 //         S  = Qt_c Kh_c^T,  dP = dout V_c^T,  P = 2^(S scale log2e - lse log2e)
 //         dl = scale P (dP - D)                     (bf16 tile)
 //         dA_c += Qt_c^T G  (c >= 1),  G <- G Pm_c^T + dl Kh_c  (G = 0 before c = 0)
@@ -146,39 +145,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const int pair0 = b * (b - 1) / 2;  // first (b, c) pair of this chunk in the head
         const size_t head_rows = (size_t)bh * a.Lp;
 
-        // row constants; partial dot products in the (idle) dl tile
-        {
-            float s = 0.f;
-            if (r < nq) {
-                const size_t off = ((size_t)bh * a.L + (size_t)b * kC + r) * kC + half * 64;
-                const uint4 *po = reinterpret_cast<const uint4 *>(a.out + off);
-                const uint4 *pd = reinterpret_cast<const uint4 *>(a.dout + off);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 x = po[i], y = pd[i];
-                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xs[e]));
-                        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ys[e]));
-                        s = fmaf(fx.x, fy.x, fmaf(fx.y, fy.y, s));
-                    }
-                }
-            }
-            float *part = reinterpret_cast<float *>(tiles + kDL * kTile);
-            part[half * kC + r] = s;
-            __syncthreads();
-            if (half == 0) {
-                float D = 0.f, l = 0.f;
-                if (r < nq) {
-                    const size_t row = (size_t)bh * a.L + (size_t)b * kC + r;
-                    D = part[r] + part[kC + r] - (a.dlse ? a.dlse[row] : 0.f);
-                    l = a.lse[row] * kLog2e;
-                }
-                bars.rD[r] = D;
-                bars.rL[r] = l;
-                a.Dg[head_rows + (size_t)b * kC + r] = D;
-            }
+        // row constants (D from bwd_rowdot_kernel)
+        if (half == 0) {
+            bars.rD[r] = a.Dg[head_rows + (size_t)b * kC + r];
+            bars.rL[r] = r < nq ? a.lse[(size_t)bh * a.L + (size_t)b * kC + r] * kLog2e : 0.f;
         }
         // (R) dout_b and Qh_b, then the chain
         if (tid == 0) {
@@ -221,25 +191,28 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         __syncthreads();
 
         // (L)
-        for (int c = 0; c < b; ++c) {
+        // the loads of step c are issued as soon as step c-1's MMAs are done,
+        // so that they overlap its epilogue
+        auto issue_loads = [&](int c) {
             const int k0 = c * kC;
-            if (tid == 0) {
-                // Qt_0 is still in its tile from the end of (R)
-                mbar_arrive_expect_tx(&bars.tma, (c > 0 ? 4 : 2) * kTile);
-                if (c > 0) load_tile(kQt, &maps.qts, (pair0 + c) * kC, bh);
-                load_tile(kKh, &maps.kh, k0, bh);
-                load_tile(kVP, &maps.v, k0, bh);
-                if (c > 0) load_tile(kPm, &maps.pm, k0, bh);
-                if (c + 1 < b) {
+            // Qt_0 is still in its tile from the end of (R)
+            mbar_arrive_expect_tx(&bars.tma, (c > 0 ? 4 : 2) * kTile);
+            if (c > 0) load_tile(kQt, &maps.qts, (pair0 + c) * kC, bh);
+            load_tile(kKh, &maps.kh, k0, bh);
+            load_tile(kVP, &maps.v, k0, bh);
+            if (c > 0) load_tile(kPm, &maps.pm, k0, bh);
+            if (c + 1 < b) {
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        tc::tma_prefetch_3d(&maps.qts, 64 * x, (pair0 + c + 1) * kC, bh);
-                        tc::tma_prefetch_3d(&maps.kh, 64 * x, k0 + kC, bh);
-                        tc::tma_prefetch_3d(&maps.v, 64 * x, k0 + kC, bh);
-                        tc::tma_prefetch_3d(&maps.pm, 64 * x, k0 + kC, bh);
-                    }
+                for (int x = 0; x < 2; ++x) {
+                    tc::tma_prefetch_3d(&maps.qts, 64 * x, (pair0 + c + 1) * kC, bh);
+                    tc::tma_prefetch_3d(&maps.kh, 64 * x, k0 + kC, bh);
+                    tc::tma_prefetch_3d(&maps.v, 64 * x, k0 + kC, bh);
+                    tc::tma_prefetch_3d(&maps.pm, 64 * x, k0 + kC, bh);
                 }
             }
+        };
+        if (tid == 0) issue_loads(0);
+        for (int c = 0; c < b; ++c) {
             if (!(ok = tma_sync())) break;
             if (tid == 0) {
                 tc::gemm128_lo<false>(tmem + kColS, tc::desc_lo(slot(kQt), false),
@@ -286,6 +259,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                      tc::desc_lo(slot(kKh), true), c > 0);
             }
             if (!(ok = mma_sync())) break;
+            if (tid == 0 && c + 1 < b) issue_loads(c + 1);  // every reader of the tiles is done
             {
                 uint32_t v[64];
                 if (c > 0) {

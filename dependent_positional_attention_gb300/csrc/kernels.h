@@ -83,7 +83,7 @@ struct BwdTcArgs {
     const float *lse, *dlse;          // [BH][L]; dlse may be null
     float *dQh, *dKh, *dV;            // [BH][Lp][128] fp32
     float *dA;                        // [BH][N][128][128] fp32 (accumulated)
-    float *Dg;                        // [BH][Lp] dout . out - dlse per query row
+    const float *Dg;                  // [BH][Lp] dout . out - dlse per query row
     float scale;
     int BH, L, Lp, N;
     uint32_t *err;
@@ -125,8 +125,8 @@ cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs 
                                  int num_sms, cudaStream_t st);
 
 struct BwdDiagArgs {
-    const __nv_bfloat16 *out, *dout;
-    const float *lse, *dlse, *Sd, *dP;
+    const float *Dg;  // [BH][Lp] dout . out - dlse (bwd_rowdot)
+    const float *lse, *Sd, *dP;
     __nv_bfloat16 *P, *dSd;
     float scale;
     int BH, L, Lp, N;
@@ -134,6 +134,9 @@ struct BwdDiagArgs {
 cudaError_t launch_bwd_solve(const float *G, const float *beta, __nv_bfloat16 *T,
                              __nv_bfloat16 *Ti, int BH, int L, int Lp, int N, cudaStream_t st);
 cudaError_t launch_bwd_diag(const BwdDiagArgs &a, cudaStream_t st);
+cudaError_t launch_bwd_rowdot(const __nv_bfloat16 *out, const __nv_bfloat16 *dout,
+                              const float *dlse, float *Dg, int BH, int L, int Lp,
+                              cudaStream_t st);
 cudaError_t launch_bwd_cvt(const float *x, __nv_bfloat16 *y, size_t n, cudaStream_t st);
 cudaError_t launch_bwd_dbeta(const float *dX, const float *dLo, const float *G, float *dbeta,
                              int BH, int L, int Lp, int N, cudaStream_t st);

@@ -120,3 +120,19 @@ def test_bf16_d128_cuda_core_route():
     """chunk 64 keeps bf16 head_dim 128 on the CUDA-core scan."""
     got, ref = run(wl.prefill_inputs(1, 2, 300, 128, "bf16", seed=12), chunk=64)
     check(got, ref, 2e-2)
+
+
+def test_autograd_function_matches_the_oracle():
+    """path_attention under torch autograd: loss.backward() runs the library's
+    backward; the gradients (FoX included) match the oracle's."""
+    x = wl.prefill_inputs(1, 2, 200, 64, "f32", seed=21, fox=True)
+    dev = torch.device("cuda:0")
+    t = {n: a.to(dev).requires_grad_(True) for n, a in x.items()}
+    out = pa.path_attention(t["q"], t["k"], t["v"], t["w"], t["beta"], log_f=t["log_f"])
+    dout = torch.randn(out.shape, generator=torch.Generator().manual_seed(3)).to(dev)
+    (out * dout).sum().backward()
+    torch.cuda.synchronize()
+    ref = oracle.prefill_bwd(*(to64(x[n]) for n in ("q", "k", "v", "w", "beta")), to64(dout),
+                             log_f=to64(x["log_f"]))
+    got = {"d" + n: to64(t[n].grad) for n in ("q", "k", "v", "w", "beta", "log_f")}
+    check(got, ref, 1e-4)
