@@ -391,7 +391,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             tc::tmem_wait_st();
             float m = lsd * kLog2e, l = 1.f;
             for (int c = b - 1; c >= 0; --c) {
-                if (fox) bars.fsm[r] = Frow[c * kC + r] * kLog2e;
+                // FoX: the bias fi - F_j splits into a row term (fi - F_ref) and
+                // a column term F_j - F_ref, F_ref the chunk's first prefix
+                float dlt = 0.f;
+                if (fox) {
+                    const float fref = Frow[c * kC];
+                    bars.fsm[r] = (Frow[c * kC + r] - fref) * kLog2e;
+                    dlt = fi - fref * kLog2e;
+                }
                 ok = group_all(2, 128, mbar_wait(&bars.s_full, sf_ph, a.err, abort_word, lim));
                 if (!ok) break;
                 sf_ph ^= 1;
@@ -406,10 +413,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (kFox) {
 #pragma unroll
                     for (int j = 0; j < kC; ++j) {
-                        const float t = fmaf(__uint_as_float(v[j]), sl2, fi - bars.fsm[j]);
+                        const float t = fmaf(__uint_as_float(v[j]), sl2, -bars.fsm[j]);
                         v[j] = __float_as_uint(t);
                         mx = fmaxf(mx, t);
                     }
+                    mx += dlt;
                 } else {
                     // max of the scaled logits from the raw extreme (min if scale < 0)
                     if (sl2 >= 0.f) {
@@ -430,7 +438,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 const float mnew = rescale ? fmaxf(m, mx) : m;
                 const float alpha = rescale ? exp2f(m - mnew) : 1.f;
                 // probabilities, packed to bf16 pairs (the logits die as they go)
-                const float xs = kFox ? 1.f : sl2;  // FoX rows already hold scaled logits
+                // FoX rows already hold the scaled logits less the row term
+                const float xs = kFox ? 1.f : sl2;
+                const float off = kFox ? dlt - mnew : -mnew;
                 float sum0 = 0.f, sum1 = 0.f;
                 uint32_t pk[kC / 2];
 #pragma unroll
@@ -438,7 +448,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     float p[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        p[e] = ex2(fmaf(__uint_as_float(v[4 * j4 + e]), xs, -mnew));
+                        p[e] = kFox ? ex2(__uint_as_float(v[4 * j4 + e]) + off)
+                                    : ex2(fmaf(__uint_as_float(v[4 * j4 + e]), xs, off));
                     sum0 += p[0] + p[1];
                     sum1 += p[2] + p[3];
                     pk[2 * j4] = pack_bf16(p[0], p[1]);
