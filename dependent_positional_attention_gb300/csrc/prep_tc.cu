@@ -20,9 +20,10 @@
 // Persistent CTAs, one chunk at a time.
 //
 // Phases per chunk (one thread issues TMA and MMAs; waits are bounded):
-//   P1 TMA W, then Q and K; MMA G -> cols 0 alone (so the solve can start),
-//      then QW -> 128, KW -> 256, QK -> 384; the next chunk's boxes are
-//      prefetched into L2
+//   P1 MMA G -> cols 0 alone (so the solve can start), then QW -> 128,
+//      KW -> 256, QK -> 384, as the chunk's W, then Q and K land (their TMA
+//      loads were issued during the previous chunk's P10); the next chunk's
+//      boxes are prefetched into L2
 //   P2 G -> fp32 smem (swizzled)
 //   P3 solve T (fp32 smem)
 //   P4 T -> bf16 tile, -(M_le*QW) -> bf16 tile, (M_gt*KW) -> bf16 tile
@@ -155,24 +156,32 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         return bars.ok != 0;
     };
 
+    // W, Q and K of a chunk: issued for the first chunk here, and for each
+    // following chunk as soon as the current one's output stores have read
+    // the tiles (during P9), so that the loads overlap P9-P10
+    auto issue_loads = [&](int job) {
+        const int bh = job / a.N, c0 = (job % a.N) * kC;
+        tc::bulk_wait_read();
+        mbar_arrive_expect_tx(&bars.tma, kTile);
+        tc::tma_load_3d(smem + kOffW, &maps.w, 0, c0, bh, &bars.tma);
+        tc::tma_load_3d(smem + kOffW + kTile / 2, &maps.w, 64, c0, bh, &bars.tma);
+        mbar_arrive_expect_tx(&bars.tma2, 2 * kTile);
+        tc::tma_load_3d(smem + kOffQ, &maps.q, 0, c0, bh, &bars.tma2);
+        tc::tma_load_3d(smem + kOffQ + kTile / 2, &maps.q, 64, c0, bh, &bars.tma2);
+        tc::tma_load_3d(smem + kOffK, &maps.k, 0, c0, bh, &bars.tma2);
+        tc::tma_load_3d(smem + kOffK + kTile / 2, &maps.k, 64, c0, bh, &bars.tma2);
+    };
+    if (tid == 0 && blockIdx.x < total) issue_loads(blockIdx.x);
     for (int job = blockIdx.x; job < total; job += gridDim.x) {
         const int bh = job / a.N, chunk = job % a.N;
         const int c0 = chunk * kC;
         const int n = min(kC, a.L - c0);
+        // beta of the chunk, read ahead of its use in P2
+        const float beta_r = (tid < kC && tid < n) ? a.beta[(size_t)bh * a.L + c0 + tid] : 0.f;
         // ---------------------------------------------------------------- P1
         // W first: G = W W^T alone lets the solve for T start while the
         // other three products run
         if (tid == 0) {
-            // the previous chunk's output stores have read the tiles reloaded here
-            tc::bulk_wait_read();
-            mbar_arrive_expect_tx(&bars.tma, kTile);
-            tc::tma_load_3d(smem + kOffW, &maps.w, 0, c0, bh, &bars.tma);
-            tc::tma_load_3d(smem + kOffW + kTile / 2, &maps.w, 64, c0, bh, &bars.tma);
-            mbar_arrive_expect_tx(&bars.tma2, 2 * kTile);
-            tc::tma_load_3d(smem + kOffQ, &maps.q, 0, c0, bh, &bars.tma2);
-            tc::tma_load_3d(smem + kOffQ + kTile / 2, &maps.q, 64, c0, bh, &bars.tma2);
-            tc::tma_load_3d(smem + kOffK, &maps.k, 0, c0, bh, &bars.tma2);
-            tc::tma_load_3d(smem + kOffK + kTile / 2, &maps.k, 64, c0, bh, &bars.tma2);
             const int next = job + gridDim.x;
             if (next < total) {
                 const int nbh = next / a.N, nc0 = (next % a.N) * kC;
@@ -208,7 +217,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         tc::fence_after_sync();
         if (!bars.ok) break;
         // ---------------------------------------------------------------- P2
-        if (tid < kC) bsm[tid] = (tid < n) ? a.beta[(size_t)bh * a.L + c0 + tid] : 0.f;
+        if (tid < kC) bsm[tid] = beta_r;
         {
             uint32_t v[32];
 #pragma unroll
@@ -409,6 +418,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 bars.ok = 0;
             } else {
                 tc::gemm_128x128x128(tmem + kColC, sQm, sT, true, false);  // P V
+                // the next chunk's W, Q, K: the P8 stores have long been issued
+                if (job + (int)gridDim.x < total) issue_loads(job + gridDim.x);
             }
         }
         ph_v ^= 1;
