@@ -20,10 +20,11 @@
 // Persistent CTAs, one chunk at a time.
 //
 // Phases per chunk (one thread issues TMA and MMAs; waits are bounded):
-//   P1 MMA G -> cols 0 alone (so the solve can start), then QW -> 128,
-//      KW -> 256, QK -> 384, as the chunk's W, then Q and K land (their TMA
-//      loads were issued during the previous chunk's P10); the next chunk's
-//      boxes are prefetched into L2
+//   P1 MMA G -> cols 0 alone, as soon as the chunk's W lands (its TMA load,
+//      and Q's and K's, were issued during the previous chunk's P10); the
+//      next chunk's boxes are prefetched into L2
+//   P3 (start) MMA QW -> 128, KW -> 256, QK -> 384, issued by a thread the
+//      diagonal-block solve leaves idle
 //   P2 G -> fp32 smem (swizzled)
 //   P3 solve T (fp32 smem)
 //   P4 T -> bf16 tile, -(M_le*QW) -> bf16 tile, (M_gt*KW) -> bf16 tile
@@ -199,18 +200,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 tc::fence_after_sync();
                 tc::gemm_128x128x128(tmem + kColA, sW, sW, false, false);  // G
                 tc::mma_commit(&bars.mma);
-                if (!mbar_wait(&bars.tma2, ph_tma, a.err, nullptr, kWaitLimitNs)) {
-                    bars.ok = 0;
-                } else {
-                    tc::fence_after_sync();
-                    tc::gemm_128x128x128(tmem + kColB, sQ, sW, false, false);  // Q W^T
-                    tc::gemm_128x128x128(tmem + kColC, sK, sW, false, false);  // K W^T
-                    tc::gemm_128x128x128(tmem + kColD, sQ, sK, false, false);  // Q K^T
-                    tc::mma_commit(&bars.mma2);
-                }
                 if (!mbar_wait(&bars.mma, ph_mma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
             }
         }
+        // Q W^T, K W^T, Q K^T are issued at the start of P3 by a thread that
+        // the diagonal-block solve leaves idle, so that this thread is not held
+        // on the MMA queue before it can release the block into the solve
+        const uint32_t ph_q = ph_tma;
         ph_tma ^= 1;
         ph_mma ^= 1;
         __syncthreads();
@@ -233,10 +229,22 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         __syncthreads();
         // ---------------------------------------------------------------- P3
+        if (tid == 128) {
+            if (!mbar_wait(&bars.tma2, ph_q, a.err, nullptr, kWaitLimitNs)) {
+                bars.ok = 0;
+            } else {
+                tc::fence_after_sync();
+                tc::gemm_128x128x128(tmem + kColB, sQ, sW, false, false);  // Q W^T
+                tc::gemm_128x128x128(tmem + kColC, sK, sW, false, false);  // K W^T
+                tc::gemm_128x128x128(tmem + kColD, sQ, sK, false, false);  // Q K^T
+                tc::mma_commit(&bars.mma2);
+            }
+        }
         // T = (I + strict_lower(diag(beta) G))^{-1} diag(beta) into Tf (fp32)
         ut_solve(Gf, Tf, bsm, tid);
         // Q W^T, K W^T, Q K^T
-        if (tid == 0 && !mbar_wait(&bars.mma2, ph_mma2, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
+        if (tid == 0 && bars.ok && !mbar_wait(&bars.mma2, ph_mma2, a.err, nullptr, kWaitLimitNs))
+            bars.ok = 0;
         ph_mma2 ^= 1;
         __syncthreads();
         tc::fence_after_sync();
