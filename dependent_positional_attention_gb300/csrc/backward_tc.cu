@@ -211,15 +211,26 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 }
             }
         };
-        if (tid == 0) issue_loads(0);
-        for (int c = 0; c < b; ++c) {
-            if (!(ok = tma_sync())) break;
-            if (tid == 0) {
-                tc::gemm128_lo<false>(tmem + kColS, tc::desc_lo(slot(kQt), false),
-                                      tc::desc_lo(slot(kKh), false), false);  // S = Qt Kh^T
-                tc::gemm128_lo<false>(tmem + kColDP, tc::desc_lo(slot(kDO), false),
-                                      tc::desc_lo(slot(kVP), false), false);  // dP = dout V^T
+        // S and dP of step c: issued by thread 0 once the step's tiles have
+        // landed, for c > 0 at the end of step c-1's epilogue (their TMEM
+        // columns are free once step c-1's first epilogue has read them)
+        auto issue_s_dp = [&]() {
+            if (!mbar_wait(&bars.tma, ph_tma, a.err, nullptr, kWaitLimitNs)) {
+                bars.ok = 0;
+                return;
             }
+            tc::fence_after_sync();
+            tc::gemm128_lo<false>(tmem + kColS, tc::desc_lo(slot(kQt), false),
+                                  tc::desc_lo(slot(kKh), false), false);  // S = Qt Kh^T
+            tc::gemm128_lo<false>(tmem + kColDP, tc::desc_lo(slot(kDO), false),
+                                  tc::desc_lo(slot(kVP), false), false);  // dP = dout V^T
+        };
+        if (tid == 0) {
+            issue_loads(0);
+            issue_s_dp();
+        }
+        for (int c = 0; c < b; ++c) {
+            ph_tma ^= 1;  // the wait on step c's tiles was done in issue_s_dp
             if (!(ok = mma_sync())) break;
             // dl (scaled) as a bf16 tile
             {
@@ -269,6 +280,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 tc::tmem_ld64(tmem + lane_off + kColG + half * 64, v);
                 store_row(slot(kGs), v);
             }
+            if (tid == 0 && c + 1 < b) issue_s_dp();
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncthreads();
