@@ -363,6 +363,8 @@ path_status_t run_bwd_prep_tc(const path_prefill_desc_t *desc, const BwdPlan &p,
     if (s != PATH_OK) return s;
     BwdDiagArgs da;
     da.Dg = at<float>(workspace, p.off_Dg);
+    da.F = ba.F;
+    da.dF = ba.dF;
     da.lse = ba.lse; da.Sd = ft[Sd_]; da.dP = ft[dP_];
     da.P = bt[P_]; da.dSd = bt[dSd_]; da.scale = desc->scale;
     da.BH = p.BH; da.L = p.L; da.Lp = p.Lp; da.N = p.N;
@@ -653,9 +655,12 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
     ba.dq = dq; ba.dk = dk; ba.dv = dv; ba.dw = dw; ba.dbeta = dbeta; ba.dlog_f = dlog_f;
     ba.scale = desc->scale;
     ba.BH = p.BH; ba.L = p.L; ba.Lp = p.Lp; ba.N = p.N; ba.C = p.C; ba.d = p.d;
-    if (p.tc && !log_f) {
+    // PaTH-FoX takes the tensor-core route too, unless scale is 0 (its key-side
+    // column sums are read back from the scaled bf16 dlogit tile)
+    if (p.tc && (!log_f || desc->scale != 0.f)) {
         // tensor-core prep (bf16 Qh, Kh, Pm; its chunk outputs OD/LSD unused
-        // here), then the tensor-core scan, then the CUDA-core backward prep
+        // here), then the tensor-core scan and key side, then the backward
+        // prep (tensor-core contractions), then (PaTH-FoX) the dlog f suffix
         char *qh = at<char>(workspace, p.off_Qh), *kh = at<char>(workspace, p.off_Kh);
         char *pm = at<char>(workspace, p.off_Wt), *od = at<char>(workspace, p.off_Sd);
         char *qts = at<char>(workspace, p.off_Qts);
@@ -699,6 +704,8 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         tb.lse = lse; tb.dlse = dlse;
         tb.dQh = ba.dQh; tb.dKh = ba.dKh; tb.dV = ba.dV; tb.dA = ba.dA;
         tb.Dg = at<float>(workspace, p.off_Dg);
+        tb.F = F;
+        tb.dF = ba.dF;
         tb.scale = desc->scale;
         tb.BH = p.BH; tb.L = p.L; tb.Lp = p.Lp; tb.N = p.N;
         tb.err = error_flag_ptr();
@@ -710,7 +717,9 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         if (s != PATH_OK) return s;
         s = cuda_status(launch_bwd_kv_tc(bm, tb, sms, st), "tensor-core backward key-side launch");
         if (s != PATH_OK) return s;
-        return run_bwd_prep_tc(desc, p, ba, workspace, st);
+        s = run_bwd_prep_tc(desc, p, ba, workspace, st);
+        if (s != PATH_OK || !log_f) return s;
+        return cuda_status(launch_fox_suffix(ba.dF, dlog_f, p.L, p.Lp, p.BH, st), "fox suffix launch");
     }
     PrepSimtArgs pa;
     pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;

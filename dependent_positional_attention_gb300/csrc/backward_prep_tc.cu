@@ -275,24 +275,39 @@ __global__ void bwd_rowdot_kernel(const __nv_bfloat16 *out, const __nv_bfloat16 
     if (lane == 0) Dg[row] = (i < L) ? s - (dlse ? dlse[(size_t)bh * L + i] : 0.f) : 0.f;
 }
 
-// The chunk's own block: P = exp(scale Sd - lse) (j <= i), dSd = scale P (dP -
-// D), as bf16 tiles.  One block per chunk.
+// The chunk's own block: P = exp(scale Sd + F_i - F_j - lse) (j <= i; the
+// FoX term only for PaTH-FoX), dSd = scale P (dP - D), as bf16 tiles; for
+// PaTH-FoX also dF_i += sum_j dlogit_ij and dF_j -= sum_i dlogit_ij.  One
+// block per chunk; dlogit staged in shared memory for the sums.
 __global__ void __launch_bounds__(kThreads) bwd_diag_kernel(BwdDiagArgs a) {
-    __shared__ float rD[kC], rL[kC];
+    extern __shared__ float dls[];  // [C][C + 1] dlogit (PaTH-FoX only)
+    __shared__ float rD[kC], rL[kC], rF[kC];
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int c0 = chunk * kC, n = min(kC, a.L - c0);
     const size_t base = ((size_t)bh * a.Lp + c0) * kC;
+    const float *F = a.F ? a.F + (size_t)bh * a.Lp + c0 : nullptr;
     for (int r = threadIdx.x; r < kC; r += kThreads) {
         rD[r] = a.Dg[(size_t)bh * a.Lp + c0 + r];
         rL[r] = r < n ? a.lse[(size_t)bh * a.L + c0 + r] : 0.f;
+        rF[r] = F ? F[r] - F[0] : 0.f;  // chunk-relative prefix
     }
     __syncthreads();
     for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
         const int r = e / kC, j = e - r * kC;
         float p = 0.f;
-        if (r < n && j <= r) p = expf(a.scale * a.Sd[base + e] - rL[r]);
+        if (r < n && j <= r) p = expf(a.scale * a.Sd[base + e] + rF[r] - rF[j] - rL[r]);
+        const float dl = p * (a.dP[base + e] - rD[r]);
         a.P[base + e] = __float2bfloat16_rn(p);
-        a.dSd[base + e] = __float2bfloat16_rn(a.scale * p * (a.dP[base + e] - rD[r]));
+        a.dSd[base + e] = __float2bfloat16_rn(a.scale * dl);
+        if (F) dls[r * (kC + 1) + j] = dl;
+    }
+    if (!F) return;
+    __syncthreads();
+    for (int r = threadIdx.x; r < n; r += kThreads) {
+        float sr = 0.f, sc = 0.f;
+        for (int j = 0; j < kC; ++j) sr += dls[r * (kC + 1) + j];
+        for (int i = 0; i < kC; ++i) sc += dls[i * (kC + 1) + r];
+        atomicAdd(a.dF + (size_t)bh * a.Lp + c0 + r, sr - sc);
     }
 }
 
@@ -353,7 +368,11 @@ cudaError_t launch_bwd_rowdot(const __nv_bfloat16 *out, const __nv_bfloat16 *dou
 }
 
 cudaError_t launch_bwd_diag(const BwdDiagArgs &a, cudaStream_t st) {
-    bwd_diag_kernel<<<dim3(a.N, a.BH), kThreads, 0, st>>>(a);
+    const size_t sm = a.F ? sizeof(float) * kC * (kC + 1) : 0;
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    bwd_diag_kernel<<<dim3(a.N, a.BH), kThreads, sm, st>>>(a);
     return cudaGetLastError();
 }
 

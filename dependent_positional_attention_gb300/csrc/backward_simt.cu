@@ -507,13 +507,15 @@ cudaError_t launch_bwd_prep(const BwdArgs &a, bool bf16_io, cudaStream_t st) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (a.dF) {
-        const int warps = 4;
-        fox_suffix_kernel<<<(a.BH + warps - 1) / warps, 32 * warps, 0, st>>>(a.dF, a.dlog_f, a.L,
-                                                                             a.Lp, a.BH);
-        return cudaGetLastError();
-    }
+    if (a.dF) return launch_fox_suffix(a.dF, a.dlog_f, a.L, a.Lp, a.BH, st);
     return cudaSuccess;
+}
+
+cudaError_t launch_fox_suffix(const float *dF, float *dlog_f, int L, int Lp, int BH,
+                              cudaStream_t st) {
+    const int warps = 4;
+    fox_suffix_kernel<<<(BH + warps - 1) / warps, 32 * warps, 0, st>>>(dF, dlog_f, L, Lp, BH);
+    return cudaGetLastError();
 }
 
 }  // namespace path

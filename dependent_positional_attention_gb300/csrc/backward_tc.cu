@@ -51,8 +51,9 @@ struct BBars {
     uint64_t tma, mma;
     uint32_t tmem_base;
     int ok;
-    float rD[kC];  // dout . out - dlse
-    float rL[kC];  // lse * log2e
+    float rD[kC];    // dout . out - dlse
+    float rL[kC];    // lse * log2e (PaTH-FoX: less the row's bias term)
+    float fcol[kC];  // PaTH-FoX: (F_j - F_ref) * log2e of the current key chunk
 };
 constexpr int kSmemB = (int)sizeof(BBars) + 1023 + kSlots * kTile;
 static_assert(kSmemB <= 232448, "shared memory budget exceeded");
@@ -63,6 +64,7 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+template <bool kFox>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_scan_tc_kernel(const __grid_constant__ BwdTcMaps maps, BwdTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -150,6 +152,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             bars.rD[r] = a.Dg[head_rows + (size_t)b * kC + r];
             bars.rL[r] = r < nq ? a.lse[(size_t)bh * a.L + (size_t)b * kC + r] * kLog2e : 0.f;
         }
+        // PaTH-FoX: the row's prefix (log2 units) and its dF row sum
+        const float fi2 = kFox ? a.F[head_rows + (size_t)b * kC + r] * kLog2e : 0.f;
+        float frow = 0.f;
         // (R) dout_b and Qh_b, then the chain
         if (tid == 0) {
             mbar_arrive_expect_tx(&bars.tma, 2 * kTile);
@@ -231,13 +236,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         for (int c = 0; c < b; ++c) {
             ph_tma ^= 1;  // the wait on step c's tiles was done in issue_s_dp
+            if (kFox && half == 0)
+                bars.fcol[r] = (a.F[head_rows + (size_t)c * kC + r] - a.F[head_rows + (size_t)c * kC]) *
+                               kLog2e;
             if (!(ok = mma_sync())) break;
             // dl (scaled) as a bf16 tile
             {
                 uint32_t sv[64], pv[64];
                 tc::tmem_ld64(tmem + lane_off + kColS + half * 64, sv);
                 tc::tmem_ld64(tmem + lane_off + kColDP + half * 64, pv);
-                const float lr = bars.rL[r], dr = bars.rD[r];
+                // FoX: logit (log2) = S scale log2e - fcol[j] + (fi2 - fref2) with
+                // fref2 = F_ref log2e; folded into the row offset below
+                const float lr = bars.rL[r] -
+                                 (kFox ? fi2 - a.F[head_rows + (size_t)c * kC] * kLog2e : 0.f);
+                const float dr = bars.rD[r];
                 const bool live = r < nq;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -245,8 +257,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float x = __uint_as_float(sv[q * 8 + e]);
-                        p[e] = live ? ex2(fmaf(x, sl2, -lr)) : 0.f;
-                        g[e] = a.scale * p[e] * (__uint_as_float(pv[q * 8 + e]) - dr);
+                        const float fb = kFox ? bars.fcol[half * 64 + q * 8 + e] : 0.f;
+                        p[e] = live ? ex2(fmaf(x, sl2, -lr - fb)) : 0.f;
+                        const float gu = p[e] * (__uint_as_float(pv[q * 8 + e]) - dr);
+                        if (kFox) frow += gu;
+                        g[e] = a.scale * gu;
                     }
                     const uint32_t off = tc::swz_off(r, half * 8 + q, kC);
                     tc::sts128(slot(kDL) + off, tc::pack2(g[0], g[1]), tc::pack2(g[2], g[3]),
@@ -287,6 +302,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             tc::fence_after_sync();
         }
         if (!ok) break;
+        if (kFox && r < nq) atomicAdd(a.dF + head_rows + (size_t)b * kC + r, frow);
         // dQh_b = G (fp32)
         {
             uint32_t v[64];
@@ -320,6 +336,7 @@ constexpr int kSmemKV = (int)sizeof(BBars) + 1023 + kvSlots * kTile;
 static_assert(kSmemKV <= 232448, "shared memory budget exceeded");
 constexpr uint32_t kColDV = 256, kColDK = 384;
 
+template <bool kFox>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_kv_tc_kernel(const __grid_constant__ BwdTcMaps maps, BwdTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -381,12 +398,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const int k0 = c * kC;
         const size_t head_rows = (size_t)bh * a.Lp;
         bool ok = true;
+        // PaTH-FoX: the key chunk's relative prefixes (fixed for the job) and
+        // this thread's column sum of dlogit (column tid % 128, rows of its half)
+        const float fref2 = kFox ? a.F[head_rows + k0] * kLog2e : 0.f;
+        if (kFox && half == 0) bars.fcol[r] = a.F[head_rows + k0 + r] * kLog2e - fref2;
+        float fcolsum = 0.f;
         for (int b = c + 1; b < a.N; ++b) {
             const int nq = min(kC, a.L - b * kC);
             if (half == 0) {
                 const size_t row = head_rows + (size_t)b * kC + r;
                 bars.rD[r] = a.Dg[row];
-                bars.rL[r] = r < nq ? a.lse[(size_t)bh * a.L + (size_t)b * kC + r] * kLog2e : 0.f;
+                float l = r < nq ? a.lse[(size_t)bh * a.L + (size_t)b * kC + r] * kLog2e : 0.f;
+                if (kFox) l -= a.F[row] * kLog2e - fref2;
+                bars.rL[r] = l;
             }
             if (tid == 0) {
                 mbar_arrive_expect_tx(&bars.tma, (b == c + 1 ? 4 : 2) * kTile);
@@ -424,7 +448,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float x = __uint_as_float(sv[q * 8 + e]);
-                        p[e] = live ? ex2(fmaf(x, sl2, -lr)) : 0.f;
+                        const float fb = kFox ? bars.fcol[half * 64 + q * 8 + e] : 0.f;
+                        p[e] = live ? ex2(fmaf(x, sl2, -lr - fb)) : 0.f;
                         g[e] = a.scale * p[e] * (__uint_as_float(pv[q * 8 + e]) - dr);
                     }
                     const uint32_t off = tc::swz_off(r, half * 8 + q, kC);
@@ -446,8 +471,21 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                             tc::desc_lo(slot(kvQt), true), b > c + 1);
             }
             if (!(ok = mma_sync())) break;
+            if (kFox) {
+                // column tid % 128 of scale * dlogit, rows of this thread's half
+                const int j = tid & (kC - 1), r0 = (tid >> 7) * 64;
+                const uint8_t *dl = tiles + kvDL * kTile;
+                float cs = 0.f;
+#pragma unroll 8
+                for (int rr = r0; rr < r0 + 64; ++rr) {
+                    const uint32_t off = tc::swz_off(rr, j >> 3, kC) + (uint32_t)((j & 7) * 2);
+                    cs += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(dl + off));
+                }
+                fcolsum += cs;
+            }
         }
         if (!ok) break;
+        if (kFox) atomicAdd(a.dF + head_rows + k0 + (tid & (kC - 1)), -fcolsum / a.scale);
         {
             uint32_t v[64];
             const size_t krow = (head_rows + k0 + r) * kC + half * 64;
@@ -480,10 +518,12 @@ cudaError_t launch_bwd_kv_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_
     const int total = (a.N - 1) * a.BH;
     if (total <= 0) return cudaSuccess;
     const int grid = total < num_sms ? total : num_sms;
-    cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV);
+    void (*kern)(const BwdTcMaps, BwdTcArgs) =
+        a.F ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV);
     if (e != cudaSuccess) return e;
-    bwd_kv_tc_kernel<<<grid, kThreadsB, kSmemKV, st>>>(maps, a);
+    kern<<<grid, kThreadsB, kSmemKV, st>>>(maps, a);
     return cudaGetLastError();
 }
 
@@ -492,10 +532,12 @@ cudaError_t launch_bwd_scan_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int nu
     const int total = (a.N - 1) * a.BH;
     if (total <= 0) return cudaSuccess;
     const int grid = total < num_sms ? total : num_sms;
-    cudaError_t e = cudaFuncSetAttribute(bwd_scan_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemB);
+    void (*kern)(const BwdTcMaps, BwdTcArgs) =
+        a.F ? bwd_scan_tc_kernel<true> : bwd_scan_tc_kernel<false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemB);
     if (e != cudaSuccess) return e;
-    bwd_scan_tc_kernel<<<grid, kThreadsB, kSmemB, st>>>(maps, a);
+    kern<<<grid, kThreadsB, kSmemB, st>>>(maps, a);
     return cudaGetLastError();
 }
 

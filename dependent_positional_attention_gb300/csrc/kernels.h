@@ -69,8 +69,8 @@ size_t bwd_prep_smem(int C);
 // bf16_io: q, k, v, w, out, dout and the gradients dq, dk, dv, dw in bf16
 cudaError_t launch_bwd(const BwdArgs &a, bool bf16_io, cudaStream_t st);
 
-// Tensor-core backward scan (bf16, head_dim 128, chunk 128, PaTH without the
-// forget gate).  Maps: 3-D bf16 tensors [BH][rows][128] in 64 x 128 boxes
+// Tensor-core backward scan (bf16, head_dim 128, chunk 128; PaTH, and
+// PaTH-FoX when F is given).  Maps: 3-D bf16 tensors [BH][rows][128] in 64 x 128 boxes
 // with the 128-byte swizzle: qh, kh, pm from the tensor-core prep (rows =
 // Lp), v and dout (rows = L), qts the carried-row store (rows = 128 times
 // the number of (query chunk, earlier key chunk) pairs of a head).
@@ -84,6 +84,8 @@ struct BwdTcArgs {
     float *dQh, *dKh, *dV;            // [BH][Lp][128] fp32
     float *dA;                        // [BH][N][128][128] fp32 (accumulated)
     const float *Dg;                  // [BH][Lp] dout . out - dlse per query row
+    const float *F;                   // [BH][Lp] FoX prefix sums, or null (PaTH)
+    float *dF;                        // [BH][Lp] FoX dF accumulator (with F; scale != 0)
     float scale;
     int BH, L, Lp, N;
     uint32_t *err;
@@ -96,6 +98,9 @@ cudaError_t launch_bwd_kv_tc(const BwdTcMaps &maps, const BwdTcArgs &a, int num_
                              cudaStream_t st);
 // The CUDA-core backward prep alone (after a tensor-core scan).
 cudaError_t launch_bwd_prep(const BwdArgs &a, bool bf16_io, cudaStream_t st);
+// dlog f_s = sum_{i >= s} dF_i (PaTH-FoX backward, last step).
+cudaError_t launch_fox_suffix(const float *dF, float *dlog_f, int L, int Lp, int BH,
+                              cudaStream_t st);
 
 // Batched 128 x 128 x 128 contraction over all chunks of all heads (tensor
 // cores): per chunk, D = alpha * sum_p (+/-) op(A_p) op(B_p) (+ E), then an
@@ -126,6 +131,8 @@ cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs 
 
 struct BwdDiagArgs {
     const float *Dg;  // [BH][Lp] dout . out - dlse (bwd_rowdot)
+    const float *F;   // [BH][Lp] FoX prefix sums, or null (PaTH)
+    float *dF;        // [BH][Lp] FoX dF accumulator (with F)
     const float *lse, *Sd, *dP;
     __nv_bfloat16 *P, *dSd;
     float scale;

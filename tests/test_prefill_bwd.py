@@ -136,3 +136,20 @@ def test_autograd_function_matches_the_oracle():
                              log_f=to64(x["log_f"]))
     got = {"d" + n: to64(t[n].grad) for n in ("q", "k", "v", "w", "beta", "log_f")}
     check(got, ref, 1e-4)
+
+
+@pytest.mark.parametrize("L", [1, 129, 700])
+def test_tensor_core_route_fox(L):
+    """PaTH-FoX, bf16, head_dim 128: the forget-gate bias and dlog_f on the
+    tensor-core route."""
+    got, ref = run(wl.prefill_inputs(1, 3, L, 128, "bf16", seed=40 + L, fox=True), use_dlse=True)
+    assert "dlog_f" in got
+    check(got, ref, 2e-2)
+
+
+def test_fox_headline_shape_sampled_heads():
+    """PaTH-FoX B8 H12 L4096 d128 bf16 (the FoX benchmark's shape); two heads
+    checked in full."""
+    x = wl.prefill_inputs(8, 12, 4096, 128, "bf16", seed=0, fox=True)
+    got, ref = run(x, heads=[3, 90])
+    check(got, ref, 2e-2)
