@@ -376,13 +376,15 @@ def backward_block(wlk, steps, warmup, ws, peaks):
     with CUDA events; the four launches of one call form one step."""
     x = wl.workload_inputs(wlk, seed=0, device="cuda")
     q, k, v, w, beta = (x[n] for n in ("q", "k", "v", "w", "beta"))
-    out, lse = pa.path_attn_prefill_fwd(q, k, v, w, beta)
+    log_f = x.get("log_f") if wlk.fox else None
+    out, lse = pa.path_attn_prefill_fwd(q, k, v, w, beta, log_f=log_f)
     dout = torch.randn(q.shape, generator=torch.Generator("cuda").manual_seed(7), device="cuda",
                        dtype=torch.float32).to(q.dtype)
     desc = pa._prefill_desc(q, None, 0)
     ws_t = torch.empty(pa.path_attn_prefill_bwd_workspace_size(desc), device="cuda",
                        dtype=torch.uint8)
-    run = lambda: pa.path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, workspace=ws_t)
+    run = lambda: pa.path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, log_f=log_f,
+                                           workspace=ws_t)
     for _ in range(warmup):
         run()
     barrier(ws)
@@ -399,8 +401,9 @@ def backward_block(wlk, steps, warmup, ws, peaks):
     flops = backward_flops(B, H, L, d)
     tf = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
-    res = {"workload": "PaTH prefill backward (dq, dk, dv, dw, dbeta) B%d H%d L%d d%d %s"
-                       % (B, H, L, d, wlk.dtype),
+    res = {"workload": "%s prefill backward (dq, dk, dv, dw, dbeta%s) B%d H%d L%d d%d %s"
+                       % ("PaTH-FoX" if wlk.fox else "PaTH", ", dlog_f" if wlk.fox else "",
+                          B, H, L, d, wlk.dtype),
            "tokens_per_s": job_throughput(B * L, ms, ws), "ms_per_step": ms,
            "flops_per_step": flops, "tflops": tf, "workspace_bytes": ws_t.numel(),
            "roofline": {"kernel": "whole backward call: prep_tc_kernel + bwd_scan_tc_kernel + "
@@ -409,7 +412,7 @@ def backward_block(wlk, steps, warmup, ws, peaks):
                         "frac": tf / peak, "traffic": None,
                         "peak_source": peaks["source"] + " bf16 dense (sustained: a step of "
                                        "about 30 launches)"}}
-    del x, out, lse, dout, ws_t
+    del x, out, lse, dout, ws_t, log_f
     torch.cuda.empty_cache()
     return res
 
@@ -546,6 +549,7 @@ def main():
         extra["decode_fox_64k"] = decode_block(wl.DECODE_64K, wl.DECODE_64K.steps, warmup, ws,
                                                peaks, fox=True)
         extra["backward_4k"] = backward_block(head, max(3, steps // 2), 3, ws, peaks)
+        extra["backward_fox_4k"] = backward_block(wl.FOX_4K, max(3, steps // 2), 3, ws, peaks)
         extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
         extra["chunk_autotune_bf16_d64"] = autotune_block(
             wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (CUDA-core route)",

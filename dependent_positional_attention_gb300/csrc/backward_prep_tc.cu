@@ -319,18 +319,22 @@ __global__ void bwd_cvt_kernel(const float *x, __nv_bfloat16 *y, size_t n4) {
     }
 }
 
-// dbeta_s = dX_ss + sum_{t<s} dLo_st G_st, one thread per row.
+// dbeta_s = dX_ss + sum_{t<s} dLo_st G_st, one warp per row (dLo is zero for
+// t >= s, so the whole row is summed).
 __global__ void bwd_dbeta_kernel(const float *dX, const float *dLo, const float *G, float *dbeta,
                                  int L, int Lp, int N, int BH) {
-    const int row = blockIdx.x * blockDim.x + threadIdx.x;  // over BH * Lp
-    if (row >= BH * Lp) return;
-    const int bh = row / Lp, i = row % Lp;
+    const size_t row = (size_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;  // over BH * Lp
+    const int lane = threadIdx.x & 31;
+    if (row >= (size_t)BH * Lp) return;
+    const int bh = (int)(row / Lp), i = (int)(row % Lp);
     if (i >= L) return;
-    const int s = i % kC;
-    const size_t base = (size_t)row * kC;
-    float v = dX[base + s];
-    for (int t = 0; t < s; ++t) v = fmaf(dLo[base + t], G[base + t], v);
-    dbeta[(size_t)bh * L + i] = v;
+    const size_t base = row * kC;
+    const float4 x = reinterpret_cast<const float4 *>(dLo + base)[lane];
+    const float4 g = reinterpret_cast<const float4 *>(G + base)[lane];
+    float v = x.x * g.x + x.y * g.y + x.z * g.z + x.w * g.w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) dbeta[(size_t)bh * L + i] = v + dX[base + i % kC];
 }
 
 }  // namespace
@@ -385,8 +389,8 @@ cudaError_t launch_bwd_cvt(const float *x, __nv_bfloat16 *y, size_t n, cudaStrea
 
 cudaError_t launch_bwd_dbeta(const float *dX, const float *dLo, const float *G, float *dbeta,
                              int BH, int L, int Lp, int N, cudaStream_t st) {
-    const int rows = BH * Lp;
-    bwd_dbeta_kernel<<<(rows + 127) / 128, 128, 0, st>>>(dX, dLo, G, dbeta, L, Lp, N, BH);
+    const size_t rows = (size_t)BH * Lp;
+    bwd_dbeta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(dX, dLo, G, dbeta, L, Lp, N, BH);
     return cudaGetLastError();
 }
 
