@@ -43,7 +43,7 @@ def prefill_flops(B, H, L, d, C=CHUNK):
     N (N-1) / 2 pairs) plus the carried-query update (one C x d x d product
     with a chunk's d x d transition matrix per pair (b, c) with c >= 1:
     2 C d^2 (N-1)(N-2)/2).
-    prep: the chunk UT transform (16 L C d, the survey's count) plus each
+    prep: the chunk UT transform (16 L C d: G, T and the boundary products) plus each
     chunk's own causal block (QK^T + PV over its lower triangle, 2 C^2 d).
     Returns (scan_flops, prep_flops)."""
     N = math.ceil(L / C)
