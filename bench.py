@@ -22,6 +22,7 @@ import math
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -88,25 +89,42 @@ class ClockSampler:
     def __init__(self):
         self.proc = None
         self.lines = []
+        self.reader = None
 
     def start(self):
+        """Starts sampling every 20 ms and returns once the first sample is in,
+        so that the samples that follow fall inside the timed region."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        first = threading.Event()
+
+        def read():
+            for line in self.proc.stdout:
+                self.lines.append(line)
+                first.set()
+            first.set()
+
+        self.reader = threading.Thread(target=read, daemon=True)
+        self.reader.start()
+        first.wait(timeout=5.0)
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.03)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        if self.reader is not None:
+            self.reader.join(timeout=5)
+        out = "".join(self.lines)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
@@ -470,7 +488,7 @@ def workload_config(head, ws):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-extra", action="store_true",
