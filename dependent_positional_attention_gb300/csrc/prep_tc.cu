@@ -54,7 +54,8 @@ constexpr int kOffR1 = 3 * kTile;            // G fp32, then T bf16 | -(M_le*QW)
 constexpr int kR1Bytes = 64 * 1024;
 constexpr int kOffR2 = kOffR1 + kR1Bytes;    // T fp32, then KWm/Y bf16 | Wt bf16
 constexpr int kOffBar = kOffR2 + 64 * 1024;
-constexpr int kSmemP = kOffBar + 640 + 1024;
+constexpr int kBarBytes = 1152;
+constexpr int kSmemP = kOffBar + kBarBytes + 1024;
 static_assert(kC * kC * 4 <= kR1Bytes, "G staging does not fit");
 static_assert(kSmemP <= 232448, "shared memory budget exceeded");
 constexpr uint32_t kColA = 0, kColB = 128, kColC = 256, kColD = 384;
@@ -64,8 +65,9 @@ struct PBars {
     uint32_t tmem_base;
     int ok;
     alignas(16) float beta[kC];
+    float fsm[kC];  // PaTH-FoX: the chunk's prefix sums relative to its first, log2 units
 };
-static_assert(sizeof(PBars) <= 640, "barrier block too large");
+static_assert(sizeof(PBars) <= kBarBytes, "barrier block too large");
 
 using tc::lds128;
 using tc::pack2;
@@ -179,6 +181,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int n = min(kC, a.L - c0);
         // beta of the chunk, read ahead of its use in P2
         const float beta_r = (tid < kC && tid < n) ? a.beta[(size_t)bh * a.L + c0 + tid] : 0.f;
+        // PaTH-FoX: the chunk's prefix sums, relative to its first (the bias
+        // F_i - F_j is unchanged), read ahead of their use in P9
+        const float f_r = (a.F && tid < kC)
+                              ? (a.F[(size_t)bh * a.Lp + c0 + tid] - a.F[(size_t)bh * a.Lp + c0]) *
+                                    1.4426950408889634f
+                              : 0.f;
         // ---------------------------------------------------------------- P1
         // W first: G = W W^T alone lets the solve for T start while the
         // other three products run
@@ -213,7 +221,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         tc::fence_after_sync();
         if (!bars.ok) break;
         // ---------------------------------------------------------------- P2
-        if (tid < kC) bsm[tid] = beta_r;
+        if (tid < kC) {
+            bsm[tid] = beta_r;
+            bars.fsm[tid] = f_r;
+        }
         {
             uint32_t v[32];
 #pragma unroll
@@ -382,8 +393,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             // per-row partial max / sum of the two column halves, in the R2
             // region (its Y / Wt tiles were last read by the P7 MMAs)
             float(*red)[2][kC] = reinterpret_cast<float(*)[2][kC]>(smem + kOffR2);
-            const float *F = a.F ? a.F + (size_t)bh * a.Lp + c0 : nullptr;
-            const float fi = F ? F[r] * 1.4426950408889634f : 0.f;
+            const bool fox = a.F != nullptr;
+            const float fi = fox ? bars.fsm[r] : 0.f;
             uint32_t v[64];
             tc::tmem_ld64(tmem + lane_off + kColD + half * 64, v);
             float mx = -INFINITY;
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             for (int i = 0; i < 64; ++i) {
                 const int j = half * 64 + i;
                 float x = __uint_as_float(v[i]) * sl2;
-                if (F) x += fi - F[j] * 1.4426950408889634f;
+                if (fox) x += fi - bars.fsm[j];
                 x = (j <= r) ? x : -INFINITY;
                 v[i] = __float_as_uint(x);
                 mx = fmaxf(mx, x);
