@@ -1,8 +1,9 @@
-// Backward prep on tensor cores (bf16, head_dim 128, chunk 128, PaTH without
-// the forget gate): the chunk's own causal block and the gradient through
-// the boundary adjustment and the UT transform, as a sequence of batched
+// Backward prep on tensor cores (bf16, head_dim 128, chunk 128; PaTH and
+// PaTH-FoX): the chunk's own causal block and the gradient through the
+// boundary adjustment and the UT transform, as a sequence of batched
 // 128 x 128 x 128 contractions over all chunks (bf16 operands, fp32
-// accumulation in TMEM) plus four small CUDA-core steps.  The formulas are
+// accumulation in TMEM) plus small CUDA-core steps: the per-row D, the UT
+// solve, the chunk's own softmax block, fp32 -> bf16 conversions and dbeta.  The formulas are
 // those of bwd_prep_kernel (backward_simt.cu); here
 //   T = Ti diag(beta),  Ti = (I + strict_lower(diag(beta) G))^{-1},
 // so that the solve dX = (I + Lo)^{-T} dT becomes the product Ti^T dT.

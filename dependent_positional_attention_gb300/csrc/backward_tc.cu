@@ -29,9 +29,16 @@
 // decreasing order of work.  Every wait is bounded; on timeout a kernel sets
 // the device error flag and stops.
 //
-// Query-side shared memory: seven 32 KB bf16 tiles (dout_b, Qt, Kh_c, V_c /
-// P, Pm_c, dl, G).  TMEM columns: [0,128) S, [128,256) dP, [256,384) G,
-// [384,512) the chain product U then dA.
+// Query-side shared memory: seven 32 KB bf16 tiles (dout_b, Qt, Kh_c, V_c,
+// Pm_c, dl, G).  TMEM columns: [0,128) S, [128,256) dP, [256,384) G,
+// [384,512) the chain product U then dA.  The loads of step c are issued as
+// soon as step c-1's MMAs are done, and step c's S and dP MMAs at the end of
+// step c-1's epilogue.
+//
+// PaTH-FoX (kFox): the logit gains F_i - F_j (F the inclusive prefix of log f),
+// split as in the forward scan into a per-row term and a chunk-relative column
+// term; dF gets exact row sums of dlogit on the query side and column sums on
+// the key side.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -45,7 +52,7 @@ constexpr int kTile = kC * kC * 2;
 constexpr int kThreadsB = 256;
 constexpr uint32_t kColS = 0, kColDP = 128, kColG = 256, kColU = 384;
 constexpr float kLog2e = 1.4426950408889634f;
-enum { kDO = 0, kQt, kKh, kVP, kPm, kDL, kGs, kSlots };
+enum { kDO = 0, kQt, kKh, kVP, kPm, kDL, kGs, kSlots };  // kVP: V (the key side's P slot)
 
 struct BBars {
     uint64_t tma, mma;
