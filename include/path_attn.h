@@ -145,10 +145,13 @@ size_t path_attn_prefill_bwd_workspace_size(const path_prefill_desc_t *desc);
  *   dbeta        : float32 [B][H][L], written.
  *   dlog_f       : float32 [B][H][L], written; required exactly when log_f is given.
  *   workspace    : at least path_attn_prefill_bwd_workspace_size(desc) bytes.
- * All arithmetic is fp32 on the CUDA cores for both dtypes (bf16 values are
- * converted on load and store).  desc->chunk: 16, 32, 64 or 128, or 0 for the
- * same default as the forward's CUDA-core route; it need not match the chunk
- * the forward used.  Supported: head_dim <= 128 and a multiple of 4.
+ * PATH_BF16 with head_dim 128 and chunk 128 (the default there) runs on the
+ * tensor cores (bf16 operands, fp32 accumulation), PaTH and PaTH-FoX alike
+ * (PaTH-FoX with scale 0 excepted); every other case runs in fp32 on the CUDA
+ * cores (bf16 values converted on load and store).  desc->chunk: 16, 32, 64
+ * or 128, or 0 for the default of the forward's CUDA-core route; it need not
+ * match the chunk the forward used.  Supported: head_dim <= 128 and a
+ * multiple of 4.
  * Pointers must be 16-byte aligned.  Argument errors are returned before
  * any launch; the call is asynchronous on `stream`.
  */
