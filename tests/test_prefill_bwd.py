@@ -24,17 +24,18 @@ pytestmark = pytest.mark.gpu
 GRADS = ("dq", "dk", "dv", "dw", "dbeta")
 
 
-def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None):
+def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None, scale=None):
     dev = torch.device("cuda:0")
     g = {n: t.to(dev) for n, t in x.items()}
     gen = torch.Generator().manual_seed(1234)
     dout = torch.randn(g["q"].shape, generator=gen).to(g["q"].dtype)
     dlse = torch.randn(g["beta"].shape, generator=gen) if use_dlse else None
     out, lse = pa.path_attn_prefill_fwd(g["q"], g["k"], g["v"], g["w"], g["beta"],
-                                        log_f=g.get("log_f"), chunk=fwd_chunk)
+                                        log_f=g.get("log_f"), chunk=fwd_chunk, scale=scale)
     got = pa.path_attn_prefill_bwd(g["q"], g["k"], g["v"], g["w"], g["beta"], out, lse,
                                    dout.to(dev), log_f=g.get("log_f"),
-                                   dlse=dlse.to(dev) if dlse is not None else None, chunk=chunk)
+                                   dlse=dlse.to(dev) if dlse is not None else None, chunk=chunk,
+                                   scale=scale)
     torch.cuda.synchronize()
     assert pa.path_attn_device_status() == 0
     sel = slice(None) if heads is None else heads
@@ -45,7 +46,7 @@ def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None):
 
     args = [pick(x[n]) for n in ("q", "k", "v", "w", "beta")]
     ref = oracle.prefill_bwd(*args, pick(dout), log_f=pick(x["log_f"]) if "log_f" in x else None,
-                             dlse=pick(dlse) if dlse is not None else None)
+                             dlse=pick(dlse) if dlse is not None else None, scale=scale)
     return {n: pick(t) for n, t in got.items()}, ref
 
 
@@ -152,4 +153,19 @@ def test_fox_headline_shape_sampled_heads():
     checked in full."""
     x = wl.prefill_inputs(8, 12, 4096, 128, "bf16", seed=0, fox=True)
     got, ref = run(x, heads=[3, 90])
+    check(got, ref, 2e-2)
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_custom_scale(dtype, d):
+    """A scale other than 1/sqrt(d), on both routes."""
+    got, ref = run(wl.prefill_inputs(1, 2, 300, d, dtype, seed=17), use_dlse=True, scale=0.37)
+    check(got, ref, 1e-4 if dtype == "f32" else 2e-2)
+
+
+def test_fox_zero_scale_takes_the_cuda_core_route():
+    """scale = 0: the logits are the forget-gate bias alone; bf16 d = 128
+    PaTH-FoX then runs on the CUDA cores and still matches the oracle."""
+    got, ref = run(wl.prefill_inputs(1, 2, 260, 128, "bf16", seed=19, fox=True), use_dlse=True,
+                   scale=0.0)
     check(got, ref, 2e-2)
