@@ -570,7 +570,8 @@ def main():
         extra["backward_fox_4k"] = backward_block(wl.FOX_4K, max(3, steps // 2), 3, ws, peaks)
         extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
         extra["chunk_autotune_bf16_d64"] = autotune_block(
-            wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (CUDA-core route)",
+            wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (chunks 16-64 on the CUDA "
+                               "cores; 128 and the default on the tensor cores, padded)",
                                8, 12, 4096, 64, "bf16"))
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -63,10 +63,12 @@ int num_sms() {
 
 struct PrefillPlan {
     int BH, L, Lp, N, C, d;
+    int dk;     // head dim of the kernels (128 on the tensor-core route)
     bool bf16;  // bf16 inputs and output
-    bool tc;    // the tensor-core route (bf16, head_dim 128, chunk 128); else CUDA cores
+    bool tc;    // the tensor-core route (bf16, chunk 128); else CUDA cores
+    bool pad;   // tensor-core route for head_dim < 128: q, k, v, w, out zero-padded to 128
     size_t esize;
-    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, total;
+    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_pad, total;
 };
 
 // Checks shared by the prefill forward and backward descriptors.
@@ -105,7 +107,12 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     const long long BH = (long long)desc->batch * desc->heads;
     p->bf16 = desc->dtype == PATH_BF16;
     p->d = desc->head_dim;
-    p->tc = p->bf16 && p->d == 128;
+    // bf16 with head_dim a multiple of 8 below 128 takes the tensor-core route on
+    // zero-padded copies (pad.cu) unless a chunk other than 128 is asked for
+    const bool pad_ok = p->bf16 && p->d < 128 && p->d % 8 == 0 &&
+                        (desc->chunk == 0 || desc->chunk == 128);
+    p->tc = p->bf16 && (p->d == 128 || pad_ok);
+    p->pad = p->tc && p->d < 128;
     if (p->tc) {
         if (desc->chunk != 0 && desc->chunk != 128)
             return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 with head_dim 128 needs chunk 0 or 128");
@@ -121,19 +128,23 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     if ((long long)p->N * p->C > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
     p->Lp = p->N * p->C;
     p->esize = p->tc ? 2 : 4;  // the CUDA-core route keeps an fp32 workspace
+    p->dk = p->tc ? 128 : p->d;
     const size_t rows = (size_t)p->BH * p->Lp;
     const size_t cc = (size_t)p->BH * p->N * p->C * p->C;
     size_t off = 0;
-    p->off_Qh = off; off = align_up(off + rows * p->d * p->esize, 256);
-    p->off_Kh = off; off = align_up(off + rows * p->d * p->esize, 256);
-    p->off_Wt = off; off = align_up(off + rows * p->d * p->esize, 256);
+    p->off_Qh = off; off = align_up(off + rows * p->dk * p->esize, 256);
+    p->off_Kh = off; off = align_up(off + rows * p->dk * p->esize, 256);
+    p->off_Wt = off; off = align_up(off + rows * p->dk * p->esize, 256);
     p->off_Sd = off; off = align_up(off + cc * 4, 256);
     p->off_F = off; off = align_up(off + rows * 4, 256);
     // fp32 scratch of the SIMT prep (the tensor-core prep keeps it on chip)
     p->off_scratch = off; off = align_up(off + (p->tc ? 0 : cc * 5 * 4), 256);
+    // padded q, k, w, v and out, [BH][L][128] bf16 each
+    p->off_pad = off; off = align_up(off + (p->pad ? (size_t)5 * p->BH * p->L * 128 * 2 : 0), 256);
     p->total = off;
     return ok();
 }
+
 
 // Backward workspace (all fp32): the forward prep's Qh, Kh, Wt, Sd, F and
 // its scratch (shared with the backward prep's), the carried query rows Qts
@@ -246,6 +257,11 @@ path_status_t plan_kcache(const path_prefill_desc_t *desc, KcachePlan *p) {
 
 template <class T> T *at(void *base, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(base) + off);
+}
+
+// Address of padded array i (0 q, 1 k, 2 w, 3 v, 4 out) of a padded-route workspace.
+char *pad_buf(void *workspace, const PrefillPlan &p, int i) {
+    return at<char>(workspace, p.off_pad) + (size_t)i * p.BH * p.L * 128 * 2;
 }
 
 path_status_t cuda_status(cudaError_t e, const char *what) {
@@ -492,6 +508,18 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
             "fox prefix launch");
         if (s != PATH_OK) return s;
     }
+    if (p.pad) {
+        const void *src[4] = {q, k, w, v};
+        for (int i = 0; i < 4 && s == PATH_OK; ++i)
+            s = cuda_status(launch_pad_rows(src[i], pad_buf(workspace, p, i), (size_t)p.BH * p.L,
+                                            p.d, st),
+                            "pad launch");
+        if (s != PATH_OK) return s;
+        q = pad_buf(workspace, p, 0);
+        k = pad_buf(workspace, p, 1);
+        w = pad_buf(workspace, p, 2);
+        v = pad_buf(workspace, p, 3);
+    }
     if (p.tc) {
         PrepTcMaps maps;
         const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.L, p.BH, 64, 128) &&
@@ -556,6 +584,11 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
     const void *Wt = at<char>(workspace, p.off_Wt);
     const float *Sd = at<float>(workspace, p.off_Sd);
     const float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
+    void *out_user = out;
+    if (p.pad) {
+        v = pad_buf(workspace, p, 3);
+        out = pad_buf(workspace, p, 4);
+    }
     if (p.tc) {
         FlashTcMaps maps;
         const bool enc =
@@ -573,7 +606,10 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
-        return cuda_status(launch_flash_tc(maps, ta, sms, st), "tensor-core scan launch");
+        s = cuda_status(launch_flash_tc(maps, ta, sms, st), "tensor-core scan launch");
+        if (s != PATH_OK || !p.pad) return s;
+        return cuda_status(launch_unpad_rows(out, out_user, (size_t)p.BH * p.L, p.d, st),
+                           "unpad launch");
     }
     FlashSimtArgs fa;
     fa.Qh = Qh; fa.Kh = Kh; fa.Wt = Wt; fa.w = w; fa.v = v;

@@ -222,4 +222,9 @@ cudaError_t launch_prep_tc(const PrepTcMaps &maps, const PrepTcArgs &a, int num_
 
 cudaError_t launch_selftest_wait(uint32_t *err_flag, uint64_t limit_ns, cudaStream_t st);
 
+// bf16 rows [rows][d] <-> [rows][128] (zero-filled columns d..127); d a
+// multiple of 8, both pointers 16-byte aligned.
+cudaError_t launch_pad_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st);
+cudaError_t launch_unpad_rows(const void *src, void *dst, size_t rows, int d, cudaStream_t st);
+
 }  // namespace path

@@ -86,12 +86,23 @@ def test_full_size_sampled_rows(wname):
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
 
 
-@pytest.mark.parametrize("d,L,chunk,fox", [(64, 300, 0, False), (64, 257, 32, True),
-                                           (32, 190, 16, False), (96, 129, 128, False)])
+@pytest.mark.parametrize("d,L,chunk,fox", [(64, 257, 32, True), (32, 190, 16, False),
+                                           (96, 129, 64, False), (36, 200, 0, False)])
 def test_cuda_core_route_other_head_dims(d, L, chunk, fox):
-    """bf16 inputs with a head_dim the tensor-core route does not take run on
-    the CUDA cores (fp32 inside, bf16 in and out); same tolerance."""
+    """bf16 with a chunk other than 128 (or a head_dim not a multiple of 8)
+    runs on the CUDA cores (fp32 inside, bf16 in and out); same tolerance."""
     eo, el = run(wl.prefill_inputs(2, 2, L, d, "bf16", seed=d + L, fox=fox), chunk=chunk)
+    assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
+
+
+@pytest.mark.parametrize("d,L,chunk,fox", [(64, 300, 0, False), (64, 700, 128, True),
+                                           (32, 129, 0, False), (96, 1, 0, True),
+                                           (120, 260, 0, False)])
+def test_padded_tensor_core_route(d, L, chunk, fox):
+    """bf16 with head_dim a multiple of 8 below 128 and chunk 128 (the
+    default): the tensor-core kernels on zero-padded copies, the caller's
+    scale kept; same tolerance."""
+    eo, el = run(wl.prefill_inputs(2, 3, L, d, "bf16", seed=d + L + 1, fox=fox), chunk=chunk)
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
 
 
