@@ -57,7 +57,9 @@ typedef struct {
     int32_t batch, heads, seq_len, head_dim;
     int32_t dtype;  /* path_dtype_t */
     float scale;    /* multiplies k^T(...)q; usually 1/sqrt(head_dim) */
-    int32_t chunk;  /* 0 = default. PATH_BF16 with head_dim 128: 128 only.
+    int32_t chunk;  /* 0 = default. PATH_BF16 with head_dim 128: 128 only
+                       (head_dim a multiple of 8 below 128: 0 or 128 for the
+                       tensor cores, others on the CUDA cores).
                        Otherwise 16, 32, 64 or 128; the default is 64
                        when batch*heads*seq_len <= 8192 and head_dim <= 64,
                        else 128. */
@@ -84,9 +86,11 @@ size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc);
  *   workspace  : device buffer of at least
  *                path_attn_prefill_workspace_size(desc) bytes.
  * Supported: head_dim <= 128 and a multiple of 4, PATH_F32 or PATH_BF16.
- * PATH_BF16 with head_dim 128 runs on the tensor cores (chunk 128); every
- * other case runs on the CUDA cores in fp32 (bf16 inputs and output are
- * converted on load and store).  seq_len may be any value >= 1 (the last
+ * PATH_BF16 with head_dim 128 runs on the tensor cores (chunk 128); so does
+ * PATH_BF16 with head_dim a multiple of 8 below 128 and chunk 0 or 128, on
+ * copies zero-padded to 128 in the workspace (exact: the padded coordinates
+ * do not change any logit).  Every other case runs on the CUDA cores in fp32
+ * (bf16 inputs and output converted on load and store).  seq_len may be any value >= 1 (the last
  * chunk may be partial).  Method: section 3 of the PaTH summary — a per-chunk UT
  * transform builds boundary-adjusted rows and the compact chunk product,
  * then a blockwise scan visits key chunks right to left, carrying the
