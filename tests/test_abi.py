@@ -160,3 +160,22 @@ def test_backward_rejects_bad_arguments(lib):
     a = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(D(1, 1, 4096, 64, 0, 0.1, 64)))
     b = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(D(1, 1, 8192, 64, 0, 0.1, 64)))
     assert 3.0 < b / a < 4.2
+
+
+def test_padded_route_workspace(lib):
+    """bf16 with head_dim a multiple of 8 below 128 and the default chunk is
+    planned on the tensor-core route with zero-padded copies: its workspace
+    holds the 128-wide padded q, k, w, v and out on top of the head_dim-128
+    layout; an explicit chunk other than 128 plans the CUDA-core route."""
+    D = pa.PrefillDesc
+    B, H, L = 2, 3, 300
+    ws = lambda d, dtype, chunk: lib.path_attn_prefill_workspace_size(
+        ctypes.byref(D(B, H, L, d, dtype, 0.1, chunk)))
+    full = ws(128, 1, 0)
+    padded = ws(64, 1, 0)
+    assert padded >= full + 5 * B * H * L * 128 * 2
+    assert ws(64, 1, 128) == padded
+    # chunk 64 on the CUDA-core route: fp32 workspace of head_dim 64, no padded copies
+    assert 0 < ws(64, 1, 64) != padded
+    # head_dim 36 (not a multiple of 8) stays on the CUDA cores
+    assert ws(36, 1, 0) > 0
