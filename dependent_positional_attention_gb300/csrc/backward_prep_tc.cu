@@ -342,13 +342,10 @@ __global__ void bwd_dbeta_kernel(const float *dX, const float *dLo, const float 
 
 cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs &a,
                                  int num_sms, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_gemm_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemG);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    // set on every call: function attributes are per device
+    cudaError_t e = cudaFuncSetAttribute(chunk_gemm_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemG);
+    if (e != cudaSuccess) return e;
     const int jobs = a.N * a.BH;
     chunk_gemm_tc_kernel<<<jobs < num_sms ? jobs : num_sms, kThreadsG, kSmemG, st>>>(maps, a);
     return cudaGetLastError();
