@@ -402,8 +402,16 @@ def path_attn_fox_prefix(log_f, f_out, stream=None):
 def path_attn_decode_step_noalloc(k_cache, v_cache, cache_len, q_t, k_t, v_t, w_t, beta_t,
                                   out, scale=None, stream=None):
     """path_attn_decode_step without a workspace (see include/path_attn.h):
-    for callers that cannot allocate device memory.  `out` must be given."""
+    for callers that cannot allocate device memory.  `out` must be given;
+    the tensors are checked as for path_attn_decode_step."""
+    import torch
     lib = load_library()
+    B, H, cap, d = k_cache.shape
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", (B, H, cap, d), k_cache.dtype)
+    for t, n in ((q_t, "q_t"), (k_t, "k_t"), (v_t, "v_t"), (w_t, "w_t"), (out, "out")):
+        _need(t, n, (B, H, d), k_cache.dtype)
+    _need(beta_t, "beta_t", (B, H), torch.float32)
     desc = decode_desc(k_cache, scale)
     _check(lib.path_attn_decode_step_noalloc(
         ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), int(cache_len), _ptr(q_t), _ptr(k_t),

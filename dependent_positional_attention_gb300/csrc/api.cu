@@ -6,13 +6,15 @@
 
 #include "../../include/path_attn.h"
 #include "common.cuh"
+#include "ctx_symbol.h"
 #include "kernels.h"
 #include "tmap.h"
 
 namespace path {
 
-// The library's only device-resident state: the error flag set by kernels
-// whose bounded waits ran out.
+// Device-resident state of the library: this error flag, set by kernels
+// whose bounded waits ran out, and the fixed split-KV scratch of the
+// allocation-free decode step (decode_noalloc.cu).
 __device__ uint32_t g_error_flag;
 
 namespace {
@@ -36,17 +38,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Per-device address of g_error_flag (looked up once per device).
+// Address of g_error_flag in the caller's current context (cached per
+// context, ctx_symbol.h).
+cudaError_t lookup_error_flag(void **p) { return cudaGetSymbolAddress(p, g_error_flag); }
+PerContextAddress g_error_flag_addr(&lookup_error_flag);
+
 uint32_t *error_flag_ptr() {
-    static uint32_t *ptrs[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptrs[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_flag) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<uint32_t *>(p);
-    }
-    return ptrs[dev];
+    void *p = nullptr;
+    return g_error_flag_addr.get(&p) == cudaSuccess ? static_cast<uint32_t *>(p) : nullptr;
 }
 
 int num_sms() {

@@ -12,9 +12,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
-#include <mutex>
-
 #include "../../include/path_attn.h"
+#include "ctx_symbol.h"
 #include "kernels.h"
 
 namespace path {
@@ -29,26 +28,10 @@ constexpr size_t kScratchFloats = size_t(1) << 21;
 static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
 
 // Host code may not use g_decode_scratch's name as an address (it is a host
-// stand-in); the device address is looked up once per device, with that
-// device current.
-std::mutex g_setup_mutex;
-float *g_scratch_addr[64] = {nullptr};
-
-cudaError_t scratch_on_current_device(float **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<float *>(p);
-    }
-    *out = g_scratch_addr[dev];
-    return cudaSuccess;
-}
+// stand-in); its device address is looked up with the caller's context
+// current and cached per context (ctx_symbol.h).
+cudaError_t lookup_scratch(void **p) { return cudaGetSymbolAddress(p, g_decode_scratch); }
+PerContextAddress g_scratch_addr(&lookup_scratch);
 
 path_status_t reject(path_status_t s, const char *fmt, ...) {
     char buf[512];
@@ -103,8 +86,9 @@ extern "C" path_status_t path_attn_decode_step_noalloc(
                       "path_attn_decode_step_noalloc holds %zu bytes (batch*heads*ceil(cache_len/"
                       "%d)*(head_dim+2)*4); use path_attn_decode_step with a workspace",
                       need * 4, kScratchFloats * 4, per);
-    float *scratch = nullptr;
-    cudaError_t e = scratch_on_current_device(&scratch);
+    void *scratch_v = nullptr;
+    cudaError_t e = g_scratch_addr.get(&scratch_v);
+    float *scratch = static_cast<float *>(scratch_v);
     if (e != cudaSuccess)
         return reject(PATH_ERR_CUDA, "scratch address lookup: %s", cudaGetErrorString(e));
     // Nothing in the scratch needs clearing: every partial the combine kernel

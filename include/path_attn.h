@@ -19,8 +19,9 @@
  *     w, out and the caches is the descriptor's dtype.
  *   - Every device pointer must be 16-byte aligned.
  *   - The caller owns every buffer, the workspace included.  The library
- *     allocates no memory and keeps no state between calls (besides a
- *     one-word device error flag, see path_attn_device_status).
+ *     allocates no memory and keeps no state between calls, besides a
+ *     one-word device error flag (see path_attn_device_status) and the fixed
+ *     scratch array of path_attn_decode_step_noalloc.
  *   - Calls are asynchronous on `stream`.  Argument errors are returned
  *     before anything is launched.  A launch failure returns PATH_ERR_CUDA.
  *   - Preconditions the library does not check or enforce: w rows have unit
@@ -247,9 +248,11 @@ path_status_t path_attn_fox_prefix(const float *log_f, float *f_out, int32_t hea
  * every GPU loading the library holds until the process exits.  A step needs
  * batch * heads * ceil(cache_len / 1024) * (head_dim + 2) * 4 bytes of it;
  * larger steps are rejected with PATH_ERR_INVALID_ARG and a message naming
- * both sizes (use path_attn_decode_step then).  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  All calls
+ * both sizes (use path_attn_decode_step then).  The first call in each CUDA
+ * context looks up the array's device address (cudaGetSymbolAddress) with
+ * that context current and caches it for that context (a context made after
+ * a device reset gets a fresh lookup); make that first call before any
+ * stream capture.  All calls
  * share the one array, which keeps the last call's contents, so calls that
  * overlap on the GPU (different streams, or different host threads on the
  * same device) race with each other: serialise them.  Nothing is allocated
