@@ -65,6 +65,11 @@ def backward_flops(B, H, L, d, C=CHUNK):
     return 2 * C * C * d * (9 * pairs + 49 * N) * B * H
 
 
+# DRAM read + write bytes per cached key of decode_split_kernel<128, fox>, from
+# ncu on B16 H12 with 8195 cached tokens (1,573,440 keys per launch)
+DECODE_TRAFFIC_PER_KEY = {False: (805.74e6 + 354.32e6) / 1573440,
+                          True: (812.07e6 + 350.02e6) / 1573440}
+
 # DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
 SCAN_TRAFFIC_B2 = 145.389312e6 + 12.049664e6
 
@@ -236,8 +241,7 @@ def prefill_block(wlk, steps, warmup, ws, peaks, seed=0, sampler=None):
                      "achieved": scan_tf, "peak": peak, "unit": "TFLOP/s",
                      "frac": scan_tf / peak,
                      # DRAM bytes per launch: ncu read + write of this kernel on the B2 case,
-                     # scaled by the batch (profiles/scan_prep_b2h12l4096.md); the headline B8
-                     # launch only
+                     # scaled by the batch; the headline B8 launch only
                      "traffic": (SCAN_TRAFFIC_B2 * B / 2
                                  if (H, L, d) == (12, 4096, 128) and not wlk.fox else None),
                      "peak_source": peaks["source"] + " bf16 dense (burst)"},
@@ -363,9 +367,11 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1)]
     evs[0].record(stream)
     bytes_total = 0
+    keys_total = 0
     for i in range(nsteps):
         step(toks[warmup + i], t)
         bytes_total += 3 * B * H * t * d * 2  # read K, write K, read V
+        keys_total += B * H * t
         if fox:
             bytes_total += B * H * t * 4  # read each key's forget-gate prefix
         t += 1
@@ -382,7 +388,11 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
            "steps": nsteps, "hbm_gbs": gbs * ws,
            "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel",
                         "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                        "frac": gbs / peak, "traffic": None,
+                        "frac": gbs / peak,
+                        # ncu dram read + write per key of decode_split_kernel (B16 H12,
+                        # cache 8192) times the mean keys of one timed step
+                        "traffic": (DECODE_TRAFFIC_PER_KEY[fox] * keys_total / nsteps
+                                    if d == 128 else None),
                         "peak_source": peaks["source"] + " copy bandwidth"}}
     del kc, vc, fc
     torch.cuda.empty_cache()
@@ -497,6 +507,13 @@ def main():
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the prefill backward on the headline shape and print its "
                          "object (for profiler captures; not the bench line)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode workload (PaTH, or PaTH-FoX with --fox) and "
+                         "print its object (for profiler captures; not the bench line)")
+    ap.add_argument("--fox", action="store_true", help="with --decode-only: the PaTH-FoX step")
+    ap.add_argument("--decode-prefix", type=int, default=None,
+                    help="override the decode workload's cached tokens (smaller cases for "
+                         "profiler captures; the default is 65536)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the headline workload's batch (smaller cases for "
                          "profiler captures; the default is the headline B8)")
@@ -549,6 +566,17 @@ def main():
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
 
+    if args.decode_only:
+        dw = wl.DECODE_64K
+        if args.decode_prefix:
+            dw = dataclasses.replace(dw, prefix_len=args.decode_prefix,
+                                     name=dw.name.replace("65536", str(args.decode_prefix)))
+        res = decode_block(dw, steps, warmup, ws, peaks, fox=args.fox)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
     if args.backward_only:
         res = backward_block(head, steps, warmup, ws, peaks)
         if rank == 0:

@@ -33,3 +33,17 @@ def oracle_prefill(x, rows=None, scale=None):
 
 def max_err(a, b):
     return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def record_margin(test, **values):
+    """Prints a measured parity margin (the largest error a test saw next to
+    its tolerance) and, when the environment variable PATH_ATTN_MARGINS
+    names a file, appends it there as one JSON line."""
+    import json
+    import os
+    line = json.dumps({"test": test, **values}, sort_keys=True)
+    print("margin", line, flush=True)
+    path = os.environ.get("PATH_ATTN_MARGINS")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")

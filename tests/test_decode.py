@@ -9,7 +9,7 @@ import torch
 import oracle
 import dependent_positional_attention_gb300 as pa
 from dependent_positional_attention_gb300 import workloads as wl
-from helpers import max_err, to64
+from helpers import max_err, record_margin, to64
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -17,6 +17,10 @@ DEV = torch.device("cuda:0")
 
 
 def run_case(B, H, d, L0, steps, seed, cap=None, heads=None, gen_device="cpu"):
+    """Builds GPU and oracle caches for L0 prefilled tokens, runs `steps`
+    decode steps on both and returns (cache build error in bf16 ulps, the
+    max|dout| of every step, GPU k cache, GPU v cache, tokens, oracle k
+    cache)."""
     cap = cap or (L0 + steps)
     x = wl.prefill_inputs(B, H, max(L0, 1), d, "bf16", seed=seed, device=gen_device)
     toks = [wl.decode_token(B, H, d, "bf16", seed=10_000 + seed + t, device=gen_device)
@@ -52,7 +56,7 @@ def run_case(B, H, d, L0, steps, seed, cap=None, heads=None, gen_device="cpu"):
         torch.cuda.synchronize()
         errs.append(max_err(to64(flat(out)[sel]), ro))
     assert pa.path_attn_device_status() == 0
-    return cache_err, errs, kc, vc, toks
+    return cache_err, errs, kc, vc, toks, ok
 
 
 @pytest.mark.parametrize("L0", [1, 63, 1000, 2100])
@@ -68,7 +72,7 @@ def test_decode_head_dim_64():
 
 
 def test_decode_empty_cache_returns_v():
-    _, errs, kc, vc, toks = run_case(1, 2, 128, 0, 1, seed=6, cap=4)
+    _, errs, kc, vc, toks, _ = run_case(1, 2, 128, 0, 1, seed=6, cap=4)
     assert max(errs) <= TOL
     # softmax over the single new key: out == v_t, and slot 0 holds k_t / v_t
     v = toks[0]["v"].to(DEV)
@@ -88,14 +92,39 @@ def test_decode_rejects_full_cache():
         pa.path_attn_decode_step(kc, kc.clone(), 8, t, t, t, t, b)
 
 
+def cache_drift(kc, ok, heads, n):
+    """Drift of the GPU key cache (re-rounded to bf16 after every update) from
+    the oracle's fp64 cache over the first n slots of the given heads: the
+    largest absolute difference and the largest per-key relative difference
+    |k_gpu - k_ref| / |k_ref|."""
+    BH = kc.shape[0] * kc.shape[1]
+    gk = to64(kc.reshape((BH,) + tuple(kc.shape[2:]))[heads][:, :n])
+    rk = ok[:, :n]
+    diff = np.abs(gk - rk)
+    rel = np.linalg.norm(gk - rk, axis=-1) / np.maximum(np.linalg.norm(rk, axis=-1), 1e-30)
+    return float(diff.max()), float(rel.max())
+
+
 @pytest.mark.slow
-def test_decode_full_size_sampled_heads():
-    """Decode workload shape: B16 H12 d128, 65536 cached tokens built by the
-    prefill-state builder, then 3 steps; 8 sampled (b,h) heads checked."""
+def test_decode_full_size_all_steps_sampled_heads():
+    """The decode workload in full: B16 H12 d128, 65536 cached tokens built by
+    the prefill-state builder, then all 256 steps with the benchmark's seeds;
+    8 sampled (b, h) heads compared with the oracle at every step.  The GPU
+    re-rounds every cached key to bf16 after each in-place update while the
+    oracle keeps fp64, so the error can grow with the step count; the
+    largest error over the 256 steps and the final cache drift are
+    recorded."""
     w = wl.DECODE_64K
     g = torch.Generator().manual_seed(1)
     heads = sorted(torch.randperm(w.batch * w.heads, generator=g)[:8].tolist())
-    cache_err, errs, *_ = run_case(w.batch, w.heads, w.head_dim, w.prefix_len, 3, seed=0,
-                                   cap=w.prefix_len + w.steps, heads=heads, gen_device="cuda")
+    cache_err, errs, kc, _, _, ok = run_case(w.batch, w.heads, w.head_dim, w.prefix_len,
+                                             w.steps, seed=0, cap=w.prefix_len + w.steps,
+                                             heads=heads, gen_device="cuda")
+    drift_abs, drift_rel = cache_drift(kc, ok, heads, w.prefix_len + w.steps)
+    record_margin("decode_64k_256_steps", max_dout=max(errs), tol_out=TOL,
+                  dout_first_step=errs[0], dout_last_step=errs[-1],
+                  worst_step=int(np.argmax(errs)), cache_build_ulp=cache_err,
+                  final_cache_drift_abs=drift_abs, final_cache_drift_rel=drift_rel)
     assert cache_err <= 1.0, cache_err
-    assert max(errs) <= TOL, errs
+    assert len(errs) == w.steps
+    assert max(errs) <= TOL, (int(np.argmax(errs)), max(errs))

@@ -10,7 +10,7 @@ import torch
 import oracle
 import dependent_positional_attention_gb300 as pa
 from dependent_positional_attention_gb300 import workloads as wl
-from helpers import max_err, to64
+from helpers import max_err, record_margin, to64
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -103,3 +103,57 @@ def test_fox_decode_with_open_gates_is_the_path_step():
     b = pa.path_attn_decode_step(kc2, vc2, L0, tok["q"], tok["k"], tok["v"], tok["w"], tok["beta"])
     torch.cuda.synchronize()
     assert torch.equal(a, b) and torch.equal(kc, kc2) and torch.equal(vc, vc2)
+
+
+@pytest.mark.slow
+def test_fox_decode_full_size_all_steps_sampled_heads():
+    """The decode workload with forget gates: B16 H12 d128, a PaTH-FoX cache of
+    65536 tokens (keys by the prefill-state builder, prefixes by
+    path_attn_fox_prefix), then all 256 steps with the benchmark's seeds; 8
+    sampled (b, h) heads compared with the oracle's FoX decode at every step.
+    The largest error over the steps and the final key-cache drift are
+    recorded."""
+    w = wl.DECODE_64K
+    B, H, d, L0, steps = w.batch, w.heads, w.head_dim, w.prefix_len, w.steps
+    cap = L0 + steps
+    BH = B * H
+    heads = sorted(torch.randperm(BH, generator=torch.Generator().manual_seed(2))[:8].tolist())
+    x = wl.prefill_inputs(B, H, L0, d, "bf16", seed=0, fox=True, device="cuda")
+    kc = torch.zeros((B, H, cap, d), device=DEV, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    fc = torch.zeros((B, H, cap), device=DEV, dtype=torch.float32)
+    pa.path_attn_build_kcache(x["k"], x["w"], x["beta"], kc)
+    vc[:, :, :L0] = x["v"]
+    pa.path_attn_fox_prefix(x["log_f"], fc)
+    flat = lambda t: t.reshape((BH,) + tuple(t.shape[2:]))
+    sel = lambda t: to64(flat(t)[heads])
+    ok = oracle.build_kcache(sel(x["k"]), sel(x["w"]), sel(x["beta"]), cap=cap)
+    ov = np.zeros_like(ok)
+    ov[:, :L0] = sel(x["v"])
+    lf = np.zeros((len(heads), cap))
+    lf[:, :L0] = sel(x["log_f"])
+    del x
+    errs = []
+    for t in range(steps):
+        g = wl.decode_token(B, H, d, "bf16", seed=10_000 + t, device="cuda", fox=True)
+        out = pa.path_attn_decode_step_fox(kc, vc, fc, L0 + t, g["q"], g["k"], g["v"], g["w"],
+                                           g["beta"], g["log_f"])
+        ro = oracle.decode_step_fox(ok, ov, lf, L0 + t,
+                                    *(sel(g[n]) for n in ("q", "k", "v", "w", "beta")),
+                                    sel(g["log_f"]))
+        torch.cuda.synchronize()
+        errs.append(max_err(sel(out), ro))
+    assert pa.path_attn_device_status() == 0
+    gk = sel(kc)
+    drift_abs = float(np.max(np.abs(gk - ok)))
+    drift_rel = float(np.max(np.linalg.norm(gk - ok, axis=-1)
+                             / np.maximum(np.linalg.norm(ok, axis=-1), 1e-30)))
+    F_ref = np.cumsum(lf, axis=1)
+    F_err = float(np.max(np.abs(sel(fc) - F_ref)))
+    record_margin("fox_decode_64k_256_steps", max_dout=max(errs), tol_out=TOL,
+                  dout_first_step=errs[0], dout_last_step=errs[-1],
+                  worst_step=int(np.argmax(errs)), final_cache_drift_abs=drift_abs,
+                  final_cache_drift_rel=drift_rel, prefix_abs_err=F_err)
+    assert len(errs) == steps
+    assert max(errs) <= TOL, (int(np.argmax(errs)), max(errs))
+    assert F_err <= 1e-5 * max(1.0, float(np.max(np.abs(F_ref))))

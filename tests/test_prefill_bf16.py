@@ -10,7 +10,7 @@ import torch
 import oracle
 import dependent_positional_attention_gb300 as pa
 from dependent_positional_attention_gb300 import workloads as wl
-from helpers import NAMES, max_err, to64
+from helpers import NAMES, max_err, record_margin, to64
 
 pytestmark = pytest.mark.gpu
 TOL_OUT, TOL_LSE = 2e-2, 1e-2
@@ -83,6 +83,8 @@ def test_full_size_sampled_rows(wname):
     n = w.sampled_rows or 64
     rows = wl.sampled_rows(w.seq_len, n)
     eo, el = run(x, rows=rows)
+    record_margin("prefill_" + wname.lower(), max_dout=eo, tol_out=TOL_OUT, max_dlse=el,
+                  tol_lse=TOL_LSE, rows_per_head=len(rows), heads=w.batch * w.heads)
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
 
 

@@ -17,7 +17,7 @@ import torch
 import oracle
 import dependent_positional_attention_gb300 as pa
 from dependent_positional_attention_gb300 import workloads as wl
-from helpers import to64
+from helpers import record_margin, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -51,10 +51,22 @@ def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None, scale=None):
 
 
 def check(got, ref, tol):
+    """Asserts every gradient's normalised error; returns, per gradient, the
+    raw elementwise max|G_gpu - G_ref|, the normalised error and max|G_ref|."""
     assert set(got) == set(ref)
+    res = {}
     for n in ref:
-        err = float(np.max(np.abs(got[n] - ref[n]))) / max(1.0, float(np.max(np.abs(ref[n]))))
+        raw = float(np.max(np.abs(got[n] - ref[n])))
+        top = float(np.max(np.abs(ref[n])))
+        err = raw / max(1.0, top)
+        res[n] = {"raw": raw, "normalised": err, "max_ref": top}
         assert err <= tol, "%s: normalised error %.3g > %.3g" % (n, err, tol)
+    return res
+
+
+def record_grads(test, res, tol):
+    record_margin(test, tol_normalised=tol,
+                  **{"%s_%s" % (n, k): v for n, r in res.items() for k, v in r.items()})
 
 
 def test_tiny_fp32():
@@ -106,7 +118,7 @@ def test_headline_shape_sampled_heads():
     (first and last) checked in full against the oracle."""
     x = wl.prefill_inputs(8, 12, 4096, 128, "bf16", seed=0)
     got, ref = run(x, heads=[0, 95])
-    check(got, ref, 2e-2)
+    record_grads("backward_4k_heads_0_95", check(got, ref, 2e-2), 2e-2)
 
 
 @pytest.mark.parametrize("L", [1, 128, 129, 700])
@@ -153,7 +165,7 @@ def test_fox_headline_shape_sampled_heads():
     checked in full."""
     x = wl.prefill_inputs(8, 12, 4096, 128, "bf16", seed=0, fox=True)
     got, ref = run(x, heads=[3, 90])
-    check(got, ref, 2e-2)
+    record_grads("backward_fox_4k_heads_3_90", check(got, ref, 2e-2), 2e-2)
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])

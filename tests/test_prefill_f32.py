@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from dependent_positional_attention_gb300 import workloads as wl
-from helpers import gpu_prefill, max_err, oracle_prefill
+from helpers import gpu_prefill, max_err, oracle_prefill, record_margin
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -22,7 +22,8 @@ def check(x, chunk=0, scale=None):
 
 def test_tiny_config_exact():
     """B1 H1 L256 d64 fp32, seed 0 (the tiny PaTH forward workload)."""
-    check(wl.workload_inputs(wl.TINY_F32, seed=0))
+    e_out, e_lse = check(wl.workload_inputs(wl.TINY_F32, seed=0))
+    record_margin("prefill_tiny_f32", max_dout=e_out, max_dlse=e_lse, tol_out=TOL, tol_lse=TOL)
 
 
 @pytest.mark.parametrize("chunk", [16, 32, 64, 128])
