@@ -392,7 +392,7 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
                         # ncu dram read + write per key of decode_split_kernel (B16 H12,
                         # cache 8192) times the mean keys of one timed step
                         "traffic": (DECODE_TRAFFIC_PER_KEY[fox] * keys_total / nsteps
-                                    if d == 128 else None),
+                                    if d == 128 and DECODE_TRAFFIC_PER_KEY[fox] else None),
                         "peak_source": peaks["source"] + " copy bandwidth"}}
     del kc, vc, fc
     torch.cuda.empty_cache()

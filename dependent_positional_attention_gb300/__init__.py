@@ -21,6 +21,9 @@ __all__ = [
     "path_attn_build_kcache", "path_attn_prefill_workspace_size",
     "path_attn_decode_workspace_size", "path_attn_build_kcache_workspace_size",
     "path_attn_device_status", "path_attn_selftest_bounded_wait", "EXPORTED_SYMBOLS",
+    "path_attn_cp_local_len", "path_attn_cp_rows", "path_attn_cp_exchange_bytes",
+    "path_attn_cp_workspace_size", "path_attn_cp_prep", "path_attn_cp_scan", "cp_all_gather",
+    "path_attention_cp",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +40,8 @@ EXPORTED_SYMBOLS = (
     "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
     "path_attn_device_status", "path_attn_selftest_bounded_wait",
     "path_attn_status_string", "path_attn_last_error", "path_attn_version",
+    "path_attn_cp_local_len", "path_attn_cp_rows", "path_attn_cp_exchange_bytes",
+    "path_attn_cp_workspace_size", "path_attn_cp_prep", "path_attn_cp_scan",
 )
 
 
@@ -105,6 +110,16 @@ def load_library(path: str | None = None):
         lib.path_attn_build_kcache_workspace_size.restype = _SZ
         lib.path_attn_build_kcache.argtypes = [pd, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP,
                                                _SZ, _VP]
+        i32 = ctypes.c_int32
+        lib.path_attn_cp_local_len.argtypes = [pd, i32, i32]
+        lib.path_attn_cp_local_len.restype = i32
+        lib.path_attn_cp_rows.argtypes = [pd, i32, i32, ctypes.POINTER(i32), i32]
+        lib.path_attn_cp_exchange_bytes.argtypes = [pd, i32]
+        lib.path_attn_cp_exchange_bytes.restype = _SZ
+        lib.path_attn_cp_workspace_size.argtypes = [pd, i32]
+        lib.path_attn_cp_workspace_size.restype = _SZ
+        lib.path_attn_cp_prep.argtypes = [pd, i32, i32] + [_VP] * 8 + [_SZ, _VP]
+        lib.path_attn_cp_scan.argtypes = [pd, i32, i32] + [_VP] * 5 + [_SZ, _VP]
         lib.path_attn_device_status.argtypes = [ctypes.c_int32]
         lib.path_attn_selftest_bounded_wait.argtypes = [ctypes.c_uint32, _VP]
         lib.path_attn_status_string.restype = ctypes.c_char_p
@@ -113,7 +128,8 @@ def load_library(path: str | None = None):
         for f in ("path_attn_prefill_fwd", "path_attn_prefill_prep", "path_attn_prefill_scan",
                   "path_attn_prefill_bwd",
                   "path_attn_decode_step", "path_attn_decode_step_noalloc",
-                  "path_attn_build_kcache",
+                  "path_attn_build_kcache", "path_attn_cp_rows", "path_attn_cp_prep",
+                  "path_attn_cp_scan",
                   "path_attn_device_status", "path_attn_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         if path is None:
@@ -451,3 +467,139 @@ def path_attn_device_status(clear=True):
 
 def path_attn_selftest_bounded_wait(limit_us=1000, stream=None):
     _check(load_library().path_attn_selftest_bounded_wait(int(limit_us), _stream(stream)))
+
+
+# ------------------------------------------------------ sequence-sharded prefill
+
+def _cp_desc(batch, heads, seq_len, scale):
+    if scale is None:
+        scale = 128 ** -0.5
+    return PrefillDesc(batch, heads, seq_len, 128, PATH_BF16, float(scale), 0)
+
+
+def path_attn_cp_local_len(batch, heads, seq_len, world, rank):
+    """Rows of the sequence that rank `rank` of `world` holds (see
+    path_attn_cp_local_len in include/path_attn.h)."""
+    n = load_library().path_attn_cp_local_len(ctypes.byref(_cp_desc(batch, heads, seq_len, None)),
+                                              int(world), int(rank))
+    if n < 0:
+        _check(PATH_ERR_INVALID_ARG)
+    return int(n)
+
+
+def path_attn_cp_rows(batch, heads, seq_len, world, rank):
+    """Global positions of the rank's local rows, in local order (a CPU int64
+    tensor); index the sequence dimension with it to shard a tensor."""
+    import torch
+    lib = load_library()
+    desc = _cp_desc(batch, heads, seq_len, None)
+    n = path_attn_cp_local_len(batch, heads, seq_len, world, rank)
+    buf = (ctypes.c_int32 * max(n, 1))()
+    _check(lib.path_attn_cp_rows(ctypes.byref(desc), int(world), int(rank), buf, n))
+    return torch.tensor(list(buf)[:n], dtype=torch.int64)
+
+
+def path_attn_cp_exchange_bytes(batch, heads, seq_len, world):
+    return int(load_library().path_attn_cp_exchange_bytes(
+        ctypes.byref(_cp_desc(batch, heads, seq_len, None)), int(world)))
+
+
+def path_attn_cp_workspace_size(batch, heads, seq_len, world):
+    return int(load_library().path_attn_cp_workspace_size(
+        ctypes.byref(_cp_desc(batch, heads, seq_len, None)), int(world)))
+
+
+def path_attn_cp_prep(q, k, v, w, beta, seq_len, world, rank, log_f=None, scale=None,
+                      exchange=None, workspace=None, stream=None):
+    """Step 1 of the sharded prefill (see path_attn_cp_prep in
+    include/path_attn.h).  q, k, v, w: the rank's local rows [B, H, Lr, 128]
+    bf16; beta: float32 [B, H, Lr]; log_f: float32 [B, H, seq_len] of the
+    whole sequence (PaTH-FoX) or None.  Returns (exchange, workspace): the
+    rank's exchange block (uint8) to all-gather, and the workspace to hand to
+    path_attn_cp_scan."""
+    import torch
+    lib = load_library()
+    B, H, Lr, d = q.shape
+    n = path_attn_cp_local_len(B, H, seq_len, world, rank)
+    if Lr != n or d != 128:
+        raise PathAttnError(PATH_ERR_INVALID_ARG, "q has shape %s, rank %d of %d holds [%d, %d, "
+                            "%d, 128]" % (tuple(q.shape), rank, world, B, H, n))
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (w, "w")):
+        _need(t, nm, (B, H, Lr, 128), torch.bfloat16)
+    _need(beta, "beta", (B, H, Lr), torch.float32)
+    if log_f is not None:
+        _need(log_f, "log_f", (B, H, seq_len), torch.float32)
+    desc = _cp_desc(B, H, seq_len, scale)
+    if exchange is None:
+        exchange = torch.empty(path_attn_cp_exchange_bytes(B, H, seq_len, world),
+                               device=q.device, dtype=torch.uint8)
+    if workspace is None:
+        workspace = torch.empty(path_attn_cp_workspace_size(B, H, seq_len, world),
+                                device=q.device, dtype=torch.uint8)
+    ptr = (lambda t: _ptr(t) if t.numel() else None)
+    _check(lib.path_attn_cp_prep(
+        ctypes.byref(desc), int(world), int(rank), ptr(q), ptr(k), ptr(v), ptr(w), ptr(beta),
+        _ptr(log_f), _ptr(exchange), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return exchange, workspace
+
+
+def path_attn_cp_scan(exchange_all, workspace, batch, heads, seq_len, world, rank, log_f=None,
+                      out=None, lse=None, scale=None, stream=None):
+    """Step 3 of the sharded prefill (see path_attn_cp_scan in
+    include/path_attn.h): exchange_all holds the world exchange blocks in rank
+    order.  Returns (out [B, H, Lr, 128] bf16, lse [B, H, Lr] float32)."""
+    import torch
+    lib = load_library()
+    n = path_attn_cp_local_len(batch, heads, seq_len, world, rank)
+    exb = path_attn_cp_exchange_bytes(batch, heads, seq_len, world)
+    if exchange_all.numel() * exchange_all.element_size() != world * exb:
+        raise PathAttnError(PATH_ERR_INVALID_ARG, "exchange_all must hold %d bytes" % (world * exb))
+    dev = exchange_all.device
+    if out is None:
+        out = torch.empty((batch, heads, n, 128), device=dev, dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((batch, heads, n), device=dev, dtype=torch.float32)
+    if n:
+        _need(out, "out", (batch, heads, n, 128), torch.bfloat16)
+        _need(lse, "lse", (batch, heads, n), torch.float32)
+    if log_f is not None:
+        _need(log_f, "log_f", (batch, heads, seq_len), torch.float32)
+    desc = _cp_desc(batch, heads, seq_len, scale)
+    _check(lib.path_attn_cp_scan(
+        ctypes.byref(desc), int(world), int(rank), _ptr(log_f), _ptr(exchange_all),
+        _ptr(out) if n else None, _ptr(lse) if n else None, _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, lse
+
+
+def cp_all_gather(exchange, world, group=None):
+    """The exchange step of the sharded prefill: every rank's exchange block,
+    gathered in rank order into one buffer (torch.distributed all-gather; over
+    NCCL for CUDA tensors)."""
+    import torch
+    import torch.distributed as dist
+    buf = torch.empty(world * exchange.numel(), device=exchange.device, dtype=exchange.dtype)
+    if world == 1:
+        buf.copy_(exchange)
+        return buf
+    try:
+        dist.all_gather_into_tensor(buf, exchange, group=group)
+    except (RuntimeError, NotImplementedError):
+        # backends without a flat all-gather: the list form into views of buf
+        dist.all_gather(list(buf.chunk(world)), exchange, group=group)
+    return buf
+
+
+def path_attention_cp(q, k, v, w, beta, seq_len, log_f=None, scale=None, group=None):
+    """Sequence-sharded PaTH / PaTH-FoX prefill on the ranks of a
+    torch.distributed process group (one GPU per rank): each rank passes its
+    local rows (path_attn_cp_rows) and gets their outputs back.  Returns
+    (out, lse) for the local rows."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    B, H = q.shape[:2]
+    exchange, ws = path_attn_cp_prep(q, k, v, w, beta, seq_len, world, rank, log_f=log_f,
+                                     scale=scale)
+    gathered = cp_all_gather(exchange, world, group)
+    return path_attn_cp_scan(gathered, ws, B, H, seq_len, world, rank, log_f=log_f, scale=scale)

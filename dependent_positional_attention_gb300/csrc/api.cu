@@ -254,6 +254,69 @@ path_status_t plan_kcache(const path_prefill_desc_t *desc, KcachePlan *p) {
     return ok();
 }
 
+// Sequence-sharded prefill: the partition of the N chunks over `world`
+// ranks (ChunkMap) and one rank's local sizes and workspace.
+struct CpPlan {
+    int BH, L, Lp, N, nb, world, rank;
+    int nloc;    // valid local chunks (a prefix of the rank's 2*nb)
+    int Lr;      // valid local rows
+    int Lq;      // padded local rows, 2 * nb * 128
+    ChunkMap cm;
+    size_t off_Qh, off_OD, off_LSD, off_F, total;  // workspace
+    size_t section;   // bytes of one of the three sections of an exchange block
+    size_t exchange;  // bytes of one rank's exchange block
+};
+
+path_status_t plan_cp(const path_prefill_desc_t *desc, int32_t world, int32_t rank, CpPlan *p) {
+    path_status_t st = check_prefill_desc(desc);
+    if (st != PATH_OK) return st;
+    if (desc->dtype != PATH_BF16 || desc->head_dim != 128 ||
+        (desc->chunk != 0 && desc->chunk != 128))
+        return fail(PATH_ERR_UNSUPPORTED,
+                    "the sharded prefill needs PATH_BF16, head_dim 128 and chunk 0 or 128");
+    if (world < 1 || world > 4096) return fail(PATH_ERR_INVALID_ARG, "world must be in 1..4096");
+    if (rank < 0 || rank >= world) return fail(PATH_ERR_INVALID_ARG, "rank must be in [0, world)");
+    p->BH = desc->batch * desc->heads;
+    p->L = desc->seq_len;
+    p->N = (p->L + 127) / 128;
+    if ((long long)p->N * 128 > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
+    p->Lp = p->N * 128;
+    p->world = world;
+    p->rank = rank;
+    p->nb = (p->N + 2 * world - 1) / (2 * world);
+    p->cm = ChunkMap{world, rank, p->nb};
+    p->Lq = 2 * p->nb * 128;
+    // valid local chunks: those whose global chunk exists (they form a prefix)
+    p->nloc = 0;
+    p->Lr = 0;
+    for (int i = 0; i < 2 * p->nb; ++i) {
+        const int c = p->cm.global_of_local(i);
+        if (c >= p->N) break;
+        ++p->nloc;
+        p->Lr += (c + 1) * 128 <= p->L ? 128 : p->L - c * 128;
+    }
+    const size_t rows = (size_t)p->BH * p->Lq;
+    size_t off = 0;
+    p->off_Qh = off; off = align_up(off + rows * 128 * 2, 256);
+    p->off_OD = off; off = align_up(off + rows * 128 * 2, 256);
+    p->off_LSD = off; off = align_up(off + rows * 4, 256);
+    p->off_F = off; off = align_up(off + (size_t)p->BH * p->Lp * 4, 256);
+    p->total = off;
+    p->section = rows * 128 * 2;
+    p->exchange = 3 * p->section;
+    return ok();
+}
+
+// A prep over every chunk of the sequence on this GPU (no sharding).
+void set_whole_sequence(PrepTcArgs &ta, int N, int L, int Lp) {
+    ta.cm = ChunkMap{1, 0, N};
+    ta.nloc = N;
+    ta.Lin = L;
+    ta.Lq = Lp;
+    ta.copy_v = 0;
+    ta.pm_transposed = 1;
+}
+
 template <class T> T *at(void *base, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(base) + off);
 }
@@ -537,12 +600,14 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
                          encode_tmap_bf16_3d(&maps.od, at<char>(workspace, p.off_Sd), 128, p.Lp,
                                              p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+        memset(&maps.vx, 0, sizeof maps.vx);
         PrepTcArgs ta;
         ta.beta = beta;
         ta.F = log_f ? at<float>(workspace, p.off_F) : nullptr;
         ta.scale = desc->scale;
         ta.LSD = at<float>(workspace, p.off_Sd + (size_t)p.BH * p.Lp * 128 * 2);
         ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        set_whole_sequence(ta, p.N, p.L, p.Lp);
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
@@ -602,6 +667,8 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
                                                  (size_t)p.BH * p.Lp * 128 * 2);
         ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
         ta.scale = desc->scale; ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        ta.cm = ChunkMap{1, 0, p.N};
+        ta.nloc = p.N; ta.Lq = p.Lp; ta.Lout = p.L; ta.zs = p.BH;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
@@ -721,12 +788,15 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+        memset(&pm_maps.vx, 0, sizeof pm_maps.vx);
         PrepTcArgs ta;
         ta.beta = beta;
         ta.F = nullptr;
         ta.scale = desc->scale;
         ta.LSD = reinterpret_cast<float *>(od + (size_t)p.BH * p.Lp * 128 * 2);
         ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        set_whole_sequence(ta, p.N, p.L, p.Lp);
+        ta.pm_transposed = 0;  // the backward's chain product reads Pm itself
         ta.err = error_flag_ptr();
         s = cuda_status(launch_prep_tc(pm_maps, ta, sms, st), "tensor-core prep launch");
         if (s != PATH_OK) return s;
@@ -920,6 +990,142 @@ path_status_t path_attn_build_kcache(const path_prefill_desc_t *desc, const void
         if (s != PATH_OK) return s;
     }
     return ok();
+}
+
+int32_t path_attn_cp_local_len(const path_prefill_desc_t *desc, int32_t world, int32_t rank) {
+    CpPlan p;
+    if (plan_cp(desc, world, rank, &p) != PATH_OK) return -1;
+    return p.Lr;
+}
+
+path_status_t path_attn_cp_rows(const path_prefill_desc_t *desc, int32_t world, int32_t rank,
+                                int32_t *rows, int32_t capacity) {
+    CpPlan p;
+    path_status_t s = plan_cp(desc, world, rank, &p);
+    if (s != PATH_OK) return s;
+    if (p.Lr > 0 && !rows) return fail(PATH_ERR_INVALID_ARG, "rows is NULL");
+    if (capacity < p.Lr)
+        return fail(PATH_ERR_INVALID_ARG, "rows holds %d entries, the rank has %d rows", capacity,
+                    p.Lr);
+    int n = 0;
+    for (int i = 0; i < p.nloc; ++i) {
+        const int c = p.cm.global_of_local(i);
+        for (int o = 0; o < 128 && c * 128 + o < p.L; ++o) rows[n++] = c * 128 + o;
+    }
+    return ok();
+}
+
+size_t path_attn_cp_exchange_bytes(const path_prefill_desc_t *desc, int32_t world) {
+    CpPlan p;
+    if (plan_cp(desc, world, 0, &p) != PATH_OK) return 0;
+    return p.exchange;
+}
+
+size_t path_attn_cp_workspace_size(const path_prefill_desc_t *desc, int32_t world) {
+    CpPlan p;
+    if (plan_cp(desc, world, 0, &p) != PATH_OK) return 0;
+    return p.total;
+}
+
+path_status_t path_attn_cp_prep(const path_prefill_desc_t *desc, int32_t world, int32_t rank,
+                                const void *q, const void *k, const void *v, const void *w,
+                                const float *beta, const float *log_f, void *exchange,
+                                void *workspace, size_t workspace_bytes, path_stream_t stream) {
+    CpPlan p;
+    path_status_t s = plan_cp(desc, world, rank, &p);
+    if (s != PATH_OK) return s;
+    const void *req[] = {q, k, v, w, beta, exchange, workspace};
+    const char *names[] = {"q", "k", "v", "w", "beta", "exchange", "workspace"};
+    for (int i = 0; i < 7; ++i) {
+        if (i < 5 && p.Lr == 0) continue;  // a rank without rows reads no input
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (log_f && !aligned16(log_f)) return fail(PATH_ERR_INVALID_ARG, "log_f is not 16-byte aligned");
+    if (workspace_bytes < p.total)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.total);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *F = at<float>(workspace, p.off_F);
+    if (log_f) {
+        // prefix sums over the whole sequence: the scan needs them at every chunk
+        s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
+        if (s != PATH_OK) return s;
+    }
+    if (p.nloc == 0) return ok();
+    char *ex = static_cast<char *>(exchange);
+    PrepTcMaps maps;
+    const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.Lr, p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.k, k, 128, p.Lr, p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.w, w, 128, p.Lr, p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.v, v, 128, p.Lr, p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.qh, at<char>(workspace, p.off_Qh), 128, p.Lq,
+                                         p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.od, at<char>(workspace, p.off_OD), 128, p.Lq,
+                                         p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.kh, ex, 128, p.Lq, p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.pm, ex + p.section, 128, p.Lq, p.BH, 64, 128) &&
+                     encode_tmap_bf16_3d(&maps.vx, ex + 2 * p.section, 128, p.Lq, p.BH, 64, 128);
+    if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+    PrepTcArgs ta;
+    ta.beta = beta;
+    ta.F = log_f ? F : nullptr;
+    ta.scale = desc->scale;
+    ta.LSD = at<float>(workspace, p.off_LSD);
+    ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+    ta.cm = p.cm; ta.nloc = p.nloc; ta.Lin = p.Lr; ta.Lq = p.Lq; ta.copy_v = 1;
+    ta.pm_transposed = 1;
+    ta.err = error_flag_ptr();
+    const int sms = num_sms();
+    if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+    return cuda_status(launch_prep_tc(maps, ta, sms, st), "tensor-core prep launch");
+}
+
+path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, int32_t rank,
+                                const float *log_f, const void *exchange_all, void *out,
+                                float *lse, void *workspace, size_t workspace_bytes,
+                                path_stream_t stream) {
+    CpPlan p;
+    path_status_t s = plan_cp(desc, world, rank, &p);
+    if (s != PATH_OK) return s;
+    if (p.nloc == 0) return ok();
+    const void *req[] = {exchange_all, out, workspace};
+    const char *names[] = {"exchange_all", "out", "workspace"};
+    for (int i = 0; i < 3; ++i) {
+        if (!req[i]) return fail(PATH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(req[i]))
+            return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+    if (workspace_bytes < p.total)
+        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    p.total);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const char *ex = static_cast<const char *>(exchange_all);
+    // the gathered blocks: [world][Kh, Pm, V][BH][Lq][128], so chunk c of head
+    // bh in section s sits at z = owner * 3 * BH + s * BH + bh
+    const uint64_t zall = (uint64_t)world * 3 * p.BH;
+    FlashTcMaps maps;
+    const bool enc =
+        encode_tmap_bf16_3d(&maps.qh, at<char>(workspace, p.off_Qh), 128, p.Lq, p.BH, 64, 128) &&
+        encode_tmap_bf16_3d(&maps.kh, ex, 128, p.Lq, zall, 64, 128) &&
+        encode_tmap_bf16_3d(&maps.pm, ex + p.section, 128, p.Lq, zall - p.BH, 64, 128) &&
+        encode_tmap_bf16_3d(&maps.v, ex + 2 * p.section, 128, p.Lq, zall - 2 * p.BH, 64, 128);
+    if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+    FlashTcArgs ta;
+    ta.OD = at<const __nv_bfloat16>(workspace, p.off_OD);
+    ta.LSD = at<const float>(workspace, p.off_LSD);
+    ta.F = log_f ? at<const float>(workspace, p.off_F) : nullptr;
+    ta.out = static_cast<__nv_bfloat16 *>(out);
+    ta.lse = lse;
+    ta.scale = desc->scale;
+    ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+    ta.cm = p.cm; ta.nloc = p.nloc; ta.Lq = p.Lq; ta.Lout = p.Lr; ta.zs = 3 * p.BH;
+    ta.err = error_flag_ptr();
+    const int sms = num_sms();
+    if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+    return cuda_status(launch_flash_tc(maps, ta, sms, st), "tensor-core scan launch");
 }
 
 path_status_t path_attn_device_status(int32_t clear) {

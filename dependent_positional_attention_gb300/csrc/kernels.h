@@ -177,21 +177,47 @@ struct KcacheArgs {
 size_t kcache_smem(int d, int C);
 cudaError_t launch_kcache_sweep(const KcacheArgs &a, cudaStream_t st);
 
+// Where each chunk of the sequence lives when the prefill is sharded over
+// `world` ranks (sequence / context parallelism).  The N chunks form 2*world
+// blocks of nb = ceil(N / (2*world)) chunks; rank r owns blocks r and
+// 2*world-1-r (a zigzag, so that every rank gets early and late query chunks
+// and the causal work is balanced).  A rank's local chunk i (its rows start
+// at local row 128*i) is global chunk global_of_local(i); a global chunk c
+// lives on rank owner at local index idx (home_of_global).  One GPU is
+// world = 1, rank = 0, nb = N: local and global chunks coincide.
+struct ChunkMap {
+    int world, rank, nb;
+    __host__ __device__ int global_of_local(int i) const {
+        return i < nb ? rank * nb + i : (2 * world - 1 - rank) * nb + (i - nb);
+    }
+    __host__ __device__ void home_of_global(int c, int &owner, int &idx) const {
+        const int blk = c / nb;
+        owner = blk < world ? blk : 2 * world - 1 - blk;
+        idx = (blk < world ? 0 : nb) + (c - blk * nb);
+    }
+};
+
 // Tensor-core scan (bf16, head_dim 128, chunk 128).  Maps: 3-D bf16 tensors
 // [BH][rows][128] in 64 x 128 boxes with 128-byte swizzle.
 struct FlashTcMaps {
-    CUtensorMap qh, kh, pm;  // workspace, rows = Lp (pm: per chunk a 128 x 128 matrix)
-    CUtensorMap v;           // input, rows = L
+    CUtensorMap qh;          // local boundary-adjusted queries, rows = Lq
+    // key side of every chunk: Kh, Pm (per chunk a 128 x 128 matrix) and V,
+    // chunk c at row 128 * idx and z = owner * zs + bh (ChunkMap)
+    CUtensorMap kh, pm, v;
 };
 
 struct FlashTcArgs {
-    const __nv_bfloat16 *OD;  // [BH][Lp][128] each chunk's own attention output (prep)
-    const float *LSD;         // [BH][Lp] its log-sum-exp
-    const float *F;
-    __nv_bfloat16 *out;
-    float *lse;
+    const __nv_bfloat16 *OD;  // [BH][Lq][128] each local chunk's own attention output (prep)
+    const float *LSD;         // [BH][Lq] its log-sum-exp
+    const float *F;           // [BH][Lp] FoX prefix sums over the whole sequence, or null
+    __nv_bfloat16 *out;       // [BH][Lout][128] local rows
+    float *lse;               // [BH][Lout] or null
     float scale;
-    int BH, L, Lp, N;
+    int BH, L, Lp, N;         // whole sequence: length, padded length, chunks
+    ChunkMap cm;
+    int nloc;                 // local chunks (query tiles) per head
+    int Lq, Lout;             // local padded rows, local rows
+    int zs;                   // z stride between owners in the key-side maps
     uint32_t *err;
 };
 
@@ -202,18 +228,26 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
 // v inputs ([BH][L][128]) and over the Qh, Kh, Pm, OD outputs ([BH][Lp][128]),
 // all with 64 x 128 boxes and the 128-byte swizzle.
 struct PrepTcMaps {
-    CUtensorMap q, k, w, v;
-    CUtensorMap qh, kh, pm, od;
+    CUtensorMap q, k, w, v;      // inputs, rows = Lin
+    CUtensorMap qh, kh, pm, od;  // outputs, rows = Lq
+    CUtensorMap vx;              // copy of V's tiles (sharded prefill), rows = Lq
 };
 
 struct PrepTcArgs {
-    const float *beta;
-    const float *F;      // FoX prefix sums [BH][Lp] (natural log units) or null
+    const float *beta;   // [BH][Lin]
+    const float *F;      // FoX prefix sums [BH][Lp] over the whole sequence (natural log
+                         // units) or null
     float scale;
     // Qh, Kh, Pm (per chunk the 128 x 128 product I - W^T T W) and OD (each
-    // chunk's own attention output, normalised) are written through the maps.
-    float *LSD;          // [BH][Lp] log-sum-exp of the OD rows (natural log)
-    int BH, L, Lp, N;
+    // chunk's own attention output, normalised) are written through the maps,
+    // local chunk i at row 128 * i.
+    float *LSD;          // [BH][Lq] log-sum-exp of the OD rows (natural log)
+    int BH, L, Lp, N;    // whole sequence
+    ChunkMap cm;
+    int nloc;            // local chunks per head (the first nloc of the rank)
+    int Lin, Lq;         // rows per head of the inputs and of the outputs
+    int copy_v;          // also store each chunk's V tile through maps.vx
+    int pm_transposed;   // store Pm^T (the forward scan) instead of Pm (the backward)
     uint32_t *err;
 };
 

@@ -7,33 +7,38 @@
 // the online softmax starts from that state, and for every earlier chunk c
 // the carried query rows Qt (which start as the boundary-adjusted rows Qh_b)
 // give
-//     S_c = Qt Kh_c^T            (logits against boundary-adjusted keys)
-//     Qt <- Qt Pm_c              (chunk product, Pm_c = I - W_c^T T_c W_c)
-//     O  += softmax-weights(S_c) V_c           (online softmax)
-// Each contraction is a 128 x 128 x 128 bf16 MMA with fp32 accumulation in
-// tensor memory.  The carried rows (after the first step) and the softmax
-// weights P are written back to tensor memory as bf16 and read from there as
-// the A operand, so that shared memory only carries the B operands: at
-// M = N = 128 an MMA with both operands in shared memory would take all of
-// its bandwidth.  Applying the whole chunk product as one d x d
-// matrix takes one MMA per chunk instead of two (Qt W^T, then X Wt) and
-// re-rounds the carried rows once per chunk rather than rounding a
-// correction term of their own size.
+//     [U_c | S_c] = Qt [Pm_c | Kh_c^T]   (carried rows through the chunk
+//                                          product, and the logits)
+//     Qt <- U_c
+//     O  += softmax-weights(S_c) V_c      (online softmax)
+// Pm_c = I - W_c^T T_c W_c is the chunk's whole transition as one d x d
+// matrix; the prep stores it transposed, so that Pm_c^T and Kh_c stack into
+// one 256-row K-major operand and U_c and S_c come from ONE 128 x 256 x 128
+// MMA (eight tcgen05.mma of N = 256): half the instructions of two N = 128
+// products, which matters because the issuing thread shares its schedulers
+// with the softmax and carried-query warps (a 128 x 128 x 16 instruction
+// then issues in about 84 cycles instead of 64, while an N = 256 one still
+// runs at its 128).  P V is a 128 x 128 x 128 MMA.  fp32 accumulation in
+// tensor memory throughout.  The carried rows (after the first step) and the
+// softmax weights P are written back to tensor memory as bf16 and read from
+// there as the A operand, so that shared memory only carries B operands.
 //
 // One CTA per SM (persistent), tiles ordered by decreasing work.  Warp roles:
-//   warps 0-3   carried-query warpgroup: Qt Pm_c (TMEM, fp32) -> bf16 (TMEM)
+//   warps 0-3   carried-query warpgroup: U_c (TMEM, fp32) -> Qt bf16 (TMEM)
 //   warps 4-7   softmax warpgroup: logits, online softmax with lazy rescale
 //               of O, P -> bf16 (TMEM), epilogue (out, lse)
-//   warp 8      TMA producer: Qh_b, then a 6-slot ring of Pm_c, Kh_c, V
+//   warp 8      TMA producer: Qh_b, then two rings: [Pm_c^T | Kh_c] pairs
+//               (64 KB slots) and V_c (32 KB slots)
 //   warp 9      MMA issuer (one thread) and TMEM owner; warps 10-11 idle
 // Registers are rebalanced at start (setmaxnreg): the producer/MMA group
 // drops to 120 per thread, the two compute groups rise to 192 (the launch's
 // 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512).
-// MMA issue order per step c: U_c = Qt Pm_c (the critical chain), S_c,
-// PV_{c+1}; the PV of a chunk runs one step late so the softmax has a full
-// step of slack.  Chunk-0 tiles need no scan: the softmax group copies the
-// prep's result.  TMEM columns: [0,128) U, [128,192) Qt (bf16 pairs),
-// [192,256) P (bf16 pairs), [256,384) S, [384,512) O.
+// MMA issue order per step c: [U|S]_c, then PV_{c+1} (one step late, so the
+// softmax has a full step of slack).  The first step of a tile reads Qh_b
+// from shared memory; the last (c = 0) needs no U and computes S_0 alone.
+// Chunk-0 tiles need no scan: the softmax group copies the prep's result.
+// TMEM columns: [0,128) U, [128,256) S, [256,320) Qt (bf16 pairs),
+// [320,384) P (bf16 pairs), [384,512) O.
 // Every wait is bounded; on timeout the kernel sets the device error flag,
 // drains its outstanding copies and MMAs, frees TMEM and exits.
 
@@ -45,28 +50,35 @@ namespace path {
 namespace {
 
 constexpr int kD = 128, kC = 128;
-constexpr int kSlots = 6;
-constexpr int kTileBytes = kC * kD * 2;  // 32 KB bf16 tile
+constexpr int kPairSlots = 2, kVSlots = 2;
+constexpr int kTileBytes = kC * kD * 2;       // 32 KB bf16 tile
+constexpr int kPairBytes = 2 * kTileBytes;    // [Pm^T | Kh] as 256 rows
 constexpr int kThreadsTC = 384;  // 3 warpgroups
-constexpr uint32_t kColU = 0, kColQt = 128, kColP = 192, kColS = 256, kColO = 384;
+constexpr uint32_t kColU = 0, kColS = 128, kColQt = 256, kColP = 320, kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// dynamic shared memory layout (offsets from a 1024-aligned base)
+// dynamic shared memory layout (offsets from a 1024-aligned base).  A pair
+// slot holds the 256-row K-major operand [Pm^T ; Kh] as two 64-column
+// sub-tiles of 256 rows: [Pm^T k0-63 | Kh k0-63 | Pm^T k64-127 | Kh k64-127],
+// 16 KB each, so that rows 0-255 of each sub-tile are 8-row groups 1024 bytes
+// apart and the sub-tiles are 32 KB apart.
 constexpr int kOffQb = 0;
-constexpr int kOffRing = kOffQb + kTileBytes;
-constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+constexpr int kOffPair = kOffQb + kTileBytes;
+constexpr int kOffV = kOffPair + kPairSlots * kPairBytes;
+constexpr int kOffBar = kOffV + kVSlots * kTileBytes;
 
 struct Bars {
-    uint64_t full[kSlots], empty[kSlots];
-    uint64_t qb_tma_full, qb_empty, u_done, qb_free, qb_conv_full;
-    uint64_t s_full, s_empty, p_full, o_done, drain;
+    uint64_t pair_full[kPairSlots], pair_empty[kPairSlots];
+    uint64_t v_full[kVSlots], v_empty[kVSlots];
+    uint64_t qb_tma_full, qb_empty, u_full, s_full, qb_conv_full;
+    uint64_t s_empty, p_full, o_done, drain;
     uint32_t tmem_base;
     int abort_word;
     float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
 };
-// barriers/misc after the ring, plus slack to align the dynamic base to 1024
+// barriers/misc after the rings, plus slack to align the dynamic base to 1024
 constexpr int kSmemBytes = kOffBar + (int)((sizeof(Bars) + 127) / 128 * 128) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 
@@ -105,15 +117,53 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Query tile t: local chunk i (tiles in decreasing order of work: local
+// chunks run in increasing global order), head bh, global chunk b.
 struct Tile {
-    int b, bh;
+    int i, b, bh;
 };
 
-__device__ __forceinline__ Tile tile_of(int t, int BH, int N) {
+__device__ __forceinline__ Tile tile_of(int t, const FlashTcArgs &a) {
     Tile x;
-    x.b = N - 1 - t / BH;
-    x.bh = t % BH;
+    x.i = a.nloc - 1 - t / a.BH;
+    x.bh = t % a.BH;
+    x.b = a.cm.global_of_local(x.i);
     return x;
+}
+
+// Fused carried-query / logit product for step c: D[0,256) = A [Pm_c^T ; Kh_c]^T
+// over K = 128 (eight N = 256 instructions).  A is the carried rows in TMEM
+// (a_tmem) or, on a tile's first step, Qh_b in shared memory (a_lo).
+template <bool kAFromSmem>
+__device__ __forceinline__ void gemm_us(uint32_t d_tmem, uint32_t a, uint32_t pair_lo) {
+    constexpr uint32_t idesc = tc::idesc_bf16(128, 256, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t boff = (uint32_t)((kk >> 2) * (kTileBytes / 16) + (kk & 3) * 2);
+        if (kAFromSmem)
+            tc::mma_bf16_lohi(d_tmem, a + (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                              pair_lo + boff, idesc, kk > 0 ? 1u : 0u);
+        else
+            tc::mma_bf16_ta(d_tmem, a + (uint32_t)(kk * 8), pair_lo + boff, idesc,
+                            kk > 0 ? 1u : 0u);
+    }
+}
+
+// Logits alone (the last step, c = 0, has no chunk product to apply): N = 128
+// over the Kh half of a pair slot, whose sub-tiles are 32 KB apart.
+template <bool kAFromSmem>
+__device__ __forceinline__ void gemm_s(uint32_t d_tmem, uint32_t a, uint32_t kh_lo) {
+    constexpr uint32_t idesc = tc::idesc_bf16(128, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t boff = (uint32_t)((kk >> 2) * (kTileBytes / 16) + (kk & 3) * 2);
+        if (kAFromSmem)
+            tc::mma_bf16_lohi(d_tmem, a + (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                              kh_lo + boff, idesc, kk > 0 ? 1u : 0u);
+        else
+            tc::mma_bf16_ta(d_tmem, a + (uint32_t)(kk * 8), kh_lo + boff, idesc,
+                            kk > 0 ? 1u : 0u);
+    }
 }
 
 template <bool kFox>
@@ -124,23 +174,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBar);
     const uint32_t sQb = smem_u32(smem + kOffQb);
-    const uint32_t sRing = smem_u32(smem + kOffRing);
+    const uint32_t sPair = smem_u32(smem + kOffPair);
+    const uint32_t sV = smem_u32(smem + kOffV);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = a.N * a.BH;
+    const int T = a.nloc * a.BH;
     volatile int *abort_word = &bars.abort_word;
     const uint64_t lim = kWaitLimitNs;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], 1);
+        for (int s = 0; s < kPairSlots; ++s) {
+            mbar_init(&bars.pair_full[s], 1);
+            mbar_init(&bars.pair_empty[s], 1);
+        }
+        for (int s = 0; s < kVSlots; ++s) {
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
         }
         mbar_init(&bars.qb_tma_full, 1);
         mbar_init(&bars.qb_empty, 2);  // MMA commit + carried-query group
-        mbar_init(&bars.u_done, 1);
-        mbar_init(&bars.qb_free, 1);
-        mbar_init(&bars.qb_conv_full, 1);
+        mbar_init(&bars.u_full, 1);
         mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.qb_conv_full, 1);
         mbar_init(&bars.s_empty, 1);
         mbar_init(&bars.p_full, 1);
         mbar_init(&bars.o_done, 1);
@@ -165,49 +219,81 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             tc::prefetch_tmap(&maps.kh);
             tc::prefetch_tmap(&maps.pm);
             tc::prefetch_tmap(&maps.v);
-            int slot = 0;
-            uint32_t ph = 0, qe_ph = 0;
-            int last_par[kSlots];
-            for (int i = 0; i < kSlots; ++i) last_par[i] = -1;
+            int ps = 0, vs = 0;
+            uint32_t pph = 0, vph = 0, qe_ph = 0;
+            int pair_par[kPairSlots], v_par[kVSlots];
+            for (int i = 0; i < kPairSlots; ++i) pair_par[i] = -1;
+            for (int i = 0; i < kVSlots; ++i) v_par[i] = -1;
             int q_last_par = -1;
             uint32_t q_loads = 0;
             bool ok = true;
-            auto load = [&](const CUtensorMap *m, int y, int z) -> bool {
-                if (!mbar_wait(&bars.empty[slot], ph ^ 1, a.err, abort_word, lim)) return false;
-                uint8_t *dst = smem + kOffRing + slot * kTileBytes;
-                mbar_arrive_expect_tx(&bars.full[slot], kTileBytes);
-                tc::tma_load_3d(dst, m, 0, y, z, &bars.full[slot]);
-                tc::tma_load_3d(dst + kTileBytes / 2, m, 64, y, z, &bars.full[slot]);
-                last_par[slot] = (int)ph;
-                if (++slot == kSlots) {
-                    slot = 0;
-                    ph ^= 1;
+            // key side of chunk c of head bh, wherever it lives (ChunkMap):
+            // [Pm_c^T | Kh_c] into a pair slot (Kh_c alone for c = 0)
+            auto load_pair = [&](int c, int bh) -> bool {
+                int owner, idx;
+                a.cm.home_of_global(c, owner, idx);
+                const int y = idx * kC, z = owner * a.zs + bh;
+                if (!mbar_wait(&bars.pair_empty[ps], pph ^ 1, a.err, abort_word, lim)) return false;
+                uint8_t *dst = smem + kOffPair + ps * kPairBytes;
+                uint64_t *full = &bars.pair_full[ps];
+                if (c >= 1) {
+                    mbar_arrive_expect_tx(full, 2 * kTileBytes);
+                    tc::tma_load_3d(dst, &maps.pm, 0, y, z, full);
+                    tc::tma_load_3d(dst + kTileBytes / 2, &maps.kh, 0, y, z, full);
+                    tc::tma_load_3d(dst + kTileBytes, &maps.pm, 64, y, z, full);
+                    tc::tma_load_3d(dst + 3 * kTileBytes / 2, &maps.kh, 64, y, z, full);
+                } else {
+                    mbar_arrive_expect_tx(full, kTileBytes);
+                    tc::tma_load_3d(dst + kTileBytes / 2, &maps.kh, 0, y, z, full);
+                    tc::tma_load_3d(dst + 3 * kTileBytes / 2, &maps.kh, 64, y, z, full);
+                }
+                pair_par[ps] = (int)pph;
+                if (++ps == kPairSlots) {
+                    ps = 0;
+                    pph ^= 1;
+                }
+                return true;
+            };
+            auto load_v = [&](int c, int bh) -> bool {
+                int owner, idx;
+                a.cm.home_of_global(c, owner, idx);
+                const int y = idx * kC, z = owner * a.zs + bh;
+                if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, a.err, abort_word, lim)) return false;
+                uint8_t *dst = smem + kOffV + vs * kTileBytes;
+                mbar_arrive_expect_tx(&bars.v_full[vs], kTileBytes);
+                tc::tma_load_3d(dst, &maps.v, 0, y, z, &bars.v_full[vs]);
+                tc::tma_load_3d(dst + kTileBytes / 2, &maps.v, 64, y, z, &bars.v_full[vs]);
+                v_par[vs] = (int)vph;
+                if (++vs == kVSlots) {
+                    vs = 0;
+                    vph ^= 1;
                 }
                 return true;
             };
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-                const Tile tl = tile_of(t, a.BH, a.N);
+                const Tile tl = tile_of(t, a);
                 const int b = tl.b, bh = tl.bh;
                 if (b == 0) continue;
                 ok = mbar_wait(&bars.qb_empty, qe_ph ^ 1, a.err, abort_word, lim);
                 qe_ph ^= 1;
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bars.qb_tma_full, kTileBytes);
-                tc::tma_load_3d(smem + kOffQb, &maps.qh, 0, b * kC, bh, &bars.qb_tma_full);
-                tc::tma_load_3d(smem + kOffQb + kTileBytes / 2, &maps.qh, 64, b * kC, bh,
+                tc::tma_load_3d(smem + kOffQb, &maps.qh, 0, tl.i * kC, bh, &bars.qb_tma_full);
+                tc::tma_load_3d(smem + kOffQb + kTileBytes / 2, &maps.qh, 64, tl.i * kC, bh,
                                 &bars.qb_tma_full);
                 q_last_par = (int)(q_loads++ & 1);
                 for (int c = b - 1; c >= 0 && ok; --c) {
-                    if (c >= 1) ok = ok && load(&maps.pm, c * kC, bh);
-                    ok = ok && load(&maps.kh, c * kC, bh);
-                    if (c < b - 1) ok = ok && load(&maps.v, (c + 1) * kC, bh);
+                    ok = ok && load_pair(c, bh);
+                    if (c < b - 1) ok = ok && load_v(c + 1, bh);
                 }
-                ok = ok && load(&maps.v, 0, bh);
+                ok = ok && load_v(0, bh);
             }
             if (*abort_word) {
                 // let every copy this thread issued land before the CTA exits
-                for (int s = 0; s < kSlots; ++s)
-                    if (last_par[s] >= 0) mbar_wait(&bars.full[s], last_par[s], a.err, nullptr, lim);
+                for (int s = 0; s < kPairSlots; ++s)
+                    if (pair_par[s] >= 0) mbar_wait(&bars.pair_full[s], pair_par[s], a.err, nullptr, lim);
+                for (int s = 0; s < kVSlots; ++s)
+                    if (v_par[s] >= 0) mbar_wait(&bars.v_full[s], v_par[s], a.err, nullptr, lim);
                 if (q_last_par >= 0) mbar_wait(&bars.qb_tma_full, q_last_par, a.err, nullptr, lim);
             }
         }
@@ -215,78 +301,68 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int slot = 0;
-            uint32_t ph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0, pf_ph = 0;
+            int ps = 0, vs = 0;
+            uint32_t pph = 0, vph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0, pf_ph = 0;
             const uint32_t qb_lo = tc::desc_lo(sQb, false);
             bool ok = true;
-            auto take = [&](uint32_t &addr) -> bool {
-                if (!mbar_wait(&bars.full[slot], ph, a.err, abort_word, lim)) return false;
-                addr = sRing + slot * kTileBytes;
-                return true;
-            };
-            auto release = [&]() {
-                tc::mma_commit(&bars.empty[slot]);
-                if (++slot == kSlots) {
-                    slot = 0;
-                    ph ^= 1;
-                }
-            };
             // O already holds the chunk's own attention block (written by the
             // softmax group), so every PV accumulates
             auto pv = [&]() -> bool {
-                uint32_t vaddr;
-                if (!take(vaddr)) return false;
+                if (!mbar_wait(&bars.v_full[vs], vph, a.err, abort_word, lim)) return false;
                 if (!mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim)) return false;
                 pf_ph ^= 1;
                 tc::fence_after_sync();
-                tc::gemm128_ta<true>(tmem + kColO, tmem + kColP, tc::desc_lo(vaddr, true), true);
-                release();
+                tc::gemm128_ta<true>(tmem + kColO, tmem + kColP,
+                                     tc::desc_lo(sV + vs * kTileBytes, true), true);
+                tc::mma_commit(&bars.v_empty[vs]);
+                if (++vs == kVSlots) {
+                    vs = 0;
+                    vph ^= 1;
+                }
                 tc::mma_commit(&bars.o_done);
                 return true;
             };
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-                const int b = tile_of(t, a.BH, a.N).b;
+                const int b = tile_of(t, a).b;
                 if (b == 0) continue;
                 for (int c = b - 1; c >= 0 && ok; --c) {
-                    if (c == b - 1) {
+                    const bool first = (c == b - 1);
+                    // the carried rows of this step: Qh_b in shared memory, or
+                    // the carried-query group's conversion of the previous U
+                    if (first) {
                         ok = mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim);
                         qt_ph ^= 1;
                     } else {
                         ok = mbar_wait(&bars.qb_conv_full, qc_ph, a.err, abort_word, lim);
                         qc_ph ^= 1;
                     }
+                    // the softmax group has read the previous S
+                    ok = ok && mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim);
+                    se_ph ^= 1;
+                    ok = ok && mbar_wait(&bars.pair_full[ps], pph, a.err, abort_word, lim);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    // the first step reads Qh_b from shared memory, later steps
-                    // the carried rows from tensor memory
-                    const bool first = (c == b - 1);
-                    uint32_t addr;
+                    const uint32_t pair_lo = tc::desc_lo(sPair + ps * kPairBytes, false);
+                    const uint32_t kh_lo = tc::desc_lo(sPair + ps * kPairBytes + kTileBytes / 2, false);
                     if (c >= 1) {
-                        // carried rows through the chunk product: U = Qt Pm_c
-                        if (!(ok = take(addr))) break;
-                        if (first)
-                            tc::gemm128_lo<true>(tmem + kColU, qb_lo, tc::desc_lo(addr, true), false);
-                        else
-                            tc::gemm128_ta<true>(tmem + kColU, tmem + kColQt, tc::desc_lo(addr, true),
-                                                 false);
-                        release();
-                        tc::mma_commit(&bars.u_done);
+                        if (first) gemm_us<true>(tmem + kColU, qb_lo, pair_lo);
+                        else gemm_us<false>(tmem + kColU, tmem + kColQt, pair_lo);
+                    } else {
+                        if (first) gemm_s<true>(tmem + kColS, qb_lo, kh_lo);
+                        else gemm_s<false>(tmem + kColS, tmem + kColQt, kh_lo);
                     }
-                    if (!(ok = take(addr))) break;
-                    if (!(ok = mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim))) break;
-                    se_ph ^= 1;
-                    tc::fence_after_sync();
-                    if (first)
-                        tc::gemm128_lo<false>(tmem + kColS, qb_lo, tc::desc_lo(addr, false), false);
-                    else
-                        tc::gemm128_ta<false>(tmem + kColS, tmem + kColQt, tc::desc_lo(addr, false),
-                                              false);
-                    release();
+                    tc::mma_commit(&bars.pair_empty[ps]);
+                    if (++ps == kPairSlots) {
+                        ps = 0;
+                        pph ^= 1;
+                    }
+                    // separate completions for the two readers: the carried-query
+                    // group sees only the steps that produce U, the softmax group
+                    // every step, so each waits on every phase of its own barrier
+                    if (c >= 1) tc::mma_commit(&bars.u_full);
                     tc::mma_commit(&bars.s_full);
-                    // Qh_b's tile is free after the first step; the carried rows
-                    // may be overwritten once U_c and S_c (their readers) complete
+                    // Qh_b's tile is free once the first step's product completes
                     if (first) tc::mma_commit(&bars.qb_empty);
-                    if (c >= 1) tc::mma_commit(&bars.qb_free);
                     if (c < b - 1) ok = pv();
                 }
                 ok = ok && pv();
@@ -303,23 +379,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // ------------------------------------------------------------ carried query
         const int quad = warp & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t ud_ph = 0, qf_ph = 0, qt_ph = 0;
+        uint32_t uf_ph = 0, qt_ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-            const int b = tile_of(t, a.BH, a.N).b;
+            const int b = tile_of(t, a).b;
             if (b == 0) continue;
             ok = group_all(1, 128, mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim));
             if (!ok) break;
             qt_ph ^= 1;
             // second arrival on qb_empty (the first is the MMA commit after the
-            // last S of this tile): the next Qh load waits for this group too,
-            // so the Qh barrier never runs a phase ahead of it.
+            // first product of this tile): the next Qh load waits for this group
+            // too, so the Qh barrier never runs a phase ahead of it.
             named_bar(1, 128);
             if (threadIdx.x == 0) mbar_arrive(&bars.qb_empty);
             for (int c = b - 1; c >= 1; --c) {
-                ok = group_all(1, 128, mbar_wait(&bars.u_done, ud_ph, a.err, abort_word, lim));
+                // [U|S]_c complete: U is the next carried rows, and the product
+                // has read the current ones, so they may be overwritten
+                ok = group_all(1, 128, mbar_wait(&bars.u_full, uf_ph, a.err, abort_word, lim));
                 if (!ok) break;
-                ud_ph ^= 1;
+                uf_ph ^= 1;
                 tc::fence_after_sync();
                 uint32_t pk[64];
                 {
@@ -329,10 +407,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     for (int j = 0; j < 64; ++j)
                         pk[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
                 }
-                ok = group_all(1, 128, mbar_wait(&bars.qb_free, qf_ph, a.err, abort_word, lim));
-                if (!ok) break;
-                qf_ph ^= 1;
-                tc::fence_after_sync();
                 tc::tmem_st32(lane_addr + kColQt, *reinterpret_cast<const uint32_t(*)[32]>(pk));
                 tc::tmem_st32(lane_addr + kColQt + 32,
                               *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
@@ -352,21 +426,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         uint32_t sf_ph = 0, od_ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-            const Tile tl = tile_of(t, a.BH, a.N);
+            const Tile tl = tile_of(t, a);
             const int b = tl.b, bh = tl.bh;
             const float *Frow = fox ? a.F + (size_t)bh * a.Lp : nullptr;
             const float fi = fox ? Frow[b * kC + r] * kLog2e : 0.f;
-            const int row = b * kC + r;
-            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lp + row) * kD;
-            const float lsd = a.LSD[(size_t)bh * a.Lp + row];
+            const int row = b * kC + r;       // in the whole sequence
+            const int lrow = tl.i * kC + r;   // in the local rows
+            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lq + lrow) * kD;
+            const float lsd = a.LSD[(size_t)bh * a.Lq + lrow];
             if (b == 0) {
                 // the chunk attends only to itself: the prep's result is final
                 if (row < a.L) {
-                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.L + row) * kD;
+                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * kD;
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         reinterpret_cast<uint4 *>(orow)[j] = reinterpret_cast<const uint4 *>(odrow)[j];
-                    if (a.lse) a.lse[(size_t)bh * a.L + row] = lsd;
+                    if (a.lse) a.lse[(size_t)bh * a.Lout + lrow] = lsd;
                 }
                 continue;
             }
@@ -492,7 +567,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             od_ph ^= 1;
             tc::fence_after_sync();
             const float inv = 1.f / l;
-            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.L + row) * kD;
+            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * kD;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[64];
@@ -514,7 +589,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     }
                 }
             }
-            if (a.lse && row < a.L) a.lse[(size_t)bh * a.L + row] = (m + log2f(l)) * kLn2;
+            if (a.lse && row < a.L) a.lse[(size_t)bh * a.Lout + lrow] = (m + log2f(l)) * kLn2;
             tc::fence_before_sync();
         }
     }
@@ -533,7 +608,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
 cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
                             cudaStream_t st) {
-    const int T = a.N * a.BH;
+    const int T = a.nloc * a.BH;
     const int grid = T < num_sms ? T : num_sms;
     void (*kern)(const FlashTcMaps, FlashTcArgs) =
         a.F ? flash_tc_kernel<true> : flash_tc_kernel<false>;

@@ -11,7 +11,9 @@
 //   Sd = Q K^T - (M_le * Q W^T) Y^T            (within-chunk logits)
 //   Pm = I - W^T Wt                            (chunk product H_first...H_last,
 //                                               as the d x d matrix applied to
-//                                               carried query rows: q <- q Pm)
+//                                               carried query rows: q <- q Pm;
+//                                               stored transposed for the
+//                                               forward scan)
 // with M_le[r][s] = s <= r and M_gt[r][s] = s > r.  Eleven 128 x 128 x 128
 // contractions run as tcgen05 MMAs (bf16 operands, fp32 accumulation in
 // TMEM).  T is solved blockwise in fp32: the 16 x 16 diagonal blocks by
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int quad = warp & 3, half = warp >> 2;
     const int r = quad * 32 + lane;               // TMEM lane / tile row of this thread
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int total = a.N * a.BH;
+    const int total = a.nloc * a.BH;
 
     if (tid == 0) {
         mbar_init(&bars.tma, 1);
@@ -161,9 +163,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
     // W, Q and K of a chunk: issued for the first chunk here, and for each
     // following chunk as soon as the current one's output stores have read
-    // the tiles (during P9), so that the loads overlap P9-P10
+    // the tiles (during P9), so that the loads overlap P9-P10.  Inputs and
+    // outputs are addressed by local row (local chunk i at row 128 i).
     auto issue_loads = [&](int job) {
-        const int bh = job / a.N, c0 = (job % a.N) * kC;
+        const int bh = job / a.nloc, c0 = (job % a.nloc) * kC;
         tc::bulk_wait_read();
         mbar_arrive_expect_tx(&bars.tma, kTile);
         tc::tma_load_3d(smem + kOffW, &maps.w, 0, c0, bh, &bars.tma);
@@ -176,11 +179,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     };
     if (tid == 0 && blockIdx.x < total) issue_loads(blockIdx.x);
     for (int job = blockIdx.x; job < total; job += gridDim.x) {
-        const int bh = job / a.N, chunk = job % a.N;
-        const int c0 = chunk * kC;
+        const int bh = job / a.nloc, li = job % a.nloc;
+        const int chunk = a.cm.global_of_local(li);
+        const int c0 = chunk * kC;  // first row of the chunk in the whole sequence
+        const int r0 = li * kC;     // its first row in the local inputs and outputs
         const int n = min(kC, a.L - c0);
         // beta of the chunk, read ahead of its use in P2
-        const float beta_r = (tid < kC && tid < n) ? a.beta[(size_t)bh * a.L + c0 + tid] : 0.f;
+        const float beta_r = (tid < kC && tid < n) ? a.beta[(size_t)bh * a.Lin + r0 + tid] : 0.f;
         // PaTH-FoX: the chunk's prefix sums, relative to its first (the bias
         // F_i - F_j is unchanged), read ahead of their use in P9
         const float f_r = (a.F && tid < kC)
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (tid == 0) {
             const int next = job + gridDim.x;
             if (next < total) {
-                const int nbh = next / a.N, nc0 = (next % a.N) * kC;
+                const int nbh = next / a.nloc, nc0 = (next % a.nloc) * kC;
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     tc::tma_prefetch_3d(&maps.q, 64 * x, nc0, nbh);
@@ -210,6 +215,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 tc::mma_commit(&bars.mma);
                 if (!mbar_wait(&bars.mma, ph_mma, a.err, nullptr, kWaitLimitNs)) bars.ok = 0;
             }
+            // the previous chunk's OD (and V copy) stores read R1, which P2
+            // overwrites with G
+            tc::bulk_wait_read();
         }
         // Q W^T, K W^T, Q K^T are issued at the start of P3 by a thread that
         // the diagonal-block solve leaves idle, so that this thread is not held
@@ -309,8 +317,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (tid == 0) {
             // the chunk's values, for its own attention block, into the free T tile
             mbar_arrive_expect_tx(&bars.vbar, kTile);
-            tc::tma_load_3d(smem + kOffR1, &maps.v, 0, c0, bh, &bars.vbar);
-            tc::tma_load_3d(smem + kOffR1 + kTile / 2, &maps.v, 64, c0, bh, &bars.vbar);
+            tc::tma_load_3d(smem + kOffR1, &maps.v, 0, r0, bh, &bars.vbar);
+            tc::tma_load_3d(smem + kOffR1 + kTile / 2, &maps.v, 64, r0, bh, &bars.vbar);
         }
         // ---------------------------------------------------------------- P6
         {
@@ -332,8 +340,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             tc::gemm_128x128x128(tmem + kColB, sQm, sWt, true, false);  // -(M_le*QW) Wt
             tc::gemm_128x128x128(tmem + kColA, sY, sW, true, false);    // Y W
             tc::gemm_128x128x128(tmem + kColD, sQm, sY, false, true);   // QK^T - (M_le*QW) Y^T
-            tc::gemm128_lo2<true, true>(tmem + kColC, tc::desc_lo(sW, true),
-                                        tc::desc_lo(sWt, true), false);  // W^T Wt
+            // W^T Wt, or its transpose Wt^T W when the chunk product is wanted
+            // as Pm^T (rows = output dimension), the K-major layout the scan's
+            // fused carried-query/logit product reads
+            if (a.pm_transposed)
+                tc::gemm128_lo2<true, true>(tmem + kColC, tc::desc_lo(sWt, true),
+                                            tc::desc_lo(sW, true), false);
+            else
+                tc::gemm128_lo2<true, true>(tmem + kColC, tc::desc_lo(sW, true),
+                                            tc::desc_lo(sWt, true), false);
         }
         if (!mma_sync()) break;
         // ---------------------------------------------------------------- P8
@@ -380,9 +395,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (tid == 0) {
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
-                tc::tma_store_3d(&maps.qh, smem + kOffQ + x * (kTile / 2), 64 * x, c0, bh);
-                tc::tma_store_3d(&maps.kh, smem + kOffK + x * (kTile / 2), 64 * x, c0, bh);
-                tc::tma_store_3d(&maps.pm, smem + kOffW + x * (kTile / 2), 64 * x, c0, bh);
+                tc::tma_store_3d(&maps.qh, smem + kOffQ + x * (kTile / 2), 64 * x, r0, bh);
+                tc::tma_store_3d(&maps.kh, smem + kOffK + x * (kTile / 2), 64 * x, r0, bh);
+                tc::tma_store_3d(&maps.pm, smem + kOffW + x * (kTile / 2), 64 * x, r0, bh);
             }
             tc::bulk_commit();
         }
@@ -439,6 +454,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 tc::gemm_128x128x128(tmem + kColC, sQm, sT, true, false);  // P V
                 // the next chunk's W, Q, K: the P8 stores have long been issued
                 if (job + (int)gridDim.x < total) issue_loads(job + gridDim.x);
+                if (a.copy_v) {
+                    // sharded prefill: the chunk's V tile for the exchange with
+                    // the other ranks (read by TMA while the MMA reads it too)
+#pragma unroll
+                    for (int x = 0; x < 2; ++x)
+                        tc::tma_store_3d(&maps.vx, smem + kOffR1 + x * (kTile / 2), 64 * x, r0, bh);
+                    tc::bulk_commit();
+                }
             }
         }
         ph_v ^= 1;
@@ -458,7 +481,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                        pack2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv),
                        pack2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv));
             if (half == 0)
-                a.LSD[(size_t)bh * a.Lp + c0 + r] = (m_row + log2f(l_row)) * 0.6931471805599453f;
+                a.LSD[(size_t)bh * a.Lq + r0 + r] = (m_row + log2f(l_row)) * 0.6931471805599453f;
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
@@ -466,7 +489,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (tid == 0) {
 #pragma unroll
             for (int x = 0; x < 2; ++x)
-                tc::tma_store_3d(&maps.od, smem + kOffR1 + kTile + x * (kTile / 2), 64 * x, c0, bh);
+                tc::tma_store_3d(&maps.od, smem + kOffR1 + kTile + x * (kTile / 2), 64 * x, r0, bh);
             tc::bulk_commit();
         }
     }
@@ -483,7 +506,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
 cudaError_t launch_prep_tc(const PrepTcMaps &maps, const PrepTcArgs &a, int num_sms,
                            cudaStream_t st) {
-    const int total = a.N * a.BH;
+    const int total = a.nloc * a.BH;
     const int grid = total < num_sms ? total : num_sms;
     cudaError_t e =
         cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);

@@ -281,6 +281,61 @@ path_status_t path_attn_build_kcache(const path_prefill_desc_t *desc, const void
                                      int32_t cache_capacity, void *workspace,
                                      size_t workspace_bytes, path_stream_t stream);
 
+/* ------------------------------------------------- sequence-sharded prefill */
+
+/*
+ * The prefill of one long sequence split over `world` ranks, one GPU each
+ * (sequence or context parallelism).  The pages' blockwise algorithm
+ * (section "3. 효율적인 학습 및 추론", FlashAttention-style algorithm) makes
+ * every query chunk scan all earlier key chunks right to left, so the only
+ * exchange is the key side of every chunk: its boundary-adjusted keys Kh, its
+ * chunk product Pm and its values V, gathered once.
+ *
+ * Partition.  The N = ceil(seq_len / 128) chunks of 128 positions form
+ * 2 * world blocks of nb = ceil(N / (2 * world)) chunks; rank r holds blocks
+ * r and 2 * world - 1 - r (a zigzag, so every rank has early and late query
+ * chunks and the causal work is balanced).  A rank's local rows are the
+ * positions of its two blocks, in order, positions >= seq_len left out;
+ * path_attn_cp_local_len gives their number Lr and path_attn_cp_rows lists
+ * them.  Local tensors are [batch][heads][Lr][...] in that row order.
+ *
+ * Per rank:
+ *   1. path_attn_cp_prep on the rank's local q, k, v, w, beta: the UT
+ *      transform of each local chunk, its boundary-adjusted rows, its chunk
+ *      product and its attention to itself; writes the rank's exchange block
+ *      (path_attn_cp_exchange_bytes bytes) and keeps the rest in `workspace`.
+ *   2. The caller gathers the exchange blocks of all ranks, in rank order,
+ *      into one buffer of world * path_attn_cp_exchange_bytes bytes (an
+ *      all-gather: ncclAllGather, torch.distributed.all_gather_into_tensor).
+ *   3. path_attn_cp_scan with the gathered buffer and the same workspace:
+ *      the scan of the rank's query chunks over all earlier chunks; writes
+ *      out [batch][heads][Lr][128] and lse [batch][heads][Lr] (or NULL).
+ * With world = 1 the two calls compute exactly what path_attn_prefill_fwd
+ * computes.  PaTH-FoX: log_f is the forget-gate log of the WHOLE sequence,
+ * float32 [batch][heads][seq_len] on every rank (4 bytes per position; the
+ * bias needs prefix sums over all earlier positions), given to both calls;
+ * NULL for PaTH.  Supported: PATH_BF16, head_dim 128, chunk 0 or 128 (else
+ * PATH_ERR_UNSUPPORTED); 1 <= world <= 4096, 0 <= rank < world.  A rank may
+ * hold no rows (Lr = 0) when seq_len is short; its calls then read no input,
+ * but its exchange block must still take part in the gather.  Pointers are
+ * device pointers, 16-byte aligned; calls are asynchronous on `stream`.
+ */
+int32_t path_attn_cp_local_len(const path_prefill_desc_t *desc, int32_t world, int32_t rank);
+/* rows: HOST array of at least Lr entries, filled with the global position of
+ * each local row. */
+path_status_t path_attn_cp_rows(const path_prefill_desc_t *desc, int32_t world, int32_t rank,
+                                int32_t *rows, int32_t capacity);
+size_t path_attn_cp_exchange_bytes(const path_prefill_desc_t *desc, int32_t world);
+size_t path_attn_cp_workspace_size(const path_prefill_desc_t *desc, int32_t world);
+path_status_t path_attn_cp_prep(const path_prefill_desc_t *desc, int32_t world, int32_t rank,
+                                const void *q, const void *k, const void *v, const void *w,
+                                const float *beta, const float *log_f, void *exchange,
+                                void *workspace, size_t workspace_bytes, path_stream_t stream);
+path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, int32_t rank,
+                                const float *log_f, const void *exchange_all, void *out,
+                                float *lse, void *workspace, size_t workspace_bytes,
+                                path_stream_t stream);
+
 /* -------------------------------------------------------------- diagnostics */
 
 /*
