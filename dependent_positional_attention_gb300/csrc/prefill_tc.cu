@@ -29,11 +29,15 @@
 //               of O, P -> bf16 (TMEM), epilogue (out, lse)
 //   warp 8      TMA producer: Qh_b, then two rings: [Pm_c^T | Kh_c] pairs
 //               (64 KB slots) and V_c (32 KB slots)
-//   warp 9      MMA issuer (one thread) and TMEM owner; warps 10-11 idle
+//   warp 9      MMA issuer of the [U|S] products (one thread), TMEM owner
+//   warp 11     MMA issuer of the P V products (one thread); warp 10 idle
+// The two product streams touch disjoint tensor memory (U, S, Qt against P,
+// O) and each thread's commits track only its own MMAs, so the carried-query
+// chain never waits behind the issue of a P V product.
 // Registers are rebalanced at start (setmaxnreg): the producer/MMA group
 // drops to 120 per thread, the two compute groups rise to 192 (the launch's
 // 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512).
-// MMA issue order per step c: [U|S]_c, then PV_{c+1} (one step late, so the
+// Per step c the products are [U|S]_c and PV_{c+1} (one step late, so the
 // softmax has a full step of slack).  The first step of a tile reads Qh_b
 // from shared memory; the last (c = 0) needs no U and computes S_0 alone.
 // Chunk-0 tiles need no scan: the softmax group copies the prep's result.
@@ -73,7 +77,7 @@ struct Bars {
     uint64_t pair_full[kPairSlots], pair_empty[kPairSlots];
     uint64_t v_full[kVSlots], v_empty[kVSlots];
     uint64_t qb_tma_full, qb_empty, u_full, s_full, qb_conv_full;
-    uint64_t s_empty, p_full, o_done, drain;
+    uint64_t s_empty, p_full, o_done, drain, drain_pv;
     uint32_t tmem_base;
     int abort_word;
     float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         mbar_init(&bars.p_full, 1);
         mbar_init(&bars.o_done, 1);
         mbar_init(&bars.drain, 1);
+        mbar_init(&bars.drain_pv, 1);
         bars.abort_word = 0;
         fence_mbar_init();
     }
@@ -299,29 +304,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         __syncwarp();
     } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ [U|S] issuer
         if (lane == 0) {
-            int ps = 0, vs = 0;
-            uint32_t pph = 0, vph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0, pf_ph = 0;
+            int ps = 0;
+            uint32_t pph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0;
             const uint32_t qb_lo = tc::desc_lo(sQb, false);
             bool ok = true;
-            // O already holds the chunk's own attention block (written by the
-            // softmax group), so every PV accumulates
-            auto pv = [&]() -> bool {
-                if (!mbar_wait(&bars.v_full[vs], vph, a.err, abort_word, lim)) return false;
-                if (!mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim)) return false;
-                pf_ph ^= 1;
-                tc::fence_after_sync();
-                tc::gemm128_ta<true>(tmem + kColO, tmem + kColP,
-                                     tc::desc_lo(sV + vs * kTileBytes, true), true);
-                tc::mma_commit(&bars.v_empty[vs]);
-                if (++vs == kVSlots) {
-                    vs = 0;
-                    vph ^= 1;
-                }
-                tc::mma_commit(&bars.o_done);
-                return true;
-            };
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
                 const int b = tile_of(t, a).b;
                 if (b == 0) continue;
@@ -363,13 +351,41 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     tc::mma_commit(&bars.s_full);
                     // Qh_b's tile is free once the first step's product completes
                     if (first) tc::mma_commit(&bars.qb_empty);
-                    if (c < b - 1) ok = pv();
                 }
-                ok = ok && pv();
             }
-            // every MMA issued so far has completed before TMEM is released
+            // every MMA this thread issued has completed before TMEM is released
             tc::mma_commit(&bars.drain);
             mbar_wait(&bars.drain, 0, a.err, nullptr, lim);
+        }
+        __syncwarp();
+    } else if (warp == 11) {
+        // ------------------------------------------------------------ P V issuer
+        if (lane == 0) {
+            int vs = 0;
+            uint32_t vph = 0, pf_ph = 0;
+            bool ok = true;
+            // O already holds the chunk's own attention block (written by the
+            // softmax group), so every PV accumulates: V_{b-1}, ..., V_0 per tile
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+                const int b = tile_of(t, a).b;
+                for (int c = b - 1; c >= 0 && ok; --c) {
+                    ok = mbar_wait(&bars.v_full[vs], vph, a.err, abort_word, lim) &&
+                         mbar_wait(&bars.p_full, pf_ph, a.err, abort_word, lim);
+                    if (!ok) break;
+                    pf_ph ^= 1;
+                    tc::fence_after_sync();
+                    tc::gemm128_ta<true>(tmem + kColO, tmem + kColP,
+                                         tc::desc_lo(sV + vs * kTileBytes, true), true);
+                    tc::mma_commit(&bars.v_empty[vs]);
+                    if (++vs == kVSlots) {
+                        vs = 0;
+                        vph ^= 1;
+                    }
+                    tc::mma_commit(&bars.o_done);
+                }
+            }
+            tc::mma_commit(&bars.drain_pv);
+            mbar_wait(&bars.drain_pv, 0, a.err, nullptr, lim);
         }
         __syncwarp();
       }
