@@ -399,9 +399,11 @@ def decode_block(wlk, steps, warmup, ws, peaks, seed=0, fox=False):
     return res
 
 
-def backward_block(wlk, steps, warmup, ws, peaks):
+def backward_block(wlk, steps, warmup, ws, peaks, workspace_bytes=None):
     """path_attn_prefill_bwd on the forward's inputs and outputs, device-timed
-    with CUDA events; the four launches of one call form one step."""
+    with CUDA events; the launches of one call form one step.  With
+    workspace_bytes the call gets that much workspace (at least its minimum)
+    and runs the (batch, head) slices in passes."""
     x = wl.workload_inputs(wlk, seed=0, device="cuda")
     q, k, v, w, beta = (x[n] for n in ("q", "k", "v", "w", "beta"))
     log_f = x.get("log_f") if wlk.fox else None
@@ -409,8 +411,10 @@ def backward_block(wlk, steps, warmup, ws, peaks):
     dout = torch.randn(q.shape, generator=torch.Generator("cuda").manual_seed(7), device="cuda",
                        dtype=torch.float32).to(q.dtype)
     desc = pa._prefill_desc(q, None, 0)
-    ws_t = torch.empty(pa.path_attn_prefill_bwd_workspace_size(desc), device="cuda",
-                       dtype=torch.uint8)
+    ws_bytes = pa.path_attn_prefill_bwd_workspace_size(desc)
+    if workspace_bytes is not None:
+        ws_bytes = min(ws_bytes, max(workspace_bytes, pa.path_attn_prefill_bwd_workspace_min(desc)))
+    ws_t = torch.empty(ws_bytes, device="cuda", dtype=torch.uint8)
     run = lambda: pa.path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, log_f=log_f,
                                            workspace=ws_t)
     for _ in range(warmup):
@@ -429,9 +433,11 @@ def backward_block(wlk, steps, warmup, ws, peaks):
     flops = backward_flops(B, H, L, d)
     tf = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
-    res = {"workload": "%s prefill backward (dq, dk, dv, dw, dbeta%s) B%d H%d L%d d%d %s"
+    res = {"workload": "%s prefill backward (dq, dk, dv, dw, dbeta%s) B%d H%d L%d d%d %s%s"
                        % ("PaTH-FoX" if wlk.fox else "PaTH", ", dlog_f" if wlk.fox else "",
-                          B, H, L, d, wlk.dtype),
+                          B, H, L, d, wlk.dtype,
+                          ", workspace %.2f GB (slices in passes)" % (ws_bytes / 1e9)
+                          if workspace_bytes is not None else ""),
            "tokens_per_s": job_throughput(B * L, ms, ws), "ms_per_step": ms,
            "flops_per_step": flops, "tflops": tf, "workspace_bytes": ws_t.numel(),
            "roofline": {"kernel": "whole backward call: prep_tc_kernel + bwd_scan_tc_kernel + "
@@ -596,6 +602,8 @@ def main():
                                                peaks, fox=True)
         extra["backward_4k"] = backward_block(head, max(3, steps // 2), 3, ws, peaks)
         extra["backward_fox_4k"] = backward_block(wl.FOX_4K, max(3, steps // 2), 3, ws, peaks)
+        extra["backward_4k_ws1gb"] = backward_block(head, max(3, steps // 2), 3, ws, peaks,
+                                                    workspace_bytes=10 ** 9)
         extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
         extra["chunk_autotune_bf16_d64"] = autotune_block(
             wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (chunks 16-64 on the CUDA "

@@ -35,7 +35,7 @@ PATH_F32, PATH_BF16 = 0, 1
 EXPORTED_SYMBOLS = (
     "path_attn_prefill_workspace_size", "path_attn_prefill_fwd", "path_attn_prefill_prep",
     "path_attn_prefill_scan", "path_attn_prefill_bwd_workspace_size", "path_attn_prefill_bwd",
-    "path_attn_decode_workspace_size", "path_attn_decode_step", "path_attn_decode_step_noalloc",
+    "path_attn_prefill_bwd_workspace_min", "path_attn_decode_workspace_size", "path_attn_decode_step", "path_attn_decode_step_noalloc",
     "path_attn_decode_step_fox", "path_attn_fox_prefix",
     "path_attn_build_kcache_workspace_size", "path_attn_build_kcache",
     "path_attn_device_status", "path_attn_selftest_bounded_wait",
@@ -95,6 +95,8 @@ def load_library(path: str | None = None):
         lib.path_attn_prefill_scan.argtypes = [pd, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]
         lib.path_attn_prefill_bwd_workspace_size.argtypes = [pd]
         lib.path_attn_prefill_bwd_workspace_size.restype = _SZ
+        lib.path_attn_prefill_bwd_workspace_min.argtypes = [pd]
+        lib.path_attn_prefill_bwd_workspace_min.restype = _SZ
         lib.path_attn_prefill_bwd.argtypes = [pd] + [_VP] * 17 + [_SZ, _VP]
         lib.path_attn_decode_workspace_size.argtypes = [dd]
         lib.path_attn_decode_workspace_size.restype = _SZ
@@ -253,13 +255,19 @@ def path_attn_prefill_bwd_workspace_size(desc: PrefillDesc) -> int:
     return int(load_library().path_attn_prefill_bwd_workspace_size(ctypes.byref(desc)))
 
 
+def path_attn_prefill_bwd_workspace_min(desc: PrefillDesc) -> int:
+    return int(load_library().path_attn_prefill_bwd_workspace_min(ctypes.byref(desc)))
+
+
 def path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, log_f=None, dlse=None, scale=None,
-                          chunk=0, workspace=None, stream=None):
+                          chunk=0, workspace=None, stream=None, workspace_bytes=None):
     """Backward of path_attn_prefill_fwd (see path_attn_prefill_bwd in
     include/path_attn.h): gradients of sum(dout * out) + sum(dlse * lse).
     Tensors as for the forward; out and lse are the forward's outputs.
-    Returns a dict with dq, dk, dv, dw (dtype of q), dbeta and, for PaTH-FoX,
-    dlog_f (float32)."""
+    workspace_bytes bounds the workspace allocated here (between
+    path_attn_prefill_bwd_workspace_min and _size; the call then runs the
+    (batch, head) slices in passes).  Returns a dict with dq, dk, dv, dw
+    (dtype of q), dbeta and, for PaTH-FoX, dlog_f (float32)."""
     import torch
     lib = load_library()
     B, H, L, d = q.shape
@@ -278,6 +286,8 @@ def path_attn_prefill_bwd(q, k, v, w, beta, out, lse, dout, log_f=None, dlse=Non
     ws_bytes = path_attn_prefill_bwd_workspace_size(desc)
     if ws_bytes == 0:
         _check(lib.path_attn_prefill_bwd(ctypes.byref(desc), *([None] * 17), 0, None))
+    if workspace_bytes is not None:
+        ws_bytes = min(ws_bytes, max(int(workspace_bytes), path_attn_prefill_bwd_workspace_min(desc)))
     if workspace is None:
         workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
     _check(lib.path_attn_prefill_bwd(

@@ -153,6 +153,8 @@ struct BwdPlan {
     int BH, L, Lp, N, C, d;
     bool bf16;
     bool tc;  // bf16, head_dim 128, chunk 128: the tensor-core scan (PaTH calls)
+    bool tc_only;  // tc and a nonzero scale: the CUDA-core route can never run, so the
+                   // regions that route keeps in fp32 are sized for bf16
     size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_Qts, off_Dg, off_dQh;
     size_t off_dKh, off_dV, off_dA, off_dF, total;
 };
@@ -167,23 +169,31 @@ path_status_t plan_bwd(const path_prefill_desc_t *desc, BwdPlan *p) {
     p->L = desc->seq_len;
     p->d = desc->head_dim;
     p->tc = p->bf16 && p->d == 128 && p->C == 128;
+    // PaTH-FoX with scale 0 takes the CUDA-core route even when tc holds
+    p->tc_only = p->tc && desc->scale != 0.f;
     p->N = (p->L + p->C - 1) / p->C;
     if ((long long)p->N * p->C > (1ll << 30)) return fail(PATH_ERR_UNSUPPORTED, "seq_len too large");
     p->Lp = p->N * p->C;
     const size_t BH = p->BH, N = p->N, C = p->C, d = p->d;
     const size_t rows = BH * p->Lp, cc = BH * N * C * C;
+    // element size of Qh, Kh, Wt and the carried-row store: bf16 on the
+    // tensor-core route, fp32 on the CUDA cores
+    const size_t es = p->tc_only ? 2 : 4;
     size_t off = 0;
-    p->off_Qh = off; off = align_up(off + rows * d * 4, 256);
-    p->off_Kh = off; off = align_up(off + rows * d * 4, 256);
-    p->off_Wt = off; off = align_up(off + rows * d * 4, 256);
-    p->off_Sd = off; off = align_up(off + cc * 4, 256);
+    p->off_Qh = off; off = align_up(off + rows * d * es, 256);
+    p->off_Kh = off; off = align_up(off + rows * d * es, 256);
+    p->off_Wt = off; off = align_up(off + rows * d * es, 256);
+    // Sd: the CUDA-core route's within-chunk logits, or the tensor-core prep's
+    // OD (bf16) and LSD (fp32)
+    p->off_Sd = off;
+    off = align_up(off + (p->tc_only ? rows * 128 * 2 + rows * 4 : cc * 4), 256);
     p->off_F = off; off = align_up(off + rows * 4, 256);
     // the CUDA-core backward prep's scratch, or the tensor-core one's tiles
-    const size_t simt_scratch = (cc * kBwdPrepCC + BH * N * 2 * C * d) * 4;
+    const size_t simt_scratch = p->tc_only ? 0 : (cc * kBwdPrepCC + BH * N * 2 * C * d) * 4;
     const size_t tc_tiles = p->tc ? rows * 128 * (kBwdBf16Tiles * 2 + kBwdF32Tiles * 4) : 0;
     p->off_scratch = off;
     off = align_up(off + (simt_scratch > tc_tiles ? simt_scratch : tc_tiles), 256);
-    p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * 4, 256);
+    p->off_Qts = off; off = align_up(off + BH * (N * (N - 1) / 2) * C * d * es, 256);
     p->off_Dg = off; off = align_up(off + rows * 4, 256);
     // zeroed from here on
     p->off_dQh = off; off = align_up(off + rows * d * 4, 256);
@@ -533,6 +543,133 @@ void record_last_error(const char *msg) {
     snprintf(g_msg, sizeof g_msg, "%s", msg ? msg : "");
 }
 
+// The descriptor of one backward pass over n (batch * head) slices, with the
+// chunk resolved once for the whole call (the CUDA-core route's default chunk
+// depends on batch * heads).
+path_prefill_desc_t bwd_pass_desc(const path_prefill_desc_t *desc, int C, int n) {
+    path_prefill_desc_t d = *desc;
+    d.batch = 1;
+    d.heads = n;
+    d.chunk = C;
+    return d;
+}
+
+// One pass of the backward over the p.BH heads the pointers start at (the
+// workspace laid out by p).
+path_status_t bwd_pass(const path_prefill_desc_t *desc, const BwdPlan &p, const void *q,
+                       const void *k, const void *v, const void *w, const float *beta,
+                       const float *log_f, const void *out, const float *lse, const void *dout,
+                       const float *dlse, void *dq, void *dk, void *dv, void *dw, float *dbeta,
+                       float *dlog_f, void *workspace, cudaStream_t st) {
+    path_status_t s = PATH_OK;
+    float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
+    if (log_f) {
+        s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
+        if (s != PATH_OK) return s;
+    }
+    BwdArgs ba;
+    ba.q = q; ba.k = k; ba.v = v; ba.w = w; ba.out = out; ba.dout = dout;
+    ba.beta = beta; ba.lse = lse; ba.dlse = dlse;
+    ba.Qh = at<float>(workspace, p.off_Qh);
+    ba.Kh = at<float>(workspace, p.off_Kh);
+    ba.Wt = at<float>(workspace, p.off_Wt);
+    ba.F = F;
+    ba.Qts = at<float>(workspace, p.off_Qts);
+    ba.dQh = at<float>(workspace, p.off_dQh);
+    ba.dKh = at<float>(workspace, p.off_dKh);
+    ba.dV = at<float>(workspace, p.off_dV);
+    ba.dA = at<float>(workspace, p.off_dA);
+    ba.dF = log_f ? at<float>(workspace, p.off_dF) : nullptr;
+    ba.scratch = at<float>(workspace, p.off_scratch);
+    ba.dq = dq; ba.dk = dk; ba.dv = dv; ba.dw = dw; ba.dbeta = dbeta; ba.dlog_f = dlog_f;
+    ba.scale = desc->scale;
+    ba.BH = p.BH; ba.L = p.L; ba.Lp = p.Lp; ba.N = p.N; ba.C = p.C; ba.d = p.d;
+    // PaTH-FoX takes the tensor-core route too, unless scale is 0 (its key-side
+    // column sums are read back from the scaled bf16 dlogit tile)
+    if (p.tc && (!log_f || desc->scale != 0.f)) {
+        // tensor-core prep (bf16 Qh, Kh, Pm; its chunk outputs OD/LSD unused
+        // here), then the tensor-core scan and key side, then the backward
+        // prep (tensor-core contractions), then (PaTH-FoX) the dlog f suffix
+        char *qh = at<char>(workspace, p.off_Qh), *kh = at<char>(workspace, p.off_Kh);
+        char *pm = at<char>(workspace, p.off_Wt), *od = at<char>(workspace, p.off_Sd);
+        char *qts = at<char>(workspace, p.off_Qts);
+        const uint64_t npairs = (uint64_t)p.N * (p.N - 1) / 2;
+        PrepTcMaps pm_maps;
+        BwdTcMaps bm;
+        const bool enc =
+            encode_tmap_bf16_3d(&pm_maps.q, q, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.k, k, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.w, w, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.v, v, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.qh, qh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.kh, kh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.pm, pm, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&pm_maps.od, od, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.qh, qh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.kh, kh, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.pm, pm, 128, p.Lp, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.v, v, 128, p.L, p.BH, 64, 128) &&
+            encode_tmap_bf16_3d(&bm.dout, dout, 128, p.L, p.BH, 64, 128) &&
+            (npairs == 0 ||
+             encode_tmap_bf16_3d(&bm.qts, qts, 128, npairs * 128, p.BH, 64, 128));
+        if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
+        const int sms = num_sms();
+        if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+        memset(&pm_maps.vx, 0, sizeof pm_maps.vx);
+        PrepTcArgs ta;
+        ta.beta = beta;
+        ta.F = nullptr;
+        ta.scale = desc->scale;
+        ta.LSD = reinterpret_cast<float *>(od + (size_t)p.BH * p.Lp * 128 * 2);
+        ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
+        set_whole_sequence(ta, p.N, p.L, p.Lp);
+        ta.pm_transposed = 0;  // the backward's chain product reads Pm itself
+        ta.err = error_flag_ptr();
+        s = cuda_status(launch_prep_tc(pm_maps, ta, sms, st), "tensor-core prep launch");
+        if (s != PATH_OK) return s;
+        s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dQh), 0, p.total - p.off_dQh, st),
+                        "accumulator clear");
+        if (s != PATH_OK) return s;
+        BwdTcArgs tb;
+        tb.out = static_cast<const __nv_bfloat16 *>(out);
+        tb.dout = static_cast<const __nv_bfloat16 *>(dout);
+        tb.lse = lse; tb.dlse = dlse;
+        tb.dQh = ba.dQh; tb.dKh = ba.dKh; tb.dV = ba.dV; tb.dA = ba.dA;
+        tb.Dg = at<float>(workspace, p.off_Dg);
+        tb.F = F;
+        tb.dF = ba.dF;
+        tb.scale = desc->scale;
+        tb.BH = p.BH; tb.L = p.L; tb.Lp = p.Lp; tb.N = p.N;
+        tb.err = error_flag_ptr();
+        s = cuda_status(launch_bwd_rowdot(tb.out, tb.dout, dlse, at<float>(workspace, p.off_Dg),
+                                          p.BH, p.L, p.Lp, st),
+                        "row dot launch");
+        if (s != PATH_OK) return s;
+        s = cuda_status(launch_bwd_scan_tc(bm, tb, sms, st), "tensor-core backward scan launch");
+        if (s != PATH_OK) return s;
+        s = cuda_status(launch_bwd_kv_tc(bm, tb, sms, st), "tensor-core backward key-side launch");
+        if (s != PATH_OK) return s;
+        s = run_bwd_prep_tc(desc, p, ba, workspace, st);
+        if (s != PATH_OK || !log_f) return s;
+        return cuda_status(launch_fox_suffix(ba.dF, dlog_f, p.L, p.Lp, p.BH, st), "fox suffix launch");
+    }
+    PrepSimtArgs pa;
+    pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
+    pa.Qh = at<char>(workspace, p.off_Qh);
+    pa.Kh = at<char>(workspace, p.off_Kh);
+    pa.Wt = at<char>(workspace, p.off_Wt);
+    pa.Sd = at<float>(workspace, p.off_Sd);
+    pa.scratch = at<float>(workspace, p.off_scratch);
+    pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
+    pa.keys_only = 0;
+    s = cuda_status(launch_prep_simt(pa, p.bf16, false, st), "backward prep launch");
+    if (s != PATH_OK) return s;
+    s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dQh), 0, p.total - p.off_dQh, st),
+                    "accumulator clear");
+    if (s != PATH_OK) return s;
+    return cuda_status(launch_bwd(ba, p.bf16, st), "backward launch");
+}
+
 }  // namespace path
 
 using namespace path;
@@ -713,8 +850,8 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
                                     void *dq, void *dk, void *dv, void *dw, float *dbeta,
                                     float *dlog_f, void *workspace, size_t workspace_bytes,
                                     path_stream_t stream) {
-    BwdPlan p;
-    path_status_t s = plan_bwd(desc, &p);
+    BwdPlan full;
+    path_status_t s = plan_bwd(desc, &full);
     if (s != PATH_OK) return s;
     const void *req[] = {q, k, v, w, beta, out, lse, dout, dq, dk, dv, dw, dbeta, workspace};
     const char *names[] = {"q", "k", "v", "w", "beta", "out", "lse", "dout", "dq", "dk",
@@ -731,116 +868,59 @@ path_status_t path_attn_prefill_bwd(const path_prefill_desc_t *desc, const void 
             return fail(PATH_ERR_INVALID_ARG, "%s is not 16-byte aligned", onames[i]);
     if (!log_f != !dlog_f)
         return fail(PATH_ERR_INVALID_ARG, "dlog_f must be given exactly when log_f is");
-    if (workspace_bytes < p.total)
-        return fail(PATH_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
-                    p.total);
+    // heads per pass: as many as the workspace holds (all of them for
+    // path_attn_prefill_bwd_workspace_size bytes, one at the minimum)
+    int hb = full.BH;
+    if (workspace_bytes < full.total) {
+        int lo = 0, hi = full.BH;  // lo fits (0 trivially), hi does not
+        while (hi - lo > 1) {
+            const int mid = lo + (hi - lo) / 2;
+            BwdPlan pm;
+            path_prefill_desc_t dm = bwd_pass_desc(desc, full.C, mid);
+            if (plan_bwd(&dm, &pm) == PATH_OK && pm.total <= workspace_bytes) lo = mid;
+            else hi = mid;
+        }
+        hb = lo;
+        if (hb == 0) {
+            BwdPlan p1;
+            path_prefill_desc_t d1 = bwd_pass_desc(desc, full.C, 1);
+            plan_bwd(&d1, &p1);
+            return fail(PATH_ERR_INVALID_ARG,
+                        "workspace too small: %zu bytes; one head per pass needs %zu "
+                        "(path_attn_prefill_bwd_workspace_min)", workspace_bytes, p1.total);
+        }
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    float *F = log_f ? at<float>(workspace, p.off_F) : nullptr;
-    if (log_f) {
-        s = cuda_status(launch_fox_prefix(log_f, F, p.L, p.Lp, p.BH, st), "fox prefix launch");
+    const size_t es = full.bf16 ? 2 : 4;
+    const size_t act = (size_t)full.L * full.d * es;  // bytes per head of q, k, ..., dw
+    const size_t vec = (size_t)full.L;                // floats per head of beta, lse, ...
+    for (int h0 = 0; h0 < full.BH; h0 += hb) {
+        const int n = full.BH - h0 < hb ? full.BH - h0 : hb;
+        path_prefill_desc_t dn = bwd_pass_desc(desc, full.C, n);
+        BwdPlan p;
+        s = plan_bwd(&dn, &p);
+        if (s != PATH_OK) return s;
+        auto A = [&](const void *x) -> const void * {
+            return static_cast<const char *>(x) + (size_t)h0 * act;
+        };
+        auto M = [&](void *x) -> void * { return static_cast<char *>(x) + (size_t)h0 * act; };
+        auto Vc = [&](const float *x) -> const float * { return x ? x + (size_t)h0 * vec : x; };
+        auto Vm = [&](float *x) -> float * { return x ? x + (size_t)h0 * vec : x; };
+        s = bwd_pass(&dn, p, A(q), A(k), A(v), A(w), Vc(beta), Vc(log_f), A(out), Vc(lse),
+                     A(dout), Vc(dlse), M(dq), M(dk), M(dv), M(dw), Vm(dbeta), Vm(dlog_f),
+                     workspace, st);
         if (s != PATH_OK) return s;
     }
-    BwdArgs ba;
-    ba.q = q; ba.k = k; ba.v = v; ba.w = w; ba.out = out; ba.dout = dout;
-    ba.beta = beta; ba.lse = lse; ba.dlse = dlse;
-    ba.Qh = at<float>(workspace, p.off_Qh);
-    ba.Kh = at<float>(workspace, p.off_Kh);
-    ba.Wt = at<float>(workspace, p.off_Wt);
-    ba.F = F;
-    ba.Qts = at<float>(workspace, p.off_Qts);
-    ba.dQh = at<float>(workspace, p.off_dQh);
-    ba.dKh = at<float>(workspace, p.off_dKh);
-    ba.dV = at<float>(workspace, p.off_dV);
-    ba.dA = at<float>(workspace, p.off_dA);
-    ba.dF = log_f ? at<float>(workspace, p.off_dF) : nullptr;
-    ba.scratch = at<float>(workspace, p.off_scratch);
-    ba.dq = dq; ba.dk = dk; ba.dv = dv; ba.dw = dw; ba.dbeta = dbeta; ba.dlog_f = dlog_f;
-    ba.scale = desc->scale;
-    ba.BH = p.BH; ba.L = p.L; ba.Lp = p.Lp; ba.N = p.N; ba.C = p.C; ba.d = p.d;
-    // PaTH-FoX takes the tensor-core route too, unless scale is 0 (its key-side
-    // column sums are read back from the scaled bf16 dlogit tile)
-    if (p.tc && (!log_f || desc->scale != 0.f)) {
-        // tensor-core prep (bf16 Qh, Kh, Pm; its chunk outputs OD/LSD unused
-        // here), then the tensor-core scan and key side, then the backward
-        // prep (tensor-core contractions), then (PaTH-FoX) the dlog f suffix
-        char *qh = at<char>(workspace, p.off_Qh), *kh = at<char>(workspace, p.off_Kh);
-        char *pm = at<char>(workspace, p.off_Wt), *od = at<char>(workspace, p.off_Sd);
-        char *qts = at<char>(workspace, p.off_Qts);
-        const uint64_t npairs = (uint64_t)p.N * (p.N - 1) / 2;
-        PrepTcMaps pm_maps;
-        BwdTcMaps bm;
-        const bool enc =
-            encode_tmap_bf16_3d(&pm_maps.q, q, 128, p.L, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.k, k, 128, p.L, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.w, w, 128, p.L, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.v, v, 128, p.L, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.qh, qh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.kh, kh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.pm, pm, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&pm_maps.od, od, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&bm.qh, qh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&bm.kh, kh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&bm.pm, pm, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&bm.v, v, 128, p.L, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&bm.dout, dout, 128, p.L, p.BH, 64, 128) &&
-            (npairs == 0 ||
-             encode_tmap_bf16_3d(&bm.qts, qts, 128, npairs * 128, p.BH, 64, 128));
-        if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
-        const int sms = num_sms();
-        if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
-        memset(&pm_maps.vx, 0, sizeof pm_maps.vx);
-        PrepTcArgs ta;
-        ta.beta = beta;
-        ta.F = nullptr;
-        ta.scale = desc->scale;
-        ta.LSD = reinterpret_cast<float *>(od + (size_t)p.BH * p.Lp * 128 * 2);
-        ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
-        set_whole_sequence(ta, p.N, p.L, p.Lp);
-        ta.pm_transposed = 0;  // the backward's chain product reads Pm itself
-        ta.err = error_flag_ptr();
-        s = cuda_status(launch_prep_tc(pm_maps, ta, sms, st), "tensor-core prep launch");
-        if (s != PATH_OK) return s;
-        s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dQh), 0, p.total - p.off_dQh, st),
-                        "accumulator clear");
-        if (s != PATH_OK) return s;
-        BwdTcArgs tb;
-        tb.out = static_cast<const __nv_bfloat16 *>(out);
-        tb.dout = static_cast<const __nv_bfloat16 *>(dout);
-        tb.lse = lse; tb.dlse = dlse;
-        tb.dQh = ba.dQh; tb.dKh = ba.dKh; tb.dV = ba.dV; tb.dA = ba.dA;
-        tb.Dg = at<float>(workspace, p.off_Dg);
-        tb.F = F;
-        tb.dF = ba.dF;
-        tb.scale = desc->scale;
-        tb.BH = p.BH; tb.L = p.L; tb.Lp = p.Lp; tb.N = p.N;
-        tb.err = error_flag_ptr();
-        s = cuda_status(launch_bwd_rowdot(tb.out, tb.dout, dlse, at<float>(workspace, p.off_Dg),
-                                          p.BH, p.L, p.Lp, st),
-                        "row dot launch");
-        if (s != PATH_OK) return s;
-        s = cuda_status(launch_bwd_scan_tc(bm, tb, sms, st), "tensor-core backward scan launch");
-        if (s != PATH_OK) return s;
-        s = cuda_status(launch_bwd_kv_tc(bm, tb, sms, st), "tensor-core backward key-side launch");
-        if (s != PATH_OK) return s;
-        s = run_bwd_prep_tc(desc, p, ba, workspace, st);
-        if (s != PATH_OK || !log_f) return s;
-        return cuda_status(launch_fox_suffix(ba.dF, dlog_f, p.L, p.Lp, p.BH, st), "fox suffix launch");
-    }
-    PrepSimtArgs pa;
-    pa.q = q; pa.k = k; pa.w = w; pa.beta = beta;
-    pa.Qh = at<char>(workspace, p.off_Qh);
-    pa.Kh = at<char>(workspace, p.off_Kh);
-    pa.Wt = at<char>(workspace, p.off_Wt);
-    pa.Sd = at<float>(workspace, p.off_Sd);
-    pa.scratch = at<float>(workspace, p.off_scratch);
-    pa.BH = p.BH; pa.L = p.L; pa.Lp = p.Lp; pa.N = p.N; pa.C = p.C; pa.d = p.d;
-    pa.keys_only = 0;
-    s = cuda_status(launch_prep_simt(pa, p.bf16, false, st), "backward prep launch");
-    if (s != PATH_OK) return s;
-    s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_dQh), 0, p.total - p.off_dQh, st),
-                    "accumulator clear");
-    if (s != PATH_OK) return s;
-    return cuda_status(launch_bwd(ba, p.bf16, st), "backward launch");
+    return ok();
+}
+
+size_t path_attn_prefill_bwd_workspace_min(const path_prefill_desc_t *desc) {
+    BwdPlan full;
+    if (plan_bwd(desc, &full) != PATH_OK) return 0;
+    path_prefill_desc_t d1 = bwd_pass_desc(desc, full.C, 1);
+    BwdPlan p1;
+    if (plan_bwd(&d1, &p1) != PATH_OK) return 0;
+    return p1.total;
 }
 
 size_t path_attn_decode_workspace_size(const path_decode_desc_t *desc) {

@@ -128,11 +128,22 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
 
 /* ----------------------------------------------------------------- backward */
 
-/* Bytes of device workspace path_attn_prefill_bwd needs for `desc` (0 if the
- * descriptor is invalid).  It grows as batch*heads*seq_len^2*head_dim/chunk:
- * the backward keeps the carried query rows of every (query chunk, earlier
- * key chunk) pair, in fp32. */
+/* Workspace of path_attn_prefill_bwd (0 if the descriptor is invalid).
+ *
+ * path_attn_prefill_bwd_workspace_size: the bytes to run every (batch, head)
+ * slice in one pass, the fastest.  It grows as
+ * batch*heads*seq_len^2*head_dim/chunk: per slice the backward keeps the
+ * carried query rows of every (query chunk, earlier key chunk) pair (bf16 on
+ * the tensor-core route, fp32 on the CUDA cores).
+ *
+ * path_attn_prefill_bwd_workspace_min: the bytes for one slice per pass, the
+ * least path_attn_prefill_bwd accepts.  Any workspace in between works: the
+ * call then runs the slices in passes of as many as the workspace holds, so
+ * its size is the caller's choice between memory and speed (for example
+ * about 1 GB at batch 8, 12 heads, 4096 positions, head_dim 128, 16 slices
+ * per pass, against 6.4 GB in one pass). */
 size_t path_attn_prefill_bwd_workspace_size(const path_prefill_desc_t *desc);
+size_t path_attn_prefill_bwd_workspace_min(const path_prefill_desc_t *desc);
 
 /*
  * Backward of path_attn_prefill_fwd: the gradients of
@@ -149,7 +160,9 @@ size_t path_attn_prefill_bwd_workspace_size(const path_prefill_desc_t *desc);
  *   dq, dk, dv, dw : [B][H][L][d], desc->dtype, written.
  *   dbeta        : float32 [B][H][L], written.
  *   dlog_f       : float32 [B][H][L], written; required exactly when log_f is given.
- *   workspace    : at least path_attn_prefill_bwd_workspace_size(desc) bytes.
+ *   workspace    : at least path_attn_prefill_bwd_workspace_min(desc) bytes
+ *                  (see above; path_attn_prefill_bwd_workspace_size(desc) for
+ *                  one pass).
  * PATH_BF16 with head_dim 128 and chunk 128 (the default there) runs on the
  * tensor cores (bf16 operands, fp32 accumulation), PaTH and PaTH-FoX alike
  * (PaTH-FoX with scale 0 excepted); every other case runs in fp32 on the CUDA

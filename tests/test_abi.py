@@ -126,15 +126,35 @@ def bwd(lib, desc, ptrs, ws_bytes=1 << 40):
     return lib.path_attn_prefill_bwd(ctypes.byref(desc), *ptrs, ws_bytes, None)
 
 
+def test_backward_workspace_sizes(lib):
+    """One slice per pass is the minimum; with a single slice the minimum is
+    the whole size; the tensor-core route sizes its regions for bf16."""
+    D = pa.PrefillDesc
+    one = D(1, 1, 4096, 128, pa.PATH_BF16, 0.088, 0)
+    assert lib.path_attn_prefill_bwd_workspace_min(ctypes.byref(one)) == \
+        lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(one)) > 0
+    head = D(8, 12, 4096, 128, pa.PATH_BF16, 0.088, 0)
+    full = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(head))
+    least = lib.path_attn_prefill_bwd_workspace_min(ctypes.byref(head))
+    assert full < 6.5e9 and least * 90 < full
+    # PaTH-FoX with scale 0 may take the CUDA-core route: fp32-sized regions
+    zero = D(8, 12, 4096, 128, pa.PATH_BF16, 0.0, 0)
+    assert lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(zero)) > full
+    assert lib.path_attn_prefill_bwd_workspace_min(ctypes.byref(D(0, 1, 16, 64, 0, 0.1, 0))) == 0
+
+
 def test_backward_rejects_bad_arguments(lib):
     """Rejected before any CUDA call, so this runs without a GPU."""
     D = pa.PrefillDesc
     desc = D(2, 3, 100, 64, 0, 0.125, 0)
     need = lib.path_attn_prefill_bwd_workspace_size(ctypes.byref(desc))
+    least = lib.path_attn_prefill_bwd_workspace_min(ctypes.byref(desc))
     assert need > lib.path_attn_prefill_workspace_size(ctypes.byref(desc)) > 0
+    # six (batch, head) slices: one per pass needs about a sixth of all at once
+    assert 0 < least < need and least * 5 < need
     # q k v w beta log_f out lse dout dlse dq dk dv dw dbeta dlog_f workspace
     good = [FAKE] * 5 + [None] + [FAKE] * 3 + [None] + [FAKE] * 5 + [None, FAKE]
-    assert bwd(lib, desc, good, ws_bytes=need - 1) == pa.PATH_ERR_INVALID_ARG
+    assert bwd(lib, desc, good, ws_bytes=least - 1) == pa.PATH_ERR_INVALID_ARG
     assert b"workspace" in lib.path_attn_last_error()
     required = [0, 1, 2, 3, 4, 6, 7, 8, 10, 11, 12, 13, 14, 16]
     for i in required:

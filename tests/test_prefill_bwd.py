@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 GRADS = ("dq", "dk", "dv", "dw", "dbeta")
 
 
-def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None, scale=None):
+def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None, scale=None, workspace_bytes=None):
     dev = torch.device("cuda:0")
     g = {n: t.to(dev) for n, t in x.items()}
     gen = torch.Generator().manual_seed(1234)
@@ -35,7 +35,7 @@ def run(x, chunk=0, use_dlse=False, fwd_chunk=0, heads=None, scale=None):
     got = pa.path_attn_prefill_bwd(g["q"], g["k"], g["v"], g["w"], g["beta"], out, lse,
                                    dout.to(dev), log_f=g.get("log_f"),
                                    dlse=dlse.to(dev) if dlse is not None else None, chunk=chunk,
-                                   scale=scale)
+                                   scale=scale, workspace_bytes=workspace_bytes)
     torch.cuda.synchronize()
     assert pa.path_attn_device_status() == 0
     sel = slice(None) if heads is None else heads
@@ -181,3 +181,36 @@ def test_fox_zero_scale_takes_the_cuda_core_route():
     got, ref = run(wl.prefill_inputs(1, 2, 260, 128, "bf16", seed=19, fox=True), use_dlse=True,
                    scale=0.0)
     check(got, ref, 2e-2)
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_bounded_workspace_in_passes(fox):
+    """A workspace below the one-pass size: the (batch, head) slices run in
+    passes (one per pass at the minimum, two and three at a time in between)
+    on the tensor-core route; every variant matches the oracle."""
+    x = wl.prefill_inputs(2, 3, 700, 128, "bf16", seed=81 + fox, fox=fox)
+    desc = pa.PrefillDesc(2, 3, 700, 128, pa.PATH_BF16, 128 ** -0.5, 0)
+    least = pa.path_attn_prefill_bwd_workspace_min(desc)
+    for ws in (least, int(2.5 * least), 3 * least):
+        got, ref = run(x, use_dlse=True, workspace_bytes=ws)
+        check(got, ref, 2e-2)
+
+
+def test_bounded_workspace_cuda_core_route():
+    got, ref = run(wl.prefill_inputs(2, 2, 300, 64, "f32", seed=83, fox=True), chunk=64,
+                   use_dlse=True, workspace_bytes=1)
+    check(got, ref, 1e-4)
+
+
+@pytest.mark.slow
+def test_long_context_shape_bounded_workspace():
+    """The long-context shape (B1 H12 L32768, beta mostly near 2) with the
+    smallest workspace (one slice per pass, about 1.5 GB against 17 GB in one
+    pass); heads 0 and 11 checked in full against the oracle's gradients."""
+    w = wl.PREFILL_32K
+    x = wl.workload_inputs(w, seed=0, device="cuda")
+    desc = pa.PrefillDesc(1, 12, w.seq_len, 128, pa.PATH_BF16, 128 ** -0.5, 0)
+    least = pa.path_attn_prefill_bwd_workspace_min(desc)
+    assert least < 2e9 < pa.path_attn_prefill_bwd_workspace_size(desc)
+    got, ref = run(x, heads=[0, 11], workspace_bytes=least)
+    record_grads("backward_32k_heads_0_11_min_workspace", check(got, ref, 2e-2), 2e-2)
