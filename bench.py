@@ -607,7 +607,7 @@ def main():
         extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
         extra["chunk_autotune_bf16_d64"] = autotune_block(
             wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (chunks 16-64 on the CUDA "
-                               "cores; 128 and the default on the tensor cores, padded)",
+                               "cores; 128 and the default on the tensor cores, head_dim-64 scan)",
                                8, 12, 4096, 64, "bf16"))
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

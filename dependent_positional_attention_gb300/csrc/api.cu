@@ -66,6 +66,9 @@ struct PrefillPlan {
     bool bf16;  // bf16 inputs and output
     bool tc;    // the tensor-core route (bf16, chunk 128); else CUDA cores
     bool pad;   // tensor-core route for head_dim < 128: q, k, v, w, out zero-padded to 128
+    bool d64;   // tensor-core route for head_dim 64 without padded copies: the prep reads
+                // q, k, w, v directly (the second 64-column box of a row lies outside
+                // the tensor and loads as zeros) and the scan runs at head_dim 64
     size_t esize;
     size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_pad, total;
 };
@@ -111,7 +114,8 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     const bool pad_ok = p->bf16 && p->d < 128 && p->d % 8 == 0 &&
                         (desc->chunk == 0 || desc->chunk == 128);
     p->tc = p->bf16 && (p->d == 128 || pad_ok);
-    p->pad = p->tc && p->d < 128;
+    p->d64 = p->tc && p->d == 64;
+    p->pad = p->tc && p->d < 128 && !p->d64;
     if (p->tc) {
         if (desc->chunk != 0 && desc->chunk != 128)
             return fail(PATH_ERR_UNSUPPORTED, "PATH_BF16 with head_dim 128 needs chunk 0 or 128");
@@ -721,10 +725,12 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
     }
     if (p.tc) {
         PrepTcMaps maps;
-        const bool enc = encode_tmap_bf16_3d(&maps.q, q, 128, p.L, p.BH, 64, 128) &&
-                         encode_tmap_bf16_3d(&maps.k, k, 128, p.L, p.BH, 64, 128) &&
-                         encode_tmap_bf16_3d(&maps.w, w, 128, p.L, p.BH, 64, 128) &&
-                         encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128) &&
+        // head_dim 64: rows of 64, so that the second box of each row reads zeros
+        const uint64_t din = p.d64 ? 64 : 128;
+        const bool enc = encode_tmap_bf16_3d(&maps.q, q, din, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.k, k, din, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.w, w, din, p.L, p.BH, 64, 128) &&
+                         encode_tmap_bf16_3d(&maps.v, v, din, p.L, p.BH, 64, 128) &&
                          encode_tmap_bf16_3d(&maps.qh, at<char>(workspace, p.off_Qh), 128, p.Lp,
                                              p.BH, 64, 128) &&
                          encode_tmap_bf16_3d(&maps.kh, at<char>(workspace, p.off_Kh), 128, p.Lp,
@@ -792,11 +798,15 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
     }
     if (p.tc) {
         FlashTcMaps maps;
+        // head_dim 64 scans at 64: the 64 x 64 corner of each chunk's Pm^T and
+        // the first 64 columns of Qh and Kh, which are exact (the prep's padded
+        // coordinates carry no weight)
+        const int ds = p.d64 ? 64 : 128;
         const bool enc =
             encode_tmap_bf16_3d(&maps.qh, Qh, 128, p.Lp, p.BH, 64, 128) &&
             encode_tmap_bf16_3d(&maps.kh, Kh, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&maps.pm, Wt, 128, p.Lp, p.BH, 64, 128) &&
-            encode_tmap_bf16_3d(&maps.v, v, 128, p.L, p.BH, 64, 128);
+            encode_tmap_bf16_3d(&maps.pm, Wt, 128, p.Lp, p.BH, 64, ds) &&
+            encode_tmap_bf16_3d(&maps.v, v, ds, p.L, p.BH, 64, 128);
         if (!enc) return fail(PATH_ERR_CUDA, "TMA descriptor encoding failed");
         FlashTcArgs ta;
         ta.OD = reinterpret_cast<const __nv_bfloat16 *>(Sd);
@@ -805,7 +815,7 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
         ta.F = F; ta.out = static_cast<__nv_bfloat16 *>(out); ta.lse = lse;
         ta.scale = desc->scale; ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.cm = ChunkMap{1, 0, p.N};
-        ta.nloc = p.N; ta.Lq = p.Lp; ta.Lout = p.L; ta.zs = p.BH;
+        ta.nloc = p.N; ta.Lq = p.Lp; ta.Lout = p.L; ta.zs = p.BH; ta.d = ds;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
@@ -1201,7 +1211,7 @@ path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, 
     ta.lse = lse;
     ta.scale = desc->scale;
     ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
-    ta.cm = p.cm; ta.nloc = p.nloc; ta.Lq = p.Lq; ta.Lout = p.Lr; ta.zs = 3 * p.BH;
+    ta.cm = p.cm; ta.nloc = p.nloc; ta.Lq = p.Lq; ta.Lout = p.Lr; ta.zs = 3 * p.BH; ta.d = 128;
     ta.err = error_flag_ptr();
     const int sms = num_sms();
     if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");

@@ -201,8 +201,8 @@ struct ChunkMap {
 // [BH][rows][128] in 64 x 128 boxes with 128-byte swizzle.
 struct FlashTcMaps {
     CUtensorMap qh;          // local boundary-adjusted queries, rows = Lq
-    // key side of every chunk: Kh, Pm (per chunk a 128 x 128 matrix) and V,
-    // chunk c at row 128 * idx and z = owner * zs + bh (ChunkMap)
+    // key side of every chunk: Kh, Pm^T (per chunk a d x d matrix, box of d
+    // rows) and V, chunk c at row 128 * idx and z = owner * zs + bh (ChunkMap)
     CUtensorMap kh, pm, v;
 };
 
@@ -218,6 +218,7 @@ struct FlashTcArgs {
     int nloc;                 // local chunks (query tiles) per head
     int Lq, Lout;             // local padded rows, local rows
     int zs;                   // z stride between owners in the key-side maps
+    int d;                    // head dim of q, v, out: 128, or 64 (the workspace stays 128 wide)
     uint32_t *err;
 };
 

@@ -53,29 +53,41 @@
 namespace path {
 namespace {
 
-constexpr int kD = 128, kC = 128;
-constexpr int kPairSlots = 2, kVSlots = 2;
-constexpr int kTileBytes = kC * kD * 2;       // 32 KB bf16 tile
-constexpr int kPairBytes = 2 * kTileBytes;    // [Pm^T | Kh] as 256 rows
+constexpr int kC = 128;
 constexpr int kThreadsTC = 384;  // 3 warpgroups
-constexpr uint32_t kColU = 0, kColS = 128, kColQt = 256, kColP = 320, kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// dynamic shared memory layout (offsets from a 1024-aligned base).  A pair
-// slot holds the 256-row K-major operand [Pm^T ; Kh] as two 64-column
-// sub-tiles of 256 rows: [Pm^T k0-63 | Kh k0-63 | Pm^T k64-127 | Kh k64-127],
-// 16 KB each, so that rows 0-255 of each sub-tile are 8-row groups 1024 bytes
-// apart and the sub-tiles are 32 KB apart.
-constexpr int kOffQb = 0;
-constexpr int kOffPair = kOffQb + kTileBytes;
-constexpr int kOffV = kOffPair + kPairSlots * kPairBytes;
-constexpr int kOffBar = kOffV + kVSlots * kTileBytes;
+// Layout for head dimension D (128, or 64).  Rows of 64 bf16 are one
+// 128-byte swizzled sub-tile; a D-wide operand has D / 64 of them.  Dynamic
+// shared memory (offsets from a 1024-aligned base): Qh_b, the pair slots and
+// the V slots.  A pair slot holds the (D + 128)-row K-major operand
+// [Pm^T ; Kh] sub-tile by sub-tile: [Pm^T k0-63 | Kh k0-63 | Pm^T k64-127 |
+// Kh k64-127], so that its rows are 8-row groups 1024 bytes apart within a
+// sub-tile.  Tensor memory: [U | S] contiguous for the fused product, then Qt
+// (bf16 pairs), P (bf16 pairs), O.
+template <int D>
+struct Cfg {
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static constexpr int kSub = D / 64;
+    static constexpr int kTileBytes = kC * D * 2;          // Qh_b or V: 128 rows
+    static constexpr int kPairSub = (D + kC) * 128;        // one sub-tile of a pair
+    static constexpr int kPairBytes = kSub * kPairSub;
+    static constexpr int kPairSlots = D == 64 ? 4 : 2, kVSlots = D == 64 ? 4 : 2;
+    static constexpr uint32_t kColU = 0, kColS = D, kColQt = D + kC, kColP = kColQt + D / 2,
+                              kColO = kColP + kC / 2;
+    static constexpr int kOffQb = 0;
+    static constexpr int kOffPair = kOffQb + kTileBytes;
+    static constexpr int kOffV = kOffPair + kPairSlots * kPairBytes;
+    static constexpr int kOffBar = kOffV + kVSlots * kTileBytes;
+    static_assert(kColO + D <= 512, "tensor memory budget exceeded");
+};
 
+template <int D>
 struct Bars {
-    uint64_t pair_full[kPairSlots], pair_empty[kPairSlots];
-    uint64_t v_full[kVSlots], v_empty[kVSlots];
+    uint64_t pair_full[Cfg<D>::kPairSlots], pair_empty[Cfg<D>::kPairSlots];
+    uint64_t v_full[Cfg<D>::kVSlots], v_empty[Cfg<D>::kVSlots];
     uint64_t qb_tma_full, qb_empty, u_full, s_full, qb_conv_full;
     uint64_t s_empty, p_full, o_done, drain, drain_pv;
     uint32_t tmem_base;
@@ -83,8 +95,12 @@ struct Bars {
     float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
 };
 // barriers/misc after the rings, plus slack to align the dynamic base to 1024
-constexpr int kSmemBytes = kOffBar + (int)((sizeof(Bars) + 127) / 128 * 128) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+template <int D>
+constexpr int smem_bytes() {
+    return Cfg<D>::kOffBar + (int)((sizeof(Bars<D>) + 127) / 128 * 128) + 1024;
+}
+static_assert(smem_bytes<128>() <= 232448 && smem_bytes<64>() <= 232448,
+              "shared memory budget exceeded");
 
 // Warpgroup barrier.  bar.sync is a warp-aligned instruction: every lane of
 // the warp must execute it together, so the warp is reconverged first (lanes
@@ -138,12 +154,12 @@ __device__ __forceinline__ Tile tile_of(int t, const FlashTcArgs &a) {
 // Fused carried-query / logit product for step c: D[0,256) = A [Pm_c^T ; Kh_c]^T
 // over K = 128 (eight N = 256 instructions).  A is the carried rows in TMEM
 // (a_tmem) or, on a tile's first step, Qh_b in shared memory (a_lo).
-template <bool kAFromSmem>
+template <int D, bool kAFromSmem>
 __device__ __forceinline__ void gemm_us(uint32_t d_tmem, uint32_t a, uint32_t pair_lo) {
-    constexpr uint32_t idesc = tc::idesc_bf16(128, 256, false, false);
+    constexpr uint32_t idesc = tc::idesc_bf16(128, D + kC, false, false);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t boff = (uint32_t)((kk >> 2) * (kTileBytes / 16) + (kk & 3) * 2);
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t boff = (uint32_t)((kk >> 2) * (Cfg<D>::kPairSub / 16) + (kk & 3) * 2);
         if (kAFromSmem)
             tc::mma_bf16_lohi(d_tmem, a + (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2),
                               pair_lo + boff, idesc, kk > 0 ? 1u : 0u);
@@ -155,12 +171,12 @@ __device__ __forceinline__ void gemm_us(uint32_t d_tmem, uint32_t a, uint32_t pa
 
 // Logits alone (the last step, c = 0, has no chunk product to apply): N = 128
 // over the Kh half of a pair slot, whose sub-tiles are 32 KB apart.
-template <bool kAFromSmem>
+template <int D, bool kAFromSmem>
 __device__ __forceinline__ void gemm_s(uint32_t d_tmem, uint32_t a, uint32_t kh_lo) {
     constexpr uint32_t idesc = tc::idesc_bf16(128, 128, false, false);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t boff = (uint32_t)((kk >> 2) * (kTileBytes / 16) + (kk & 3) * 2);
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t boff = (uint32_t)((kk >> 2) * (Cfg<D>::kPairSub / 16) + (kk & 3) * 2);
         if (kAFromSmem)
             tc::mma_bf16_lohi(d_tmem, a + (uint32_t)((kk >> 2) * 1024 + (kk & 3) * 2),
                               kh_lo + boff, idesc, kk > 0 ? 1u : 0u);
@@ -170,13 +186,30 @@ __device__ __forceinline__ void gemm_s(uint32_t d_tmem, uint32_t a, uint32_t kh_
     }
 }
 
-template <bool kFox>
+// O (+)= P V over the 128 keys of a chunk: N = D, the V tile MN-major.
+template <int D>
+__device__ __forceinline__ void gemm_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
+                                        bool accumulate) {
+    constexpr uint32_t idesc = tc::idesc_bf16(128, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        tc::mma_bf16_ta(d_tmem, p_tmem + (uint32_t)(kk * 8), v_lo + (uint32_t)(kk * 128), idesc,
+                        (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <bool kFox, int D>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     flash_tc_kernel(const __grid_constant__ FlashTcMaps maps, FlashTcArgs a) {
+    using K = Cfg<D>;
+    constexpr int kTileBytes = K::kTileBytes, kPairBytes = K::kPairBytes;
+    constexpr int kPairSlots = K::kPairSlots, kVSlots = K::kVSlots;
+    constexpr int kOffQb = K::kOffQb, kOffPair = K::kOffPair, kOffV = K::kOffV;
+    constexpr uint32_t kColU = K::kColU, kColS = K::kColS, kColQt = K::kColQt, kColP = K::kColP,
+                       kColO = K::kColO;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Bars &bars = *reinterpret_cast<Bars *>(smem + kOffBar);
+    Bars<D> &bars = *reinterpret_cast<Bars<D> *>(smem + K::kOffBar);
     const uint32_t sQb = smem_u32(smem + kOffQb);
     const uint32_t sPair = smem_u32(smem + kOffPair);
     const uint32_t sV = smem_u32(smem + kOffV);
@@ -241,16 +274,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!mbar_wait(&bars.pair_empty[ps], pph ^ 1, a.err, abort_word, lim)) return false;
                 uint8_t *dst = smem + kOffPair + ps * kPairBytes;
                 uint64_t *full = &bars.pair_full[ps];
-                if (c >= 1) {
-                    mbar_arrive_expect_tx(full, 2 * kTileBytes);
-                    tc::tma_load_3d(dst, &maps.pm, 0, y, z, full);
-                    tc::tma_load_3d(dst + kTileBytes / 2, &maps.kh, 0, y, z, full);
-                    tc::tma_load_3d(dst + kTileBytes, &maps.pm, 64, y, z, full);
-                    tc::tma_load_3d(dst + 3 * kTileBytes / 2, &maps.kh, 64, y, z, full);
-                } else {
-                    mbar_arrive_expect_tx(full, kTileBytes);
-                    tc::tma_load_3d(dst + kTileBytes / 2, &maps.kh, 0, y, z, full);
-                    tc::tma_load_3d(dst + 3 * kTileBytes / 2, &maps.kh, 64, y, z, full);
+                // per sub-tile: Pm^T's D rows (box of D rows), then Kh's 128
+                mbar_arrive_expect_tx(full, c >= 1 ? kPairBytes : kTileBytes);
+#pragma unroll
+                for (int sub = 0; sub < K::kSub; ++sub) {
+                    uint8_t *ds = dst + sub * K::kPairSub;
+                    if (c >= 1) tc::tma_load_3d(ds, &maps.pm, 64 * sub, y, z, full);
+                    tc::tma_load_3d(ds + D * 128, &maps.kh, 64 * sub, y, z, full);
                 }
                 pair_par[ps] = (int)pph;
                 if (++ps == kPairSlots) {
@@ -266,8 +296,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!mbar_wait(&bars.v_empty[vs], vph ^ 1, a.err, abort_word, lim)) return false;
                 uint8_t *dst = smem + kOffV + vs * kTileBytes;
                 mbar_arrive_expect_tx(&bars.v_full[vs], kTileBytes);
-                tc::tma_load_3d(dst, &maps.v, 0, y, z, &bars.v_full[vs]);
-                tc::tma_load_3d(dst + kTileBytes / 2, &maps.v, 64, y, z, &bars.v_full[vs]);
+#pragma unroll
+                for (int sub = 0; sub < K::kSub; ++sub)
+                    tc::tma_load_3d(dst + sub * (kC * 128), &maps.v, 64 * sub, y, z, &bars.v_full[vs]);
                 v_par[vs] = (int)vph;
                 if (++vs == kVSlots) {
                     vs = 0;
@@ -283,9 +314,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 qe_ph ^= 1;
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bars.qb_tma_full, kTileBytes);
-                tc::tma_load_3d(smem + kOffQb, &maps.qh, 0, tl.i * kC, bh, &bars.qb_tma_full);
-                tc::tma_load_3d(smem + kOffQb + kTileBytes / 2, &maps.qh, 64, tl.i * kC, bh,
-                                &bars.qb_tma_full);
+#pragma unroll
+                for (int sub = 0; sub < K::kSub; ++sub)
+                    tc::tma_load_3d(smem + kOffQb + sub * (kC * 128), &maps.qh, 64 * sub,
+                                    tl.i * kC, bh, &bars.qb_tma_full);
                 q_last_par = (int)(q_loads++ & 1);
                 for (int c = b - 1; c >= 0 && ok; --c) {
                     ok = ok && load_pair(c, bh);
@@ -331,13 +363,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (!ok) break;
                     tc::fence_after_sync();
                     const uint32_t pair_lo = tc::desc_lo(sPair + ps * kPairBytes, false);
-                    const uint32_t kh_lo = tc::desc_lo(sPair + ps * kPairBytes + kTileBytes / 2, false);
+                    const uint32_t kh_lo = tc::desc_lo(sPair + ps * kPairBytes + D * 128, false);
                     if (c >= 1) {
-                        if (first) gemm_us<true>(tmem + kColU, qb_lo, pair_lo);
-                        else gemm_us<false>(tmem + kColU, tmem + kColQt, pair_lo);
+                        if (first) gemm_us<D, true>(tmem + kColU, qb_lo, pair_lo);
+                        else gemm_us<D, false>(tmem + kColU, tmem + kColQt, pair_lo);
                     } else {
-                        if (first) gemm_s<true>(tmem + kColS, qb_lo, kh_lo);
-                        else gemm_s<false>(tmem + kColS, tmem + kColQt, kh_lo);
+                        if (first) gemm_s<D, true>(tmem + kColS, qb_lo, kh_lo);
+                        else gemm_s<D, false>(tmem + kColS, tmem + kColQt, kh_lo);
                     }
                     tc::mma_commit(&bars.pair_empty[ps]);
                     if (++ps == kPairSlots) {
@@ -374,8 +406,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (!ok) break;
                     pf_ph ^= 1;
                     tc::fence_after_sync();
-                    tc::gemm128_ta<true>(tmem + kColO, tmem + kColP,
-                                         tc::desc_lo(sV + vs * kTileBytes, true), true);
+                    gemm_pv<D>(tmem + kColO, tmem + kColP, tc::desc_lo(sV + vs * kTileBytes, true),
+                               true);
                     tc::mma_commit(&bars.v_empty[vs]);
                     if (++vs == kVSlots) {
                         vs = 0;
@@ -415,17 +447,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (!ok) break;
                 uf_ph ^= 1;
                 tc::fence_after_sync();
-                uint32_t pk[64];
+                uint32_t pk[D / 2];
                 {
-                    uint32_t v[128];
-                    tc::tmem_ld128(lane_addr + kColU, v);
+                    uint32_t v[D];
+                    if constexpr (D == 128)
+                        tc::tmem_ld128(lane_addr + kColU, v);
+                    else
+                        tc::tmem_ld64(lane_addr + kColU, v);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j)
+                    for (int j = 0; j < D / 2; ++j)
                         pk[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
                 }
-                tc::tmem_st32(lane_addr + kColQt, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-                tc::tmem_st32(lane_addr + kColQt + 32,
-                              *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h)
+                    tc::tmem_st32(lane_addr + kColQt + 32 * h,
+                                  *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * h));
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 named_bar(1, 128);
@@ -448,14 +484,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             const float fi = fox ? Frow[b * kC + r] * kLog2e : 0.f;
             const int row = b * kC + r;       // in the whole sequence
             const int lrow = tl.i * kC + r;   // in the local rows
-            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lq + lrow) * kD;
+            // the prep's own-chunk output is 128 wide (head_dim 64 zero-padded)
+            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lq + lrow) * 128;
             const float lsd = a.LSD[(size_t)bh * a.Lq + lrow];
             if (b == 0) {
                 // the chunk attends only to itself: the prep's result is final
                 if (row < a.L) {
-                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * kD;
+                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < D / 8; ++j)
                         reinterpret_cast<uint4 *>(orow)[j] = reinterpret_cast<const uint4 *>(odrow)[j];
                     if (a.lse) a.lse[(size_t)bh * a.Lout + lrow] = lsd;
                 }
@@ -464,7 +501,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             // start from the chunk's own block: O = OD (weights summing to 1
             // against the reference m = LSD in log2 units), l = 1
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -556,7 +593,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 if (rescale) {
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
                         tc::tmem_ld32(lane_addr + kColO + cc * 32, o);
 #pragma unroll
@@ -583,9 +620,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             od_ph ^= 1;
             tc::fence_after_sync();
             const float inv = 1.f / l;
-            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * kD;
+            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t v[64];
                 __syncwarp();  // the ragged-row branch below diverges; the load is warp-aligned
                 tc::tmem_ld64(lane_addr + kColO + cc * 64, v);
@@ -626,12 +663,14 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
                             cudaStream_t st) {
     const int T = a.nloc * a.BH;
     const int grid = T < num_sms ? T : num_sms;
+    if (a.d != 128 && a.d != 64) return cudaErrorInvalidValue;
     void (*kern)(const FlashTcMaps, FlashTcArgs) =
-        a.F ? flash_tc_kernel<true> : flash_tc_kernel<false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        a.d == 64 ? (a.F ? flash_tc_kernel<true, 64> : flash_tc_kernel<false, 64>)
+                  : (a.F ? flash_tc_kernel<true, 128> : flash_tc_kernel<false, 128>);
+    const int smem = a.d == 64 ? smem_bytes<64>() : smem_bytes<128>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsTC, kSmemBytes, st>>>(maps, a);
+    kern<<<grid, kThreadsTC, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 

@@ -183,19 +183,21 @@ def test_backward_rejects_bad_arguments(lib):
 
 
 def test_padded_route_workspace(lib):
-    """bf16 with head_dim a multiple of 8 below 128 and the default chunk is
-    planned on the tensor-core route with zero-padded copies: its workspace
-    holds the 128-wide padded q, k, w, v and out on top of the head_dim-128
-    layout; an explicit chunk other than 128 plans the CUDA-core route."""
+    """bf16 with head_dim a multiple of 8 below 128 (64 excepted) and the
+    default chunk is planned on the tensor-core route with zero-padded copies:
+    its workspace holds the 128-wide padded q, k, w, v and out on top of the
+    head_dim-128 layout.  Head_dim 64 reads its tensors directly (no copies):
+    the head_dim-128 layout alone.  An explicit chunk other than 128 plans the
+    CUDA-core route."""
     D = pa.PrefillDesc
     B, H, L = 2, 3, 300
     ws = lambda d, dtype, chunk: lib.path_attn_prefill_workspace_size(
         ctypes.byref(D(B, H, L, d, dtype, 0.1, chunk)))
     full = ws(128, 1, 0)
-    padded = ws(64, 1, 0)
+    padded = ws(96, 1, 0)
     assert padded >= full + 5 * B * H * L * 128 * 2
-    assert ws(64, 1, 128) == padded
+    assert ws(64, 1, 0) == full == ws(64, 1, 128)
     # chunk 64 on the CUDA-core route: fp32 workspace of head_dim 64, no padded copies
-    assert 0 < ws(64, 1, 64) != padded
+    assert 0 < ws(64, 1, 64) != full
     # head_dim 36 (not a multiple of 8) stays on the CUDA cores
     assert ws(36, 1, 0) > 0

@@ -97,13 +97,27 @@ def test_cuda_core_route_other_head_dims(d, L, chunk, fox):
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("fox", [False, True])
+def test_head_dim_64_full_size(fox):
+    """B8 H12 L4096 head_dim 64 (the head_dim-64 scan, the prep reading the
+    64-wide tensors directly), 64 sampled rows of every head."""
+    x = wl.prefill_inputs(8, 12, 4096, 64, "bf16", seed=0, fox=fox, device="cuda")
+    rows = wl.sampled_rows(4096, 64)
+    eo, el = run(x, rows=rows)
+    record_margin("prefill_d64_4k" + ("_fox" if fox else ""), max_dout=eo, tol_out=TOL_OUT,
+                  max_dlse=el, tol_lse=TOL_LSE)
+    assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
+
+
 @pytest.mark.parametrize("d,L,chunk,fox", [(64, 300, 0, False), (64, 700, 128, True),
+                                           (64, 1, 0, True), (64, 129, 0, False),
                                            (32, 129, 0, False), (96, 1, 0, True),
                                            (120, 260, 0, False)])
 def test_padded_tensor_core_route(d, L, chunk, fox):
     """bf16 with head_dim a multiple of 8 below 128 and chunk 128 (the
-    default): the tensor-core kernels on zero-padded copies, the caller's
-    scale kept; same tolerance."""
+    default) on the tensor cores: head_dim 64 on its own scan, the others on
+    zero-padded copies; the caller's scale kept; same tolerance."""
     eo, el = run(wl.prefill_inputs(2, 3, L, d, "bf16", seed=d + L + 1, fox=fox), chunk=chunk)
     assert eo <= TOL_OUT and el <= TOL_LSE, (eo, el)
 
