@@ -92,7 +92,7 @@ struct Bars {
     uint64_t s_empty, p_full, o_done, drain, drain_pv;
     uint32_t tmem_base;
     int abort_word;
-    float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
+    alignas(16) float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
 };
 // barriers/misc after the rings, plus slack to align the dynamic base to 1024
 template <int D>
@@ -102,27 +102,8 @@ constexpr int smem_bytes() {
 static_assert(smem_bytes<128>() <= 232448 && smem_bytes<64>() <= 232448,
               "shared memory budget exceeded");
 
-// Warpgroup barrier.  bar.sync is a warp-aligned instruction: every lane of
-// the warp must execute it together, so the warp is reconverged first (lanes
-// may leave a bounded wait loop at different iterations).
-__device__ __forceinline__ void named_bar(int id, int n) {
-    __syncwarp();
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Barrier over a warpgroup that also ANDs `ok` across its threads, so that a
-// wait that gave up in one thread makes the whole group leave together.
-__device__ __forceinline__ bool group_all(int id, int n, bool ok) {
-    uint32_t r;
-    __syncwarp();
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)ok), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
-}
+using tc::group_all;
+using tc::named_bar;
 
 // 2^x on the MUFU unit (inputs here are <= 0 after the max subtraction;
 // results below 2^-126 flush to zero, which a softmax weight can ignore).
@@ -539,11 +520,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (threadIdx.x == 128) mbar_arrive(&bars.s_empty);
                 float mx = -INFINITY;
                 if (kFox) {
+                    // the chunk's column prefixes, four per shared-memory load
+                    const uint32_t fsm_s = smem_u32(bars.fsm);
 #pragma unroll
-                    for (int j = 0; j < kC; ++j) {
-                        const float t = fmaf(__uint_as_float(v[j]), sl2, -bars.fsm[j]);
-                        v[j] = __float_as_uint(t);
-                        mx = fmaxf(mx, t);
+                    for (int j4 = 0; j4 < kC / 4; ++j4) {
+                        const uint4 f4 = tc::lds128(fsm_s + 16 * j4);
+                        const uint32_t fw[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * j4 + e;
+                            const float t = fmaf(__uint_as_float(v[j]), sl2, -__uint_as_float(fw[e]));
+                            v[j] = __float_as_uint(t);
+                            mx = fmaxf(mx, t);
+                        }
                     }
                     mx += dlt;
                 } else {

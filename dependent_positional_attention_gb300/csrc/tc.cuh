@@ -103,6 +103,28 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
                  : "memory");
 }
 
+// Named barrier over n threads.  bar.sync is a warp-aligned instruction: every
+// lane of the warp must execute it together, so the warp is reconverged first
+// (lanes may leave a bounded wait loop at different iterations).
+__device__ __forceinline__ void named_bar(int id, int n) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also ANDs `ok` across its threads, so that a wait that
+// gave up in one thread makes the whole group leave together.
+__device__ __forceinline__ bool group_all(int id, int n, bool ok) {
+    uint32_t r;
+    __syncwarp();
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
 // ------------------------------------------------------------------ TMEM
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {

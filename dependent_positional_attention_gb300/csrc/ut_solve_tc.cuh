@@ -12,7 +12,15 @@ namespace path {
 namespace utc {
 
 constexpr int kN = 128;    // chunk rows
-constexpr int kThr = 256;  // threads of the calling block
+constexpr int kThr = 256;  // threads that run the solve: warps 0-7 of the calling block
+
+// Barrier over the solving threads only (named barrier 1), so that a block may
+// hold further warps that do other work meanwhile.  bar.sync is warp-aligned:
+// the warp is reconverged first.
+__device__ __forceinline__ void solve_sync() {
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;" ::"n"(kThr) : "memory");
+}
 
 // fp32 128 x 128 matrices in shared memory (G, then T): row stride 128 floats,
 // the 16-byte groups of row r permuted by group ^ sw_f(r).  sw_f takes eight
@@ -121,7 +129,7 @@ __device__ __forceinline__ void ut_merge(float *G, float *Tf, const float *beta,
     mma3_rows<NT>(acc, acc2, G, r2 + i0, r1, Tf, r1, r1 + j0, j0, S, lane);
     // inverse mode: P = diag(beta_2) G21 Ti11, so that Ti21 = -Ti22 P
     store_frag<NT>(G, r1 + i0, r2 + j0, acc, acc2, 1.f, lane, kInv ? beta + r2 + i0 : nullptr);
-    __syncthreads();
+    solve_sync();
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -129,7 +137,7 @@ __device__ __forceinline__ void ut_merge(float *G, float *Tf, const float *beta,
     // T21[i][j] = -sum_k T22[i][k] P[k][j]; T22[i][k] = 0 for k > i
     mma3_rows<NT>(acc, acc2, Tf, r2 + i0, r2, G, r1, r2 + j0, 0, i0 + 16, lane);
     store_frag<NT>(Tf, r2 + i0, r1 + j0, acc, acc2, -1.f, lane);
-    __syncthreads();
+    solve_sync();
 }
 
 // T = (I + strict_lower(diag(beta) G))^{-1} diag(beta) into Tf (fp32, sw
@@ -176,7 +184,7 @@ __device__ __forceinline__ void ut_solve(float *G, float *Tf, const float *beta,
 #pragma unroll
         for (int i = 0; i < 16; ++i) Tf[sw(o + i, o + c)] = x[i] * bc;
     }
-    __syncthreads();
+    solve_sync();
     const int warp = tid >> 5, lane = tid & 31;
     ut_merge<16, kInv>(G, Tf, beta, warp, lane);
     ut_merge<32, kInv>(G, Tf, beta, warp, lane);
