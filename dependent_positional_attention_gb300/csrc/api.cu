@@ -70,7 +70,7 @@ struct PrefillPlan {
                 // q, k, w, v directly (the second 64-column box of a row lies outside
                 // the tensor and loads as zeros) and the scan runs at head_dim 64
     size_t esize;
-    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_pad, total;
+    size_t off_Qh, off_Kh, off_Wt, off_Sd, off_F, off_scratch, off_pad, off_tile, total;
 };
 
 // Checks shared by the prefill forward and backward descriptors.
@@ -144,6 +144,8 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     p->off_scratch = off; off = align_up(off + (p->tc ? 0 : cc * 5 * 4), 256);
     // padded q, k, w, v and out, [BH][L][128] bf16 each
     p->off_pad = off; off = align_up(off + (p->pad ? (size_t)5 * p->BH * p->L * 128 * 2 : 0), 256);
+    // the tensor-core scan's tile counter
+    p->off_tile = off; off = align_up(off + (p->tc ? 4 : 0), 256);
     p->total = off;
     return ok();
 }
@@ -276,7 +278,7 @@ struct CpPlan {
     int Lr;      // valid local rows
     int Lq;      // padded local rows, 2 * nb * 128
     ChunkMap cm;
-    size_t off_Qh, off_OD, off_LSD, off_F, total;  // workspace
+    size_t off_Qh, off_OD, off_LSD, off_F, off_tile, total;  // workspace
     size_t section;   // bytes of one of the three sections of an exchange block
     size_t exchange;  // bytes of one rank's exchange block
 };
@@ -315,6 +317,7 @@ path_status_t plan_cp(const path_prefill_desc_t *desc, int32_t world, int32_t ra
     p->off_OD = off; off = align_up(off + rows * 128 * 2, 256);
     p->off_LSD = off; off = align_up(off + rows * 4, 256);
     p->off_F = off; off = align_up(off + (size_t)p->BH * p->Lp * 4, 256);
+    p->off_tile = off; off = align_up(off + 4, 256);  // the scan's tile counter
     p->total = off;
     p->section = rows * 128 * 2;
     p->exchange = 3 * p->section;
@@ -816,6 +819,7 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
         ta.scale = desc->scale; ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
         ta.cm = ChunkMap{1, 0, p.N};
         ta.nloc = p.N; ta.Lq = p.Lp; ta.Lout = p.L; ta.zs = p.BH; ta.d = ds;
+        ta.tile_ctr = at<int>(workspace, p.off_tile);
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
@@ -1212,6 +1216,7 @@ path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, 
     ta.scale = desc->scale;
     ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
     ta.cm = p.cm; ta.nloc = p.nloc; ta.Lq = p.Lq; ta.Lout = p.Lr; ta.zs = 3 * p.BH; ta.d = 128;
+    ta.tile_ctr = at<int>(workspace, p.off_tile);
     ta.err = error_flag_ptr();
     const int sms = num_sms();
     if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");

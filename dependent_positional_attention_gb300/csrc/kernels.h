@@ -219,6 +219,8 @@ struct FlashTcArgs {
     int Lq, Lout;             // local padded rows, local rows
     int zs;                   // z stride between owners in the key-side maps
     int d;                    // head dim of q, v, out: 128, or 64 (the workspace stays 128 wide)
+    int *tile_ctr;            // device counter of the dynamic tile queue (the launcher zeroes
+                              // it on the stream first), or null: static round-robin tiles
     uint32_t *err;
 };
 

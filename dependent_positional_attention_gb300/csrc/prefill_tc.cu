@@ -36,7 +36,9 @@
 // chain never waits behind the issue of a P V product.
 // Registers are rebalanced at start (setmaxnreg): the producer/MMA group
 // drops to 120 per thread, the two compute groups rise to 192 (the launch's
-// 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512).
+// 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512);
+// PaTH-FoX uses 136 / 184 (136*128 + 2*184*128 = 64512), the split at which
+// that instance compiles without spills.
 // Per step c the products are [U|S]_c and PV_{c+1} (one step late, so the
 // softmax has a full step of slack).  The first step of a tile reads Qh_b
 // from shared memory; the last (c = 0) needs no U and computes S_0 alone.
@@ -58,6 +60,13 @@ constexpr int kThreadsTC = 384;  // 3 warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Query tiles reach the roles through a ring of tile indices that the
+// producer fills: after the CTA's first tile, in the order of a device
+// counter (a dynamic queue over tiles sorted by decreasing work; each CTA
+// claims its next tile when it starts the current one), or round-robin when
+// there is no counter or for PaTH-FoX.  Readers: the two MMA issuers and
+// the carried-query and softmax groups.
+constexpr int kTileRing = 4, kTileReaders = 4;
 
 // Layout for head dimension D (128, or 64).  Rows of 64 bf16 are one
 // 128-byte swizzled sub-tile; a D-wide operand has D / 64 of them.  Dynamic
@@ -90,6 +99,8 @@ struct Bars {
     uint64_t v_full[Cfg<D>::kVSlots], v_empty[Cfg<D>::kVSlots];
     uint64_t qb_tma_full, qb_empty, u_full, s_full, qb_conv_full;
     uint64_t s_empty, p_full, o_done, drain, drain_pv;
+    uint64_t tile_full[kTileRing], tile_empty[kTileRing];
+    int tile_ring[kTileRing];  // query tile index, -1 once the queue is empty
     uint32_t tmem_base;
     int abort_word;
     alignas(16) float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
@@ -104,6 +115,28 @@ static_assert(smem_bytes<128>() <= 232448 && smem_bytes<64>() <= 232448,
 
 using tc::group_all;
 using tc::named_bar;
+
+// Next query tile from the ring (slot ts, phase parity ph), for a reader
+// role: -1 when the queue is exhausted, -2 when a wait gave up.  A group
+// reader (n threads behind named barrier id) reads the slot together and
+// releases it once every thread has read it; a single-thread reader passes
+// id = 0.
+template <int D>
+__device__ __forceinline__ int next_tile(Bars<D> &bars, int &ts, uint32_t &ph, int id, int n,
+                                         bool first_thread, uint32_t *err,
+                                         volatile int *abort_word) {
+    bool ok = mbar_wait(&bars.tile_full[ts], ph, err, abort_word, kWaitLimitNs);
+    if (id) ok = group_all(id, n, ok);
+    if (!ok) return -2;
+    const int t = *reinterpret_cast<volatile int *>(&bars.tile_ring[ts]);
+    if (id) named_bar(id, n);
+    if (first_thread) mbar_arrive(&bars.tile_empty[ts]);
+    if (++ts == kTileRing) {
+        ts = 0;
+        ph ^= 1;
+    }
+    return t;
+}
 
 // 2^x on the MUFU unit (inputs here are <= 0 after the max subtraction;
 // results below 2^-126 flush to zero, which a softmax weight can ignore).
@@ -218,6 +251,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         mbar_init(&bars.o_done, 1);
         mbar_init(&bars.drain, 1);
         mbar_init(&bars.drain_pv, 1);
+        for (int s = 0; s < kTileRing; ++s) {
+            mbar_init(&bars.tile_full[s], 1);
+            mbar_init(&bars.tile_empty[s], kTileReaders);
+        }
         bars.abort_word = 0;
         fence_mbar_init();
     }
@@ -230,7 +267,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     tc::fence_after_sync();
     const uint32_t tmem = bars.tmem_base;
     if (warp >= 8) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kFox ? 136 : 120) : "memory");
       if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -287,7 +324,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 return true;
             };
-            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+            int ts = 0;
+            uint32_t te_ph = 0;
+            int t_next = blockIdx.x;
+            // PaTH-FoX keeps the round-robin order: measured faster with it
+            // (0.628 against 0.645 ms at B8 H12 L4096), where the plain scan
+            // gains from the queue (0.572 -> 0.539 ms)
+            const bool dynamic = !kFox && a.tile_ctr != nullptr;
+            while (ok) {
+                // the CTA's next tile, published to the readers; the tile after
+                // it is claimed now, so that the counter's round trip overlaps
+                // this tile's loads
+                const int t = t_next < T ? t_next : -1;
+                if (t >= 0)
+                    t_next = dynamic ? (int)gridDim.x + atomicAdd(a.tile_ctr, 1) : t + gridDim.x;
+                ok = mbar_wait(&bars.tile_empty[ts], te_ph ^ 1, a.err, abort_word, lim);
+                if (!ok) break;
+                bars.tile_ring[ts] = t;
+                mbar_arrive(&bars.tile_full[ts]);
+                if (++ts == kTileRing) {
+                    ts = 0;
+                    te_ph ^= 1;
+                }
+                if (t < 0) break;
                 const Tile tl = tile_of(t, a);
                 const int b = tl.b, bh = tl.bh;
                 if (b == 0) continue;
@@ -323,7 +382,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             uint32_t pph = 0, qt_ph = 0, qc_ph = 0, se_ph = 0;
             const uint32_t qb_lo = tc::desc_lo(sQb, false);
             bool ok = true;
-            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+            int ts = 0;
+            uint32_t tf_ph = 0;
+            while (ok) {
+                const int t = next_tile(bars, ts, tf_ph, 0, 1, true, a.err, abort_word);
+                if (t < 0) break;
                 const int b = tile_of(t, a).b;
                 if (b == 0) continue;
                 for (int c = b - 1; c >= 0 && ok; --c) {
@@ -379,7 +442,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             bool ok = true;
             // O already holds the chunk's own attention block (written by the
             // softmax group), so every PV accumulates: V_{b-1}, ..., V_0 per tile
-            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+            int ts = 0;
+            uint32_t tf_ph = 0;
+            while (ok) {
+                const int t = next_tile(bars, ts, tf_ph, 0, 1, true, a.err, abort_word);
+                if (t < 0) break;
                 const int b = tile_of(t, a).b;
                 for (int c = b - 1; c >= 0 && ok; --c) {
                     ok = mbar_wait(&bars.v_full[vs], vph, a.err, abort_word, lim) &&
@@ -403,14 +470,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         __syncwarp();
       }
     } else {
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFox ? 184 : 192) : "memory");
       if (warp < 4) {
         // ------------------------------------------------------------ carried query
         const int quad = warp & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t uf_ph = 0, qt_ph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        int ts = 0;
+        uint32_t tf_ph = 0;
+        while (ok) {
+            const int t = next_tile(bars, ts, tf_ph, 1, 128, threadIdx.x == 0, a.err, abort_word);
+            if (t < 0) break;
             const int b = tile_of(t, a).b;
             if (b == 0) continue;
             ok = group_all(1, 128, mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim));
@@ -458,7 +529,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         constexpr bool fox = kFox;
         uint32_t sf_ph = 0, od_ph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        int ts = 0;
+        uint32_t tf_ph = 0;
+        while (ok) {
+            const int t = next_tile(bars, ts, tf_ph, 2, 128, threadIdx.x == 128, a.err, abort_word);
+            if (t < 0) break;
             const Tile tl = tile_of(t, a);
             const int b = tl.b, bh = tl.bh;
             const float *Frow = fox ? a.F + (size_t)bh * a.Lp : nullptr;
@@ -659,6 +734,10 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
     const int smem = a.d == 64 ? smem_bytes<64>() : smem_bytes<128>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (a.tile_ctr) {
+        e = cudaMemsetAsync(a.tile_ctr, 0, sizeof(int), st);
+        if (e != cudaSuccess) return e;
+    }
     kern<<<grid, kThreadsTC, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
