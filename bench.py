@@ -71,7 +71,7 @@ DECODE_TRAFFIC_PER_KEY = {False: (805.74e6 + 354.32e6) / 1573440,
                           True: (812.07e6 + 350.02e6) / 1573440}
 
 # DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
-SCAN_TRAFFIC_B2 = 144.819456e6 + 11.021568e6
+SCAN_TRAFFIC_B2 = 144.668416e6 + 10.739712e6
 
 
 def load_peaks():
