@@ -349,6 +349,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (t < 0) break;
                 const Tile tl = tile_of(t, a);
                 const int b = tl.b, bh = tl.bh;
+                // the softmax group starts the tile from the prep's own-chunk
+                // output and log-sum-exp, a couple of steps from now: bring them
+                // to L2 (they were written by the prep and have left it since)
+                tc::bulk_prefetch_l2(a.OD + ((size_t)bh * a.Lq + tl.i * kC) * 128, kC * 128 * 2);
+                tc::bulk_prefetch_l2(a.LSD + (size_t)bh * a.Lq + tl.i * kC, kC * 4);
                 if (b == 0) continue;
                 ok = mbar_wait(&bars.qb_empty, qe_ph ^ 1, a.err, abort_word, lim);
                 qe_ph ^= 1;

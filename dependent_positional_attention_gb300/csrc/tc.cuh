@@ -65,6 +65,12 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
+// Brings `bytes` (a multiple of 16) at the 16-byte aligned global address
+// `p` into L2, without waiting.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
