@@ -67,8 +67,8 @@ def backward_flops(B, H, L, d, C=CHUNK):
 
 # DRAM read + write bytes per cached key of decode_split_kernel<128, fox>, from
 # ncu on B16 H12 with 8195 cached tokens (1,573,440 keys per launch)
-DECODE_TRAFFIC_PER_KEY = {False: (805.74e6 + 354.32e6) / 1573440,
-                          True: (812.07e6 + 350.02e6) / 1573440}
+DECODE_TRAFFIC_PER_KEY = {False: (805.738240e6 + 354.663424e6) / 1573440,
+                          True: (812.037376e6 + 349.548032e6) / 1573440}
 
 # DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
 SCAN_TRAFFIC_B2 = 144.668416e6 + 10.739712e6

@@ -72,12 +72,13 @@ __device__ __forceinline__ float group_sum(float v) {
 }
 
 constexpr int kDecThreads = 256;
-// Keys in flight per thread and loop iteration: 8 for the PaTH step (88% of
-// measured HBM copy bandwidth on GB300 at a 64K-token cache, against 76% with
-// 4); the PaTH-FoX step, which also loads each key's forget-gate prefix, runs
-// best with 4 (84% against 66% with 8).
+// Keys in flight per thread and loop iteration: 8 (88% of measured HBM copy
+// bandwidth on GB300 at a 64K-token cache, against 76% with 4).  The split
+// kernel is held to 128 registers (two CTAs per SM): left free, the PaTH-FoX
+// instance took 147 and ran one CTA per SM at 60% of the bandwidth; held,
+// it runs at 88% (it ran at 84% with 4 keys in flight).
 template <bool FOX>
-__host__ __device__ constexpr int dec_unroll() { return FOX ? 4 : 8; }
+__host__ __device__ constexpr int dec_unroll() { return 8; }
 
 // F_t = F_{t-1} + log f_t of the new token (PaTH-FoX), F_{-1} = 0.
 __device__ __forceinline__ float fox_prefix_now(const DecodeArgs &a, int bh) {
@@ -86,7 +87,7 @@ __device__ __forceinline__ float fox_prefix_now(const DecodeArgs &a, int bh) {
 }
 
 template <int D, bool FOX>
-__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(DecodeArgs a) {
     constexpr int UNROLL = dec_unroll<FOX>();
     constexpr int LPK = D / 8;                      // lanes per key
     constexpr int KPW = 32 / LPK;                   // keys per warp per load
@@ -133,12 +134,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(DecodeArgs a)
             if (j < j1) {
                 kr[u] = *reinterpret_cast<const uint4 *>(kc + (size_t)j * D);
                 vr[u] = ld_stream(vc + (size_t)j * D);
-                if (FOX) fj[u] = fc[j];
             } else {
                 kr[u] = make_uint4(0, 0, 0, 0);
                 vr[u] = make_uint4(0, 0, 0, 0);
-                if (FOX) fj[u] = 0.f;
             }
+        }
+        if (FOX) {
+            // lane u of the key group loads the prefix of the group's key u;
+            // the group's lanes then take all UNROLL of them by shuffles
+            const int jl = base + g + sub * GROUPS;
+            const float fl = (sub < UNROLL && jl < j1) ? fc[jl] : 0.f;
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) fj[u] = __shfl_sync(0xffffffffu, fl, lane - sub + u);
         }
         float s[UNROLL];
 #pragma unroll
