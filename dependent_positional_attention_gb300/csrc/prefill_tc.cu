@@ -300,6 +300,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (c >= 1) tc::tma_load_3d(ds, &maps.pm, 64 * sub, y, z, full);
                     tc::tma_load_3d(ds + D * 128, &maps.kh, 64 * sub, y, z, full);
                 }
+                // PaTH-FoX: the softmax group reads the chunk's prefixes about a
+                // step before the product runs; bring them to L2 with the pair
+                if (kFox) tc::bulk_prefetch_l2(a.F + (size_t)bh * a.Lp + (size_t)c * kC, kC * 4);
                 pair_par[ps] = (int)pph;
                 if (++ps == kPairSlots) {
                     ps = 0;
@@ -579,14 +582,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
             tc::tmem_wait_st();
             float m = lsd * kLog2e, l = 1.f;
+            // FoX: the prefixes of the step's key chunk, loaded one step ahead
+            // (a load at the step's start would hold the group's barrier)
+            float fcol_next = fox ? Frow[(b - 1) * kC + r] : 0.f;
+            float fref_next = fox ? Frow[(b - 1) * kC] : 0.f;
             for (int c = b - 1; c >= 0; --c) {
                 // FoX: the bias fi - F_j splits into a row term (fi - F_ref) and
                 // a column term F_j - F_ref, F_ref the chunk's first prefix
                 float dlt = 0.f;
                 if (fox) {
-                    const float fref = Frow[c * kC];
-                    bars.fsm[r] = (Frow[c * kC + r] - fref) * kLog2e;
+                    const float fref = fref_next;
+                    bars.fsm[r] = (fcol_next - fref) * kLog2e;
                     dlt = fi - fref * kLog2e;
+                    if (c >= 1) {
+                        fcol_next = Frow[(c - 1) * kC + r];
+                        fref_next = Frow[(c - 1) * kC];
+                    }
                 }
                 ok = group_all(2, 128, mbar_wait(&bars.s_full, sf_ph, a.err, abort_word, lim));
                 if (!ok) break;
