@@ -64,7 +64,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // producer fills: after the CTA's first tile, in the order of a device
 // counter (a dynamic queue over tiles sorted by decreasing work; each CTA
 // claims its next tile when it starts the current one), or round-robin when
-// there is no counter or for PaTH-FoX.  Readers: the two MMA issuers and
+// there is no counter.  Readers: the two MMA issuers and
 // the carried-query and softmax groups.
 constexpr int kTileRing = 4, kTileReaders = 4;
 
@@ -330,10 +330,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             int ts = 0;
             uint32_t te_ph = 0;
             int t_next = blockIdx.x;
-            // PaTH-FoX keeps the round-robin order: measured faster with it
-            // (0.628 against 0.645 ms at B8 H12 L4096), where the plain scan
-            // gains from the queue (0.572 -> 0.539 ms)
-            const bool dynamic = !kFox && a.tile_ctr != nullptr;
+            const bool dynamic = a.tile_ctr != nullptr;
             while (ok) {
                 // the CTA's next tile, published to the readers; the tile after
                 // it is claimed now, so that the counter's round trip overlaps
