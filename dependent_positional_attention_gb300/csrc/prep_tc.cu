@@ -31,13 +31,15 @@
 //   P2 G -> fp32 smem (region Ra)             | QW -> B, KW -> C, QK -> D
 //   P3 solve T (fp32, region Rb)              |   (run during the solve)
 //   P4 T -> bf16, -(M_le*QW) -> bf16  (rdy4a) | Wt = T W -> A
-//      (M_gt*KW) -> bf16              (rdy4b) | Y = KWm T^T -> C, then V load
+//      (M_gt*KW) -> bf16              (rdy4b) | Y = KWm T^T -> C
 //   P6 Wt -> bf16 (half 0, rdy6a),            | -(M_le*QW) Wt -> B       (b1)
 //      Y -> bf16 (half 1, rdy6b)              | Y W -> A (b2), W^T Wt -> C (b3),
-//                                             | += -(M_le*QW) Y^T -> D   (b4)
-//   P8 Qh (half 0, after b1), Kh (half 1,     | Qh, Kh, Pm stored by TMA; the
-//      after b2), Pm (after b3)       (rdy8)  | next chunk's W, Q, K loaded
-//   P9 causal softmax of Sd -> P      (rdy9)  | P V -> C
+//                                             | += -(M_le*QW) Y^T -> D   (b4);
+//                                             | V over the T tile
+//   P8 Qh (half 0, after b1), Kh (half 1,     | Qh, Kh, Pm stored by TMA
+//      after b2), Pm (after b3)       (rdy8)  |
+//   P9 causal softmax of Sd -> P      (rdy9)  | P V -> C; then the next chunk's
+//                                             | W, Q, K over the stored tiles
 //   P10 own-chunk output and LSE      (rdy10) | output stored; next G
 // The two 64 KB staging regions swap roles every chunk: Ra holds G (fp32),
 // then the T / -(M_le*QW) / V / P / output tiles, Rb holds T (fp32), then the
@@ -265,13 +267,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 if (!wait(&bars.rdy4b, ph)) break;
                 gemm(tmem + kColC, sY, sT, false, false);
                 tc::mma_commit(&bars.y_done);
-                // the chunk's values, for its own attention block, over the T tile
-                if (!wait(&bars.y_done, ph)) break;
-                mbar_arrive_expect_tx(&bars.vbar, kTile);
-                tc::tma_load_3d(smem + (ph ? kOffR2 : kOffR1), &maps.v, 0, r0, bh, &bars.vbar);
-                tc::tma_load_3d(smem + (ph ? kOffR2 : kOffR1) + kTile / 2, &maps.v, 64, r0, bh,
-                                &bars.vbar);
-                pend_v = ph;
                 // -(M_le*QW) Wt -> B
                 if (!wait(&bars.rdy6a, ph)) break;
                 gemm(tmem + kColB, sQm, sWt, true, false);
@@ -292,6 +287,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 tc::mma_commit(&bars.b3);
                 gemm(tmem + kColD, sQm, sY, false, true);
                 tc::mma_commit(&bars.b4);
+                // the chunk's values, for its own attention block, over the T tile
+                // (free once Y = KWm T^T is complete; loaded after b1-b4 so that
+                // this wait does not hold them up)
+                if (!wait(&bars.y_done, ph)) break;
+                mbar_arrive_expect_tx(&bars.vbar, kTile);
+                tc::tma_load_3d(smem + (ph ? kOffR2 : kOffR1), &maps.v, 0, r0, bh, &bars.vbar);
+                tc::tma_load_3d(smem + (ph ? kOffR2 : kOffR1) + kTile / 2, &maps.v, 64, r0, bh,
+                                &bars.vbar);
+                pend_v = ph;
                 // Qh, Kh, Pm -> global; then the next chunk's W, Q, K over them
                 if (!wait(&bars.rdy8, ph)) break;
 #pragma unroll
@@ -301,10 +305,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     tc::tma_store_3d(&maps.pm, smem + kOffW + x * (kTile / 2), 64 * x, r0, bh);
                 }
                 tc::bulk_commit();
-                if (next < total) {
-                    tc::bulk_wait_read();
-                    issue_loads(next, it + 1);
-                }
                 if (!wait(&bars.vbar, ph)) break;
                 pend_v = -1;
                 if (a.copy_v) {
@@ -316,12 +316,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                                          64 * x, r0, bh);
                     tc::bulk_commit();
                 }
-                // P V -> C (Pm in C was read in P8)
+                // P V -> C (Pm in C was read in P8), ahead of the wait for the
+                // stores above to read their tiles, which takes a while
                 if (!wait(&bars.rdy9, ph)) break;
                 gemm(tmem + kColC, sQm, sT, true, false);
                 tc::mma_commit(&bars.pv_done);
-                // the next chunk's G -> A (Kh's YW in A was read in P8)
+                // the next chunk's W, Q, K over the stored tiles, then its G -> A
+                // (Kh's YW in A was read in P8)
                 if (next < total) {
+                    tc::bulk_wait_read();
+                    issue_loads(next, it + 1);
                     if (!wait(&bars.tma_w, ph ^ 1)) break;
                     pend_w = -1;
                     gemm(tmem + kColA, sW, sW, false, false);
