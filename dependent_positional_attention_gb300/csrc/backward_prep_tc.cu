@@ -225,31 +225,85 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 // Ti = (I + strict_lower(diag(beta) G))^{-1} by the tensor-core prep's blocked
 // solve in inverse mode, written as bf16 Ti and T = Ti diag(beta).  One block
 // of 256 threads per chunk.
+// 16 bytes global -> shared without registers (cp.async, L2 only); the
+// group below completes in issue order.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Ti = (I + strict_lower(diag(beta) G))^{-1} and T = Ti diag(beta) (bf16) of
+// every chunk.  Persistent: each CTA solves its chunks one after another
+// while the next chunk's G streams into the second of two shared buffers.
 __global__ void __launch_bounds__(utc::kThr) bwd_solve_kernel(const float *G, const float *beta,
                                                                __nv_bfloat16 *T, __nv_bfloat16 *Ti,
-                                                               int L, int Lp, int N) {
+                                                               int BH, int L, int Lp, int N) {
     extern __shared__ uint8_t smem_raw[];
-    float *Gs = reinterpret_cast<float *>(
+    float *Gbuf = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
-    float *Tf = Gs + kC * kC;
-    float *bs = Tf + kC * kC;
-    const int chunk = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-    const int c0 = chunk * kC, n = min(kC, L - c0);
-    const size_t base = ((size_t)bh * Lp + c0) * kC;
-    if (tid < kC) bs[tid] = tid < n ? beta[(size_t)bh * L + c0 + tid] : 0.f;
-    for (int e = tid; e < kC * kC / 4; e += utc::kThr) {
-        const int r = e / (kC / 4), c = (e % (kC / 4)) * 4;
-        *reinterpret_cast<float4 *>(Gs + utc::sw(r, c)) = reinterpret_cast<const float4 *>(G + base)[e];
+    float *Tf = Gbuf + 2 * kC * kC;
+    float *bsm = Tf + kC * kC;  // two beta rows
+    const int tid = threadIdx.x;
+    const int total = N * BH;
+    // G of job -> buffer b, in the solve's swizzled layout; beta alongside
+    auto fetch = [&](int job, int b) {
+        const int chunk = job % N, bh = job / N;
+        const int c0 = chunk * kC, n = min(kC, L - c0);
+        const float *src = G + ((size_t)bh * Lp + c0) * kC;
+        float *dst = Gbuf + b * kC * kC;
+        for (int e = tid; e < kC * kC / 4; e += utc::kThr) {
+            const int r = e / (kC / 4), c = (e % (kC / 4)) * 4;
+            cp_async16(dst + utc::sw(r, c), src + (size_t)e * 4);
+        }
+        if (tid < kC) bsm[b * kC + tid] = tid < n ? beta[(size_t)bh * L + c0 + tid] : 0.f;
+        cp_async_commit();
+    };
+    int k = 0;
+    if (blockIdx.x < total) fetch(blockIdx.x, 0);
+    for (int job = blockIdx.x; job < total; job += gridDim.x, ++k) {
+        const int b = k & 1;
+        const int next = job + gridDim.x;
+        // the next chunk's G streams in while this one is solved
+        if (next < total) {
+            fetch(next, b ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        float *Gs = Gbuf + b * kC * kC;
+        const float *bs = bsm + b * kC;
+        utc::ut_solve<true>(Gs, Tf, bs, tid);
+        __syncthreads();
+        // Ti and T rows, eight columns a store
+        const int chunk = job % N, bh = job / N;
+        const size_t base = ((size_t)bh * Lp + chunk * kC) * kC;
+        for (int e = tid; e < kC * kC / 8; e += utc::kThr) {
+            const int r = e / (kC / 8), c = (e % (kC / 8)) * 8;
+            const float4 t0 = *reinterpret_cast<const float4 *>(Tf + utc::sw(r, c));
+            const float4 t1 = *reinterpret_cast<const float4 *>(Tf + utc::sw(r, c + 4));
+            const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            uint32_t wi[4], wt[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                wi[q] = tc::pack2(t[2 * q], t[2 * q + 1]);
+                wt[q] = tc::pack2(t[2 * q] * bs[c + 2 * q], t[2 * q + 1] * bs[c + 2 * q + 1]);
+            }
+            *reinterpret_cast<uint4 *>(Ti + base + (size_t)e * 8) = make_uint4(wi[0], wi[1], wi[2], wi[3]);
+            *reinterpret_cast<uint4 *>(T + base + (size_t)e * 8) = make_uint4(wt[0], wt[1], wt[2], wt[3]);
+        }
+        // every thread is done with this buffer before the fetch after next
+        // (issued at the start of the next job) reuses it
+        __syncthreads();
     }
-    __syncthreads();
-    utc::ut_solve<true>(Gs, Tf, bs, tid);
-    __syncthreads();
-    for (int e = tid; e < kC * kC; e += utc::kThr) {
-        const int r = e / kC, c = e % kC;
-        const float t = Tf[utc::sw(r, c)];
-        Ti[base + e] = __float2bfloat16_rn(t);
-        T[base + e] = __float2bfloat16_rn(t * bs[c]);
-    }
+    cp_async_wait<0>();
 }
 
 // D = dout . out - dlse for every row of the padded layout [BH][Lp] (0 on the
@@ -353,11 +407,18 @@ cudaError_t launch_chunk_gemm_tc(const ChunkGemmMaps &maps, const ChunkGemmArgs 
 
 cudaError_t launch_bwd_solve(const float *G, const float *beta, __nv_bfloat16 *T,
                              __nv_bfloat16 *Ti, int BH, int L, int Lp, int N, cudaStream_t st) {
-    const size_t sm = sizeof(float) * (2 * kC * kC + kC) + 16;
+    const size_t sm = sizeof(float) * (3 * kC * kC + 2 * kC) + 16;
     cudaError_t e =
         cudaFuncSetAttribute(bwd_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    bwd_solve_kernel<<<dim3(N, BH), utc::kThr, sm, st>>>(G, beta, T, Ti, L, Lp, N);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long total = (long long)N * BH;
+    const int grid = (int)(total < sms ? total : sms);
+    if (grid <= 0) return cudaSuccess;
+    bwd_solve_kernel<<<grid, utc::kThr, sm, st>>>(G, beta, T, Ti, BH, L, Lp, N);
     return cudaGetLastError();
 }
 
