@@ -606,10 +606,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 tc::fence_before_sync();
                 named_bar(2, 128);  // also publishes this chunk's FoX prefix
                 if (threadIdx.x == 128) mbar_arrive(&bars.s_empty);
+                // row extremes over interleaved partial results, so that no
+                // chain of 128 dependent max operations sits in the step (the
+                // maximum is exact, so the order changes nothing)
                 float mx = -INFINITY;
                 if (kFox) {
                     // the chunk's column prefixes, four per shared-memory load
                     const uint32_t fsm_s = smem_u32(bars.fsm);
+                    float mp[4];  // four here: eight push this instance into spills
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mp[i] = -INFINITY;
 #pragma unroll
                     for (int j4 = 0; j4 < kC / 4; ++j4) {
                         const uint4 f4 = tc::lds128(fsm_s + 16 * j4);
@@ -619,19 +625,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                             const int j = 4 * j4 + e;
                             const float t = fmaf(__uint_as_float(v[j]), sl2, -__uint_as_float(fw[e]));
                             v[j] = __float_as_uint(t);
-                            mx = fmaxf(mx, t);
+                            mp[e] = fmaxf(mp[e], t);
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, mp[i]);
                     mx += dlt;
                 } else {
                     // max of the scaled logits from the raw extreme (min if scale < 0)
+                    float mp[8];
                     if (sl2 >= 0.f) {
 #pragma unroll
-                        for (int j = 0; j < kC; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+                        for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < kC; ++j) mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(v[j]));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, mp[i]);
                     } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mp[i] = INFINITY;
+#pragma unroll
+                        for (int j = 0; j < kC; ++j) mp[j & 7] = fminf(mp[j & 7], __uint_as_float(v[j]));
                         mx = INFINITY;
 #pragma unroll
-                        for (int j = 0; j < kC; ++j) mx = fminf(mx, __uint_as_float(v[j]));
+                        for (int i = 0; i < 8; ++i) mx = fminf(mx, mp[i]);
                     }
                     mx *= sl2;
                 }

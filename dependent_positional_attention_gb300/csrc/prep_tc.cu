@@ -530,7 +530,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 wait(&bars.b4, ph);
                 uint32_t v[64];
                 tc::tmem_ld64(tmem + lane_off + kColD + half * 64, v);
-                float mx = -INFINITY;
+                // eight interleaved partial maxima (exact in any order), so that
+                // no chain of 64 dependent max operations sits in the phase
+                float mp[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
                     const int j = half * 64 + i;
@@ -538,8 +542,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     if (fox) x += fi - bars.fsm[j];
                     x = (j <= r) ? x : -INFINITY;
                     v[i] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
+                    mp[i & 7] = fmaxf(mp[i & 7], x);
                 }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx = fmaxf(mx, mp[i]);
                 red[0][half][r] = mx;
                 tc::named_bar(kBarAll, kCompute);
                 m_row = fmaxf(red[0][0][r], red[0][1][r]);  // finite: column r is unmasked
