@@ -24,9 +24,14 @@
 // there as the A operand, so that shared memory only carries B operands.
 //
 // One CTA per SM (persistent), tiles ordered by decreasing work.  Warp roles:
-//   warps 0-3   carried-query warpgroup: U_c (TMEM, fp32) -> Qt bf16 (TMEM)
-//   warps 4-7   softmax warpgroup: logits, online softmax with lazy rescale
-//               of O, P -> bf16 (TMEM), epilogue (out, lse)
+//   warps 0-7   row group: warp w owns TMEM lanes 32 (w & 3) .. + 31 (query
+//               rows) and column half w >> 2.  Per step it converts its half
+//               of U_c (fp32) into the next carried rows Qt (bf16, TMEM),
+//               then runs the online softmax over its half of the logits
+//               (row maxima exchanged with the other half's warp, lazy
+//               rescale of its half of O, P -> bf16 in TMEM); epilogue (out,
+//               lse) per half.  Two warps per scheduler share the work that
+//               a carried-query and a softmax warpgroup used to split by role.
 //   warp 8      TMA producer: Qh_b, then two rings: [Pm_c^T | Kh_c] pairs
 //               (64 KB slots) and V_c (32 KB slots)
 //   warp 9      MMA issuer of the [U|S] products (one thread), TMEM owner
@@ -35,14 +40,14 @@
 // O) and each thread's commits track only its own MMAs, so the carried-query
 // chain never waits behind the issue of a P V product.
 // Registers are rebalanced at start (setmaxnreg): the producer/MMA group
-// drops to 120 per thread, the two compute groups rise to 192 (the launch's
+// drops to 120 per thread, the row group rises to 192 (the launch's
 // 168 x 384 budget is redistributed exactly: 120*128 + 2*192*128 = 64512);
 // PaTH-FoX uses 136 / 184 (136*128 + 2*184*128 = 64512), the split at which
 // that instance compiles without spills.
 // Per step c the products are [U|S]_c and PV_{c+1} (one step late, so the
 // softmax has a full step of slack).  The first step of a tile reads Qh_b
 // from shared memory; the last (c = 0) needs no U and computes S_0 alone.
-// Chunk-0 tiles need no scan: the softmax group copies the prep's result.
+// Chunk-0 tiles need no scan: the row group copies the prep's result.
 // TMEM columns: [0,128) U, [128,256) S, [256,320) Qt (bf16 pairs),
 // [320,384) P (bf16 pairs), [384,512) O.
 // Every wait is bounded; on timeout the kernel sets the device error flag,
@@ -64,9 +69,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // producer fills: after the CTA's first tile, in the order of a device
 // counter (a dynamic queue over tiles sorted by decreasing work; each CTA
 // claims its next tile when it starts the current one), or round-robin when
-// there is no counter.  Readers: the two MMA issuers and
-// the carried-query and softmax groups.
-constexpr int kTileRing = 4, kTileReaders = 4;
+// there is no counter.  Readers: the two MMA issuers and the row group.
+constexpr int kTileRing = 4, kTileReaders = 3;
 
 // Layout for head dimension D (128, or 64).  Rows of 64 bf16 are one
 // 128-byte swizzled sub-tile; a D-wide operand has D / 64 of them.  Dynamic
@@ -97,13 +101,14 @@ template <int D>
 struct Bars {
     uint64_t pair_full[Cfg<D>::kPairSlots], pair_empty[Cfg<D>::kPairSlots];
     uint64_t v_full[Cfg<D>::kVSlots], v_empty[Cfg<D>::kVSlots];
-    uint64_t qb_tma_full, qb_empty, u_full, s_full, qb_conv_full;
+    uint64_t qb_tma_full, qb_empty, s_full, qb_conv_full;
     uint64_t s_empty, p_full, o_done, drain, drain_pv;
     uint64_t tile_full[kTileRing], tile_empty[kTileRing];
     int tile_ring[kTileRing];  // query tile index, -1 once the queue is empty
     uint32_t tmem_base;
     int abort_word;
     alignas(16) float fsm[kC];  // FoX prefix of the current key chunk (log2 units)
+    float xm[2][kC];            // per-row maxima (then partial sums) of the two column halves
 };
 // barriers/misc after the rings, plus slack to align the dynamic base to 1024
 template <int D>
@@ -242,12 +247,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             mbar_init(&bars.v_empty[s], 1);
         }
         mbar_init(&bars.qb_tma_full, 1);
-        mbar_init(&bars.qb_empty, 2);  // MMA commit + carried-query group
-        mbar_init(&bars.u_full, 1);
+        mbar_init(&bars.qb_empty, 1);  // the MMA commit of the tile's first product
         mbar_init(&bars.s_full, 1);
-        mbar_init(&bars.qb_conv_full, 1);
-        mbar_init(&bars.s_empty, 1);
-        mbar_init(&bars.p_full, 1);
+        // one arrival per warp of the row group
+        mbar_init(&bars.qb_conv_full, 8);
+        mbar_init(&bars.s_empty, 8);
+        mbar_init(&bars.p_full, 8);
         mbar_init(&bars.o_done, 1);
         mbar_init(&bars.drain, 1);
         mbar_init(&bars.drain_pv, 1);
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     if (c >= 1) tc::tma_load_3d(ds, &maps.pm, 64 * sub, y, z, full);
                     tc::tma_load_3d(ds + D * 128, &maps.kh, 64 * sub, y, z, full);
                 }
-                // PaTH-FoX: the softmax group reads the chunk's prefixes about a
+                // PaTH-FoX: the row group reads the chunk's prefixes about a
                 // step before the product runs; bring them to L2 with the pair
                 if (kFox) tc::bulk_prefetch_l2(a.F + (size_t)bh * a.Lp + (size_t)c * kC, kC * 4);
                 pair_par[ps] = (int)pph;
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (t < 0) break;
                 const Tile tl = tile_of(t, a);
                 const int b = tl.b, bh = tl.bh;
-                // the softmax group starts the tile from the prep's own-chunk
+                // the row group starts the tile from the prep's own-chunk
                 // output and log-sum-exp, a couple of steps from now: bring them
                 // to L2 (they were written by the prep and have left it since)
                 tc::bulk_prefetch_l2(a.OD + ((size_t)bh * a.Lq + tl.i * kC) * 128, kC * 128 * 2);
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 for (int c = b - 1; c >= 0 && ok; --c) {
                     const bool first = (c == b - 1);
                     // the carried rows of this step: Qh_b in shared memory, or
-                    // the carried-query group's conversion of the previous U
+                    // the row group's conversion of the previous U
                     if (first) {
                         ok = mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim);
                         qt_ph ^= 1;
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         ok = mbar_wait(&bars.qb_conv_full, qc_ph, a.err, abort_word, lim);
                         qc_ph ^= 1;
                     }
-                    // the softmax group has read the previous S
+                    // the row group has read the previous S
                     ok = ok && mbar_wait(&bars.s_empty, se_ph ^ 1, a.err, abort_word, lim);
                     se_ph ^= 1;
                     ok = ok && mbar_wait(&bars.pair_full[ps], pph, a.err, abort_word, lim);
@@ -425,10 +430,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         ps = 0;
                         pph ^= 1;
                     }
-                    // separate completions for the two readers: the carried-query
-                    // group sees only the steps that produce U, the softmax group
-                    // every step, so each waits on every phase of its own barrier
-                    if (c >= 1) tc::mma_commit(&bars.u_full);
+                    // U (when there is one) and S, for the row group
                     tc::mma_commit(&bars.s_full);
                     // Qh_b's tile is free once the first step's product completes
                     if (first) tc::mma_commit(&bars.qb_empty);
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             uint32_t vph = 0, pf_ph = 0;
             bool ok = true;
             // O already holds the chunk's own attention block (written by the
-            // softmax group), so every PV accumulates: V_{b-1}, ..., V_0 per tile
+            // row group), so every PV accumulates: V_{b-1}, ..., V_0 per tile
             int ts = 0;
             uint32_t tf_ph = 0;
             while (ok) {
@@ -476,60 +478,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFox ? 184 : 192) : "memory");
-      if (warp < 4) {
-        // ------------------------------------------------------------ carried query
-        const int quad = warp & 3;
-        const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t uf_ph = 0, qt_ph = 0;
-        bool ok = true;
-        int ts = 0;
-        uint32_t tf_ph = 0;
-        while (ok) {
-            const int t = next_tile(bars, ts, tf_ph, 1, 128, threadIdx.x == 0, a.err, abort_word);
-            if (t < 0) break;
-            const int b = tile_of(t, a).b;
-            if (b == 0) continue;
-            ok = group_all(1, 128, mbar_wait(&bars.qb_tma_full, qt_ph, a.err, abort_word, lim));
-            if (!ok) break;
-            qt_ph ^= 1;
-            // second arrival on qb_empty (the first is the MMA commit after the
-            // first product of this tile): the next Qh load waits for this group
-            // too, so the Qh barrier never runs a phase ahead of it.
-            named_bar(1, 128);
-            if (threadIdx.x == 0) mbar_arrive(&bars.qb_empty);
-            for (int c = b - 1; c >= 1; --c) {
-                // [U|S]_c complete: U is the next carried rows, and the product
-                // has read the current ones, so they may be overwritten
-                ok = group_all(1, 128, mbar_wait(&bars.u_full, uf_ph, a.err, abort_word, lim));
-                if (!ok) break;
-                uf_ph ^= 1;
-                tc::fence_after_sync();
-                uint32_t pk[D / 2];
-                {
-                    uint32_t v[D];
-                    if constexpr (D == 128)
-                        tc::tmem_ld128(lane_addr + kColU, v);
-                    else
-                        tc::tmem_ld64(lane_addr + kColU, v);
-#pragma unroll
-                    for (int j = 0; j < D / 2; ++j)
-                        pk[j] = pack_bf16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                }
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h)
-                    tc::tmem_st32(lane_addr + kColQt + 32 * h,
-                                  *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * h));
-                tc::tmem_wait_st();
-                tc::fence_before_sync();
-                named_bar(1, 128);
-                if (threadIdx.x == 0) mbar_arrive(&bars.qb_conv_full);
-            }
-        }
-      } else {
-        // ------------------------------------------------------------ softmax
-        const int quad = warp & 3;
+      {
+        // ------------------------------------------------------------ rows
+        // Warps 0-7: warp w owns TMEM lane quadrant w & 3 (32 query rows) and
+        // column half w >> 2.  Per step it turns its half of U into the next
+        // carried rows, then runs the online softmax over its half of S; the
+        // two warps of a quadrant exchange the row maximum through shared
+        // memory (pair barrier 2 + quadrant, 64 threads) and keep partial row
+        // sums until the epilogue.  Two warps per scheduler hide each other's
+        // latency, where one warp per row ran the softmax alone.
+        const int quad = warp & 3, hh = warp >> 2;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+        constexpr int kOH = D / 2;  // columns of O (and of U) per half
+        const int pair_bar = 2 + quad;
         const float sl2 = a.scale * kLog2e;
         constexpr bool fox = kFox;
         uint32_t sf_ph = 0, od_ph = 0;
@@ -537,7 +499,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         int ts = 0;
         uint32_t tf_ph = 0;
         while (ok) {
-            const int t = next_tile(bars, ts, tf_ph, 2, 128, threadIdx.x == 128, a.err, abort_word);
+            const int t = next_tile(bars, ts, tf_ph, 1, 256, threadIdx.x == 0, a.err, abort_word);
             if (t < 0) break;
             const Tile tl = tile_of(t, a);
             const int b = tl.b, bh = tl.bh;
@@ -546,23 +508,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             const int row = b * kC + r;       // in the whole sequence
             const int lrow = tl.i * kC + r;   // in the local rows
             // the prep's own-chunk output is 128 wide (head_dim 64 zero-padded)
-            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lq + lrow) * 128;
+            const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lq + lrow) * 128 + hh * kOH;
             const float lsd = a.LSD[(size_t)bh * a.Lq + lrow];
             if (b == 0) {
                 // the chunk attends only to itself: the prep's result is final
                 if (row < a.L) {
-                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D;
+                    __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D + hh * kOH;
 #pragma unroll
-                    for (int j = 0; j < D / 8; ++j)
+                    for (int j = 0; j < kOH / 8; ++j)
                         reinterpret_cast<uint4 *>(orow)[j] = reinterpret_cast<const uint4 *>(odrow)[j];
-                    if (a.lse) a.lse[(size_t)bh * a.Lout + lrow] = lsd;
+                    if (hh == 0 && a.lse) a.lse[(size_t)bh * a.Lout + lrow] = lsd;
                 }
                 continue;
             }
             // start from the chunk's own block: O = OD (weights summing to 1
-            // against the reference m = LSD in log2 units), l = 1
+            // against the reference m = LSD in log2 units); half 0 carries
+            // that weight in its partial row sum
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < kOH / 32; ++cc) {
                 uint32_t o[32];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -575,13 +538,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                         o[q * 8 + 2 * e + 1] = __float_as_uint(f.y);
                     }
                 }
-                tc::tmem_st32(lane_addr + kColO + cc * 32, o);
+                tc::tmem_st32(lane_addr + kColO + hh * kOH + cc * 32, o);
             }
             tc::tmem_wait_st();
-            float m = lsd * kLog2e, l = 1.f;
+            float m = lsd * kLog2e, l = hh == 0 ? 1.f : 0.f;
             // FoX: the prefixes of the step's key chunk, loaded one step ahead
-            // (a load at the step's start would hold the group's barrier)
-            float fcol_next = fox ? Frow[(b - 1) * kC + r] : 0.f;
+            // (a load at the step's start would hold the group's barrier);
+            // half 0 publishes them, one per thread
+            float fcol_next = (fox && hh == 0) ? Frow[(b - 1) * kC + r] : 0.f;
             float fref_next = fox ? Frow[(b - 1) * kC] : 0.f;
             for (int c = b - 1; c >= 0; --c) {
                 // FoX: the bias fi - F_j splits into a row term (fi - F_ref) and
@@ -589,43 +553,58 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 float dlt = 0.f;
                 if (fox) {
                     const float fref = fref_next;
-                    bars.fsm[r] = (fcol_next - fref) * kLog2e;
+                    if (hh == 0) bars.fsm[r] = (fcol_next - fref) * kLog2e;
                     dlt = fi - fref * kLog2e;
                     if (c >= 1) {
-                        fcol_next = Frow[(c - 1) * kC + r];
+                        if (hh == 0) fcol_next = Frow[(c - 1) * kC + r];
                         fref_next = Frow[(c - 1) * kC];
                     }
                 }
-                ok = group_all(2, 128, mbar_wait(&bars.s_full, sf_ph, a.err, abort_word, lim));
+                // [U|S]_c complete (the group barrier also publishes the prefixes)
+                ok = group_all(1, 256, mbar_wait(&bars.s_full, sf_ph, a.err, abort_word, lim));
                 if (!ok) break;
                 sf_ph ^= 1;
                 tc::fence_after_sync();
-                // one load of the logit row, then S is released to the next MMA
-                uint32_t v[128];
-                tc::tmem_ld128(lane_addr + kColS, v);
+                if (c >= 1) {
+                    // U -> the next carried rows (bf16), this half's columns; the
+                    // product has read the current ones, so they may be overwritten
+                    if (D == 128 || hh == 0) {
+                        uint32_t u[64], pk[32];
+                        tc::tmem_ld64(lane_addr + kColU + (D == 128 ? hh * 64 : 0), u);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            pk[j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
+                        tc::tmem_st32(lane_addr + kColQt + (D == 128 ? hh * 32 : 0), pk);
+                        tc::tmem_wait_st();
+                    }
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars.qb_conv_full);
+                }
+                // this half of the logit row, then S is released to the next MMA
+                uint32_t v[64];
+                tc::tmem_ld64(lane_addr + kColS + hh * 64, v);
                 tc::fence_before_sync();
-                named_bar(2, 128);  // also publishes this chunk's FoX prefix
-                if (threadIdx.x == 128) mbar_arrive(&bars.s_empty);
-                // row extremes over interleaved partial results, so that no
-                // chain of 128 dependent max operations sits in the step (the
-                // maximum is exact, so the order changes nothing)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.s_empty);
+                // row extremes over interleaved partial results (exact in any order)
                 float mx = -INFINITY;
                 if (kFox) {
                     // the chunk's column prefixes, four per shared-memory load
-                    const uint32_t fsm_s = smem_u32(bars.fsm);
-                    float mp[4];  // four here: eight push this instance into spills
+                    const uint32_t fsm_s = smem_u32(bars.fsm + hh * 64);
+                    float mp[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) mp[i] = -INFINITY;
 #pragma unroll
-                    for (int j4 = 0; j4 < kC / 4; ++j4) {
+                    for (int j4 = 0; j4 < 16; ++j4) {
                         const uint4 f4 = tc::lds128(fsm_s + 16 * j4);
                         const uint32_t fw[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int j = 4 * j4 + e;
-                            const float t = fmaf(__uint_as_float(v[j]), sl2, -__uint_as_float(fw[e]));
-                            v[j] = __float_as_uint(t);
-                            mp[e] = fmaxf(mp[e], t);
+                            const float tt = fmaf(__uint_as_float(v[j]), sl2, -__uint_as_float(fw[e]));
+                            v[j] = __float_as_uint(tt);
+                            mp[e] = fmaxf(mp[e], tt);
                         }
                     }
 #pragma unroll
@@ -638,24 +617,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
 #pragma unroll
-                        for (int j = 0; j < kC; ++j) mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(v[j]));
+                        for (int j = 0; j < 64; ++j) mp[j & 7] = fmaxf(mp[j & 7], __uint_as_float(v[j]));
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mx = fmaxf(mx, mp[i]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mp[i] = INFINITY;
 #pragma unroll
-                        for (int j = 0; j < kC; ++j) mp[j & 7] = fminf(mp[j & 7], __uint_as_float(v[j]));
+                        for (int j = 0; j < 64; ++j) mp[j & 7] = fminf(mp[j & 7], __uint_as_float(v[j]));
                         mx = INFINITY;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mx = fminf(mx, mp[i]);
                     }
                     mx *= sl2;
                 }
+                // the row maximum from both halves (the next write of this slot
+                // comes after the next step's group barrier)
+                bars.xm[hh][r] = mx;
+                named_bar(pair_bar, 64);
+                mx = fmaxf(bars.xm[0][r], bars.xm[1][r]);
                 // lazy rescale: keep the reference max unless it grows by > 2^8.
                 // The decision is made per warp (the O rescale uses warp-aligned
-                // TMEM loads/stores); a lane that did not need it rescales by its
-                // exact factor, which is <= 1.
+                // TMEM loads/stores) and is the same in both warps of a quadrant;
+                // a lane that did not need it rescales by its exact factor, <= 1.
                 const bool rescale = __any_sync(0xffffffffu, mx - m > kRescaleThreshold);
                 const float mnew = rescale ? fmaxf(m, mx) : m;
                 const float alpha = rescale ? exp2f(m - mnew) : 1.f;
@@ -664,9 +648,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 const float xs = kFox ? 1.f : sl2;
                 const float off = kFox ? dlt - mnew : -mnew;
                 float sum0 = 0.f, sum1 = 0.f;
-                uint32_t pk[kC / 2];
+                uint32_t pk[32];
 #pragma unroll
-                for (int j4 = 0; j4 < kC / 4; ++j4) {
+                for (int j4 = 0; j4 < 16; ++j4) {
                     float p[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -680,49 +664,55 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 // previous PV done: P buffer free and O stable (the first step
                 // follows the previous tile's epilogue, which waited already)
                 if (c < b - 1) {
-                    ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
+                    ok = group_all(1, 256, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
                     if (!ok) break;
                     od_ph ^= 1;
                     tc::fence_after_sync();
                 }
                 if (rescale) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < kOH / 32; ++cc) {
                         uint32_t o[32];
-                        tc::tmem_ld32(lane_addr + kColO + cc * 32, o);
+                        tc::tmem_ld32(lane_addr + kColO + hh * kOH + cc * 32, o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc::tmem_st32(lane_addr + kColO + cc * 32, o);
+                        tc::tmem_st32(lane_addr + kColO + hh * kOH + cc * 32, o);
                     }
-                    tc::tmem_wait_st();
                 }
-                tc::tmem_st32(lane_addr + kColP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-                tc::tmem_st32(lane_addr + kColP + 32,
-                              *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                tc::tmem_st32(lane_addr + kColP + hh * 32, pk);
                 tc::tmem_wait_st();
                 l = l * alpha + (sum0 + sum1);
                 m = mnew;
                 tc::fence_before_sync();
-                named_bar(2, 128);
-                if (threadIdx.x == 128) mbar_arrive(&bars.p_full);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_full);
+                // FoX: the first step has no group barrier between this step's
+                // reads of the prefixes and the next step's writes
+                if (fox && c == b - 1 && c >= 1) named_bar(1, 256);
             }
             if (!ok) break;
-            // epilogue: out = O / l, lse = ln(2) * (m + log2 l)
-            ok = group_all(2, 128, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
+            // epilogue: out = O / l, lse = ln(2) * (m + log2 l), l the sum of the
+            // two halves' partial sums
+            ok = group_all(1, 256, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
             if (!ok) break;
             od_ph ^= 1;
             tc::fence_after_sync();
-            const float inv = 1.f / l;
-            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D;
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t v[64];
+            bars.xm[hh][r] = l;
+            named_bar(pair_bar, 64);
+            const float lt = bars.xm[0][r] + bars.xm[1][r];
+            const float inv = 1.f / lt;
+            __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D + hh * kOH;
+            {
+                uint32_t v[kOH];
                 __syncwarp();  // the ragged-row branch below diverges; the load is warp-aligned
-                tc::tmem_ld64(lane_addr + kColO + cc * 64, v);
+                if constexpr (kOH == 64)
+                    tc::tmem_ld64(lane_addr + kColO + hh * kOH, v);
+                else
+                    tc::tmem_ld32(lane_addr + kColO + hh * kOH, v);
                 if (row < a.L) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < kOH / 8; ++q) {
                         uint4 u;
                         u.x = pack_bf16(__uint_as_float(v[q * 8 + 0]) * inv,
                                         __uint_as_float(v[q * 8 + 1]) * inv);
@@ -732,14 +722,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                                         __uint_as_float(v[q * 8 + 5]) * inv);
                         u.w = pack_bf16(__uint_as_float(v[q * 8 + 6]) * inv,
                                         __uint_as_float(v[q * 8 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + cc * 64 + q * 8) = u;
+                        *reinterpret_cast<uint4 *>(orow + q * 8) = u;
                     }
                 }
             }
-            if (a.lse && row < a.L) a.lse[(size_t)bh * a.Lout + lrow] = (m + log2f(l)) * kLn2;
+            if (hh == 0 && a.lse && row < a.L)
+                a.lse[(size_t)bh * a.Lout + lrow] = (m + log2f(lt)) * kLn2;
             tc::fence_before_sync();
         }
-    }
+      }
 
     }
     tc::fence_before_sync();
