@@ -447,8 +447,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             int vs = 0;
             uint32_t vph = 0, pf_ph = 0;
             bool ok = true;
-            // O already holds the chunk's own attention block (written by the
-            // row group), so every PV accumulates: V_{b-1}, ..., V_0 per tile
+            // V_{b-1}, ..., V_0 per tile; the tile's first P V writes O, the
+            // rest accumulate (the chunk's own block joins in the epilogue)
             int ts = 0;
             uint32_t tf_ph = 0;
             while (ok) {
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     pf_ph ^= 1;
                     tc::fence_after_sync();
                     gemm_pv<D>(tmem + kColO, tmem + kColP, tc::desc_lo(sV + vs * kTileBytes, true),
-                               true);
+                               c < b - 1);
                     tc::mma_commit(&bars.v_empty[vs]);
                     if (++vs == kVSlots) {
                         vs = 0;
@@ -521,27 +521,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 }
                 continue;
             }
-            // start from the chunk's own block: O = OD (weights summing to 1
-            // against the reference m = LSD in log2 units); half 0 carries
-            // that weight in its partial row sum
-#pragma unroll
-            for (int cc = 0; cc < kOH / 32; ++cc) {
-                uint32_t o[32];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 u = reinterpret_cast<const uint4 *>(odrow)[cc * 4 + q];
-                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
-                        o[q * 8 + 2 * e] = __float_as_uint(f.x);
-                        o[q * 8 + 2 * e + 1] = __float_as_uint(f.y);
-                    }
-                }
-                tc::tmem_st32(lane_addr + kColO + hh * kOH + cc * 32, o);
-            }
-            tc::tmem_wait_st();
-            float m = lsd * kLog2e, l = hh == 0 ? 1.f : 0.f;
+            // the scan starts from an empty state (the tile's first P V writes O
+            // without accumulating); the chunk's own block joins in the epilogue
+            float m = -INFINITY, l = 0.f;
             // FoX: the prefixes of the step's key chunk, loaded one step ahead
             // (a load at the step's start would hold the group's barrier);
             // half 0 publishes them, one per thread
@@ -669,7 +651,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                     od_ph ^= 1;
                     tc::fence_after_sync();
                 }
-                if (rescale) {
+                // (the first step's P V overwrites O: nothing to rescale)
+                if (rescale && c < b - 1) {
 #pragma unroll
                     for (int cc = 0; cc < kOH / 32; ++cc) {
                         uint32_t o[32];
@@ -692,8 +675,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (fox && c == b - 1 && c >= 1) named_bar(1, 256);
             }
             if (!ok) break;
-            // epilogue: out = O / l, lse = ln(2) * (m + log2 l), l the sum of the
-            // two halves' partial sums
+            // epilogue: the scan's state (O against the reference m, log2 units;
+            // l the sum of the two halves' partial sums) merged with the chunk's
+            // own block (OD normalised, LSD its log-sum-exp), weights 2^(m - M)
+            // and 2^(LSD log2e - M), M the larger; lse = ln(2) * (M + log2 of
+            // the summed weight).  This half's OD row is loaded before the wait
+            // for the last P V.
+            uint32_t od[kOH / 2];
+#pragma unroll
+            for (int j = 0; j < kOH / 8; ++j) {
+                const uint4 u = reinterpret_cast<const uint4 *>(odrow)[j];
+                od[4 * j] = u.x;
+                od[4 * j + 1] = u.y;
+                od[4 * j + 2] = u.z;
+                od[4 * j + 3] = u.w;
+            }
             ok = group_all(1, 256, mbar_wait(&bars.o_done, od_ph, a.err, abort_word, lim));
             if (!ok) break;
             od_ph ^= 1;
@@ -701,7 +697,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             bars.xm[hh][r] = l;
             named_bar(pair_bar, 64);
             const float lt = bars.xm[0][r] + bars.xm[1][r];
-            const float inv = 1.f / lt;
+            const float lsd2 = lsd * kLog2e;
+            const float mm = fmaxf(m, lsd2);
+            const float wa = exp2f(m - mm), wb = exp2f(lsd2 - mm);
+            const float den = fmaf(lt, wa, wb);
+            const float ia = wa / den, ib = wb / den;
             __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D + hh * kOH;
             {
                 uint32_t v[kOH];
@@ -713,21 +713,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 if (row < a.L) {
 #pragma unroll
                     for (int q = 0; q < kOH / 8; ++q) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(
+                                *reinterpret_cast<const __nv_bfloat162 *>(&od[q * 4 + e]));
+                            y[2 * e] = fmaf(__uint_as_float(v[q * 8 + 2 * e]), ia, f.x * ib);
+                            y[2 * e + 1] = fmaf(__uint_as_float(v[q * 8 + 2 * e + 1]), ia, f.y * ib);
+                        }
                         uint4 u;
-                        u.x = pack_bf16(__uint_as_float(v[q * 8 + 0]) * inv,
-                                        __uint_as_float(v[q * 8 + 1]) * inv);
-                        u.y = pack_bf16(__uint_as_float(v[q * 8 + 2]) * inv,
-                                        __uint_as_float(v[q * 8 + 3]) * inv);
-                        u.z = pack_bf16(__uint_as_float(v[q * 8 + 4]) * inv,
-                                        __uint_as_float(v[q * 8 + 5]) * inv);
-                        u.w = pack_bf16(__uint_as_float(v[q * 8 + 6]) * inv,
-                                        __uint_as_float(v[q * 8 + 7]) * inv);
+                        u.x = pack_bf16(y[0], y[1]);
+                        u.y = pack_bf16(y[2], y[3]);
+                        u.z = pack_bf16(y[4], y[5]);
+                        u.w = pack_bf16(y[6], y[7]);
                         *reinterpret_cast<uint4 *>(orow + q * 8) = u;
                     }
                 }
             }
             if (hh == 0 && a.lse && row < a.L)
-                a.lse[(size_t)bh * a.Lout + lrow] = (m + log2f(lt)) * kLn2;
+                a.lse[(size_t)bh * a.Lout + lrow] = (mm + log2f(den)) * kLn2;
             tc::fence_before_sync();
         }
       }
