@@ -71,7 +71,7 @@ DECODE_TRAFFIC_PER_KEY = {False: (805.738240e6 + 354.663424e6) / 1573440,
                           True: (812.037376e6 + 349.548032e6) / 1573440}
 
 # DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
-SCAN_TRAFFIC_B2 = 145.729536e6 + 10.107136e6
+SCAN_TRAFFIC_B2 = 156.042752e6 + 11.008256e6
 
 
 def load_peaks():
