@@ -186,18 +186,25 @@ def job_throughput(units_per_rank, ms_per_step_max, ws):
 
 
 def timed_prefill(x, steps, warmup, ws, fox=False, sampler=None):
-    """Times K prefill steps (prep + scan) with CUDA events on the launching
-    stream; returns (ms_per_step, prep_ms, scan_ms)."""
+    """Times K prefill steps with CUDA events on the launching stream.  A step
+    is one path_attn_prefill_fwd call, in which the scan starts on the SMs the
+    prep's last chunks leave idle.  A second pass of K steps calls the two
+    stages separately, with an event between them, for the per-kernel times
+    (prep, scan) that the roofline uses.  Returns (ms_per_step, prep_ms,
+    scan_ms, clocks)."""
     q, k, v, w, beta = (x[n] for n in ("q", "k", "v", "w", "beta"))
     log_f = x.get("log_f") if fox else None
     stream = torch.cuda.current_stream()
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
     ws_t = pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f)
+
+    def step():
+        pa.path_attn_prefill_fwd(q, k, v, w, beta, log_f=log_f, out=out, lse=lse,
+                                 workspace=ws_t)
+
     for _ in range(warmup):
-        pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f, workspace=ws_t)
-        pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        step()
     barrier(ws)
     torch.cuda.synchronize()
     if sampler:
@@ -206,16 +213,25 @@ def timed_prefill(x, steps, warmup, ws, fox=False, sampler=None):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(steps):
-        ev[i][0].record(stream)
-        pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f, workspace=ws_t)
-        ev[i][1].record(stream)
-        pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
-        ev[i][2].record(stream)
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     barrier(ws)
     total = t0.elapsed_time(t1) / steps
+    # per-kernel breakdown: the same work as separate stage calls
+    for _ in range(warmup):
+        pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f, workspace=ws_t)
+        pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        pa.path_attn_prefill_prep(q, k, v, w, beta, log_f=log_f, workspace=ws_t)
+        ev[i][1].record(stream)
+        pa.path_attn_prefill_scan(q, w, v, ws_t, log_f=log_f, out=out, lse=lse)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
     prep = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     scan = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     if pa.path_attn_device_status() != 0:

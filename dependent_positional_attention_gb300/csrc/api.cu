@@ -60,6 +60,9 @@ int num_sms() {
     return cache[dev];
 }
 
+// Offset of the per-head ready counters within the prefill's counter region.
+constexpr size_t kReadyOff = 64;
+
 struct PrefillPlan {
     int BH, L, Lp, N, C, d;
     int dk;     // head dim of the kernels (128 on the tensor-core route)
@@ -144,8 +147,9 @@ path_status_t plan_prefill(const path_prefill_desc_t *desc, PrefillPlan *p) {
     p->off_scratch = off; off = align_up(off + (p->tc ? 0 : cc * 5 * 4), 256);
     // padded q, k, w, v and out, [BH][L][128] bf16 each
     p->off_pad = off; off = align_up(off + (p->pad ? (size_t)5 * p->BH * p->L * 128 * 2 : 0), 256);
-    // the tensor-core scan's tile counter
-    p->off_tile = off; off = align_up(off + (p->tc ? 4 : 0), 256);
+    // the tensor-core scan's tile counter, then (at kReadyOff) the prep's
+    // per-head counts of finished chunks
+    p->off_tile = off; off = align_up(off + (p->tc ? kReadyOff + (size_t)4 * p->BH : 0), 256);
     p->total = off;
     return ok();
 }
@@ -332,6 +336,7 @@ void set_whole_sequence(PrepTcArgs &ta, int N, int L, int Lp) {
     ta.Lq = Lp;
     ta.copy_v = 0;
     ta.pm_transposed = 1;
+    ta.ready = nullptr;
 }
 
 template <class T> T *at(void *base, size_t off) {
@@ -689,10 +694,16 @@ size_t path_attn_prefill_workspace_size(const path_prefill_desc_t *desc) {
     return p.total;
 }
 
-path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void *q,
-                                     const void *k, const void *v, const void *w,
-                                     const float *beta, const float *log_f, void *workspace,
-                                     size_t workspace_bytes, path_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// overlap: the scan is launched next and may start while the prep runs (the
+// fused forward); the prep then counts each head's finished chunks.
+path_status_t prefill_prep(const path_prefill_desc_t *desc, const void *q, const void *k,
+                           const void *v, const void *w, const float *beta, const float *log_f,
+                           void *workspace, size_t workspace_bytes, path_stream_t stream,
+                           bool overlap) {
     PrefillPlan p;
     path_status_t s = plan_prefill(desc, &p);
     if (s != PATH_OK) return s;
@@ -757,6 +768,15 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
+        if (overlap) {
+            // the scan's tile counter and the per-head counters, zeroed in
+            // stream order before the prep
+            s = cuda_status(cudaMemsetAsync(at<char>(workspace, p.off_tile), 0,
+                                            kReadyOff + (size_t)4 * p.BH, st),
+                            "counter reset");
+            if (s != PATH_OK) return s;
+            ta.ready = at<int>(workspace, p.off_tile + kReadyOff);
+        }
         return cuda_status(launch_prep_tc(maps, ta, sms, st), "tensor-core prep launch");
     }
     PrepSimtArgs pa;
@@ -771,10 +791,10 @@ path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void
     return cuda_status(launch_prep_simt(pa, p.bf16, false, st), "prep launch");
 }
 
-path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void *w,
-                                     const void *v, const float *log_f, void *out, float *lse,
-                                     void *workspace, size_t workspace_bytes,
-                                     path_stream_t stream) {
+// overlap: launched directly after prefill_prep(..., overlap = true).
+path_status_t prefill_scan(const path_prefill_desc_t *desc, const void *w, const void *v,
+                           const float *log_f, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, path_stream_t stream, bool overlap) {
     PrefillPlan p;
     path_status_t s = plan_prefill(desc, &p);
     if (s != PATH_OK) return s;
@@ -820,10 +840,11 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
         ta.cm = ChunkMap{1, 0, p.N};
         ta.nloc = p.N; ta.Lq = p.Lp; ta.Lout = p.L; ta.zs = p.BH; ta.d = ds;
         ta.tile_ctr = at<int>(workspace, p.off_tile);
+        ta.ready = overlap ? at<int>(workspace, p.off_tile + kReadyOff) : nullptr;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
         if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
-        s = cuda_status(launch_flash_tc(maps, ta, sms, st), "tensor-core scan launch");
+        s = cuda_status(launch_flash_tc(maps, ta, sms, st, overlap), "tensor-core scan launch");
         if (s != PATH_OK || !p.pad) return s;
         return cuda_status(launch_unpad_rows(out, out_user, (size_t)p.BH * p.L, p.d, st),
                            "unpad launch");
@@ -833,6 +854,24 @@ path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void
     fa.Sd = Sd; fa.F = F; fa.out = out; fa.lse = lse; fa.scale = desc->scale;
     fa.BH = p.BH; fa.L = p.L; fa.Lp = p.Lp; fa.N = p.N; fa.C = p.C; fa.d = p.d;
     return cuda_status(launch_flash_simt(fa, p.bf16, st), "scan launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+path_status_t path_attn_prefill_prep(const path_prefill_desc_t *desc, const void *q,
+                                     const void *k, const void *v, const void *w,
+                                     const float *beta, const float *log_f, void *workspace,
+                                     size_t workspace_bytes, path_stream_t stream) {
+    return prefill_prep(desc, q, k, v, w, beta, log_f, workspace, workspace_bytes, stream, false);
+}
+
+path_status_t path_attn_prefill_scan(const path_prefill_desc_t *desc, const void *w,
+                                     const void *v, const float *log_f, void *out, float *lse,
+                                     void *workspace, size_t workspace_bytes,
+                                     path_stream_t stream) {
+    return prefill_scan(desc, w, v, log_f, out, lse, workspace, workspace_bytes, stream, false);
 }
 
 path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void *q,
@@ -845,10 +884,11 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
     if (!aligned16(v)) return fail(PATH_ERR_INVALID_ARG, "v is not 16-byte aligned");
     if (!aligned16(out)) return fail(PATH_ERR_INVALID_ARG, "out is not 16-byte aligned");
     if (lse && !aligned16(lse)) return fail(PATH_ERR_INVALID_ARG, "lse is not 16-byte aligned");
-    path_status_t s = path_attn_prefill_prep(desc, q, k, v, w, beta, log_f, workspace,
-                                             workspace_bytes, stream);
+    // the scan starts on the SMs the prep's last chunks leave idle
+    path_status_t s = prefill_prep(desc, q, k, v, w, beta, log_f, workspace, workspace_bytes,
+                                   stream, true);
     if (s != PATH_OK) return s;
-    return path_attn_prefill_scan(desc, w, v, log_f, out, lse, workspace, workspace_bytes, stream);
+    return prefill_scan(desc, w, v, log_f, out, lse, workspace, workspace_bytes, stream, true);
 }
 
 size_t path_attn_prefill_bwd_workspace_size(const path_prefill_desc_t *desc) {
@@ -1169,7 +1209,7 @@ path_status_t path_attn_cp_prep(const path_prefill_desc_t *desc, int32_t world, 
     ta.LSD = at<float>(workspace, p.off_LSD);
     ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
     ta.cm = p.cm; ta.nloc = p.nloc; ta.Lin = p.Lr; ta.Lq = p.Lq; ta.copy_v = 1;
-    ta.pm_transposed = 1;
+    ta.pm_transposed = 1; ta.ready = nullptr;
     ta.err = error_flag_ptr();
     const int sms = num_sms();
     if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");
@@ -1217,6 +1257,7 @@ path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, 
     ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
     ta.cm = p.cm; ta.nloc = p.nloc; ta.Lq = p.Lq; ta.Lout = p.Lr; ta.zs = 3 * p.BH; ta.d = 128;
     ta.tile_ctr = at<int>(workspace, p.off_tile);
+    ta.ready = nullptr;
     ta.err = error_flag_ptr();
     const int sms = num_sms();
     if (sms <= 0) return fail(PATH_ERR_CUDA, "device query failed");

@@ -116,4 +116,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of device time
 
+// ------------------------------------------------------ grid-level ordering
+
+// Lets the grid launched after this one on the stream with programmatic
+// stream serialisation start while this one still runs (a no-op otherwise).
+// The dependent grid must then order its reads itself (counter_wait).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Adds v to a global counter with release semantics at GPU scope: every write
+// this thread has made or observed is visible to a thread that reads the new
+// value with an acquire.
+__device__ __forceinline__ void counter_release_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int counter_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until the global counter *p reaches `target` (acquire at GPU
+// scope).  Gives up like mbar_wait: after `limit_ns` of device time it sets
+// the error flag and the CTA abort word and returns false; it also returns
+// false once another role of the CTA has aborted.
+__device__ __forceinline__ bool counter_wait(const int *p, int target, uint32_t *err_flag,
+                                             volatile int *abort_word, uint64_t limit_ns) {
+    if (counter_acquire(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(200);
+        if (counter_acquire(p) >= target) return true;
+        if (abort_word && *abort_word) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            set_error(err_flag, kErrTimeout);
+            if (abort_word) *abort_word = 1;
+            return false;
+        }
+    }
+}
+
 }  // namespace path

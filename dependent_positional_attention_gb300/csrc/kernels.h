@@ -219,13 +219,21 @@ struct FlashTcArgs {
     int Lq, Lout;             // local padded rows, local rows
     int zs;                   // z stride between owners in the key-side maps
     int d;                    // head dim of q, v, out: 128, or 64 (the workspace stays 128 wide)
-    int *tile_ctr;            // device counter of the dynamic tile queue (the launcher zeroes
-                              // it on the stream first), or null: static round-robin tiles
+    int *tile_ctr;            // device counter of the dynamic tile queue, or null: static
+                              // round-robin tiles
+    const int *ready;         // [BH] chunks of each head the prep has finished (the prep's
+                              // PrepTcArgs::ready), when the scan overlaps the prep: a tile
+                              // starts once its head counts nloc.  Null: the prep is complete
     uint32_t *err;
 };
 
+// after_prep = false: the launcher zeroes tile_ctr on the stream first and
+// launches in stream order.  after_prep = true: the launch directly follows
+// the prep's on the stream and may start while the prep runs (programmatic
+// stream serialisation); the caller zeroed tile_ctr and a.ready before the
+// prep launch.
 cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
-                            cudaStream_t st);
+                            cudaStream_t st, bool after_prep = false);
 
 // Tensor-core prep (bf16, head_dim 128, chunk 128): maps over the raw q, k, w,
 // v inputs ([BH][L][128]) and over the Qh, Kh, Pm, OD outputs ([BH][Lp][128]),
@@ -251,6 +259,8 @@ struct PrepTcArgs {
     int Lin, Lq;         // rows per head of the inputs and of the outputs
     int copy_v;          // also store each chunk's V tile through maps.vx
     int pm_transposed;   // store Pm^T (the forward scan) instead of Pm (the backward)
+    int *ready;          // [BH] zeroed counters, each raised by one (release) once all
+                         // of a chunk's outputs are in global memory; or null
     uint32_t *err;
 };
 

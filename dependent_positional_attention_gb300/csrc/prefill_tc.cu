@@ -341,8 +341,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 // it is claimed now, so that the counter's round trip overlaps
                 // this tile's loads
                 const int t = t_next < T ? t_next : -1;
-                if (t >= 0)
+                if (t >= 0) {
                     t_next = dynamic ? (int)gridDim.x + atomicAdd(a.tile_ctr, 1) : t + gridDim.x;
+                    // running behind the prep: the tile's head must be complete
+                    // (its rows, chunk products and own-chunk outputs) before
+                    // any role reads them; the tensor copies read after the
+                    // acquire
+                    if (a.ready) {
+                        ok = counter_wait(a.ready + tile_of(t, a).bh, a.nloc, a.err, abort_word,
+                                          lim);
+                        if (!ok) break;
+                        tc::fence_proxy_async_global();
+                    }
+                }
                 ok = mbar_wait(&bars.tile_empty[ts], te_ph ^ 1, a.err, abort_word, lim);
                 if (!ok) break;
                 bars.tile_ring[ts] = t;
@@ -509,14 +520,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             const int lrow = tl.i * kC + r;   // in the local rows
             // the prep's own-chunk output is 128 wide (head_dim 64 zero-padded)
             const __nv_bfloat16 *odrow = a.OD + ((size_t)bh * a.Lq + lrow) * 128 + hh * kOH;
-            const float lsd = a.LSD[(size_t)bh * a.Lq + lrow];
+            // OD and LSD through L2 only (.cg): the prep may have written
+            // them while this grid ran
+            const float lsd = __ldcg(a.LSD + (size_t)bh * a.Lq + lrow);
             if (b == 0) {
                 // the chunk attends only to itself: the prep's result is final
                 if (row < a.L) {
                     __nv_bfloat16 *orow = a.out + ((size_t)bh * a.Lout + lrow) * D + hh * kOH;
 #pragma unroll
                     for (int j = 0; j < kOH / 8; ++j)
-                        reinterpret_cast<uint4 *>(orow)[j] = reinterpret_cast<const uint4 *>(odrow)[j];
+                        reinterpret_cast<uint4 *>(orow)[j] =
+                            __ldcg(reinterpret_cast<const uint4 *>(odrow) + j);
                     if (hh == 0 && a.lse) a.lse[(size_t)bh * a.Lout + lrow] = lsd;
                 }
                 continue;
@@ -684,7 +698,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             uint32_t od[kOH / 2];
 #pragma unroll
             for (int j = 0; j < kOH / 8; ++j) {
-                const uint4 u = reinterpret_cast<const uint4 *>(odrow)[j];
+                const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(odrow) + j);
                 od[4 * j] = u.x;
                 od[4 * j + 1] = u.y;
                 od[4 * j + 2] = u.z;
@@ -749,7 +763,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }  // namespace
 
 cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int num_sms,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool after_prep) {
     const int T = a.nloc * a.BH;
     const int grid = T < num_sms ? T : num_sms;
     if (a.d != 128 && a.d != 64) return cudaErrorInvalidValue;
@@ -759,12 +773,27 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
     const int smem = a.d == 64 ? smem_bytes<64>() : smem_bytes<128>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (a.tile_ctr) {
-        e = cudaMemsetAsync(a.tile_ctr, 0, sizeof(int), st);
-        if (e != cudaSuccess) return e;
+    if (!after_prep) {
+        if (a.tile_ctr) {
+            e = cudaMemsetAsync(a.tile_ctr, 0, sizeof(int), st);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<grid, kThreadsTC, smem, st>>>(maps, a);
+        return cudaGetLastError();
     }
-    kern<<<grid, kThreadsTC, smem, st>>>(maps, a);
-    return cudaGetLastError();
+    // behind the prep: each CTA may start on an SM the prep has left, and
+    // its tiles wait on the prep's per-head counters
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps, a);
 }
 
 }  // namespace path

@@ -172,6 +172,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int total = a.nloc * a.BH;
     volatile int *abort_word = &bars.abort_word;
     constexpr uint64_t lim = kWaitLimitNs;
+    // a scan launched behind this grid may take each SM this grid leaves;
+    // it waits on the per-head counters (a.ready) before reading any output
+    launch_dependents();
 
     if (tid == 0) {
         uint64_t *one[] = {&bars.tma_w, &bars.tma_qk, &bars.vbar, &bars.g_done, &bars.qkw_done,
@@ -207,6 +210,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             // outstanding loads (parity of the phase still to land, or -1),
             // waited for before the CTA exits after an abort
             int pend_w = -1, pend_qk = -1, pend_v = -1;
+            // the head of the previous chunk, counted in a.ready once its
+            // stores are complete (checked a chunk later, when they long are)
+            int done_bh = -1;
+            auto publish = [&](int bh) {
+                tc::fence_proxy_async_global();
+                counter_release_add(a.ready + bh, 1);
+            };
             auto wait = [&](uint64_t *bar, uint32_t ph) {
                 ok = ok && mbar_wait(bar, ph, a.err, abort_word, lim);
                 if (ok) tc::fence_after_sync();
@@ -340,6 +350,18 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 tc::bulk_commit();
                 tc::bulk_wait_read();
                 mbar_arrive(&bars.xfree);
+                if (a.ready) {
+                    // every group but this chunk's (Qh/Kh/Pm, V copy, OD) is
+                    // complete: the previous chunk is in global memory
+                    if (done_bh >= 0) {
+                        if (a.copy_v)
+                            tc::bulk_wait_all_but<3>();
+                        else
+                            tc::bulk_wait_all_but<2>();
+                        publish(done_bh);
+                    }
+                    done_bh = bh;
+                }
             }
             if (!ok) {
                 // let every copy this thread issued land before the CTA exits
@@ -352,6 +374,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             tc::mma_commit(&bars.drain);
             mbar_wait(&bars.drain, 0, a.err, nullptr, lim);
             tc::bulk_wait();
+            if (a.ready && ok && done_bh >= 0) publish(done_bh);
         }
         __syncwarp();
     } else {

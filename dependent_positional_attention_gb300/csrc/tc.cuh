@@ -64,13 +64,19 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
                  : "memory");
 }
 
-// Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
+// All committed bulk stores but the N most recent groups are complete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_all_but() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Brings `bytes` (a multiple of 16) at the 16-byte aligned global address
 // `p` into L2, without waiting.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

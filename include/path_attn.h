@@ -105,7 +105,10 @@ path_status_t path_attn_prefill_fwd(const path_prefill_desc_t *desc, const void 
 
 /*
  * The two stages of path_attn_prefill_fwd, callable separately (same
- * descriptor, same workspace; prefill_fwd is exactly prep then scan):
+ * descriptor, same workspace; prefill_fwd computes exactly prep then scan,
+ * with identical results; inside prefill_fwd the scan may start on the SMs
+ * the prep has left while the prep's last chunks run, each of its query
+ * tiles waiting until the prep has finished that tile's head):
  *
  * path_attn_prefill_prep: per chunk, the UT transform of the chunk's
  * transitions and everything derived from it (boundary-adjusted rows, the

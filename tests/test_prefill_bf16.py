@@ -71,6 +71,41 @@ def test_repeat_calls_are_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def stages(g, out, lse):
+    """The prep and the scan as two calls: the scan starts after the prep has
+    finished."""
+    ws = pa.path_attn_prefill_prep(g["q"], g["k"], g["v"], g["w"], g["beta"],
+                                   log_f=g.get("log_f"))
+    pa.path_attn_prefill_scan(g["q"], g["w"], g["v"], ws, log_f=g.get("log_f"), out=out,
+                              lse=lse)
+    return ws
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", [(8, 12, 4096, 128, False), (8, 12, 4096, 128, True),
+                                   (8, 12, 4096, 64, False), (3, 2, 700, 128, False),
+                                   (2, 3, 1000, 96, True)])
+def test_fused_call_equals_stages(shape):
+    """In the one-call forward the scan's tiles start while the prep still
+    runs, each once the prep's counter for its head is complete.  Every tile
+    does the same arithmetic as in the two-call form, so the outputs must be
+    identical bit for bit, on every repeat; a tile that read a row, chunk
+    product or own-chunk output before it was written would differ."""
+    B, H, L, d, fox = shape
+    x = wl.prefill_inputs(B, H, L, d, "bf16", seed=90 + L + d, fox=fox, device="cuda")
+    out0, lse0 = torch.empty_like(x["q"]), torch.empty(B, H, L, device=DEV)
+    ws = stages(x, out0, lse0)
+    out, lse = torch.empty_like(out0), torch.empty_like(lse0)
+    for _ in range(8):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        pa.path_attn_prefill_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"],
+                                 log_f=x.get("log_f"), out=out, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert pa.path_attn_device_status() == 0
+        assert torch.equal(out, out0) and torch.equal(lse, lse0)
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("wname", ["PREFILL_4K", "FOX_4K", "PREFILL_32K"])
 def test_full_size_sampled_rows(wname):
