@@ -70,8 +70,9 @@ def backward_flops(B, H, L, d, C=CHUNK):
 DECODE_TRAFFIC_PER_KEY = {False: (805.738240e6 + 354.663424e6) / 1573440,
                           True: (812.037376e6 + 349.548032e6) / 1573440}
 
-# DRAM read + write (bytes) of one scan launch, B2 H12 L4096 d128, from ncu
-SCAN_TRAFFIC_B2 = 156.042752e6 + 11.008256e6
+# DRAM read + write (bytes) of one scan launch of the headline workload (B8 H12 L4096 d128),
+# from a one-pass ncu capture of that launch
+SCAN_TRAFFIC_B8 = 507.67e6 + 88.50e6
 
 
 def load_peaks():
@@ -256,10 +257,10 @@ def prefill_block(wlk, steps, warmup, ws, peaks, seed=0, sampler=None):
         "roofline": {"kernel": "flash_tc_kernel (tensor-core scan)", "bound": "tensor",
                      "achieved": scan_tf, "peak": peak, "unit": "TFLOP/s",
                      "frac": scan_tf / peak,
-                     # DRAM bytes per launch: ncu read + write of this kernel on the B2 case,
-                     # scaled by the batch; the headline B8 launch only
-                     "traffic": (SCAN_TRAFFIC_B2 * B / 2
-                                 if (H, L, d) == (12, 4096, 128) and not wlk.fox else None),
+                     # DRAM bytes per launch: ncu read + write of this kernel's headline
+                     # launch (B8 H12 L4096 d128, not FoX); null for the other workloads
+                     "traffic": (SCAN_TRAFFIC_B8
+                                 if (B, H, L, d) == (8, 12, 4096, 128) and not wlk.fox else None),
                      "peak_source": peaks["source"] + " bf16 dense (burst)"},
     }
     del x
