@@ -782,17 +782,19 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
     // or so apart, so most tiles read chunks another CTA has just brought
     // into L2.  About ten CTAs per head (grid / 10 heads per group; at least
     // 2.5 grids of tiles per group, so that the group's light tiles still
-    // balance the CTAs' ends): at B8 H12 L4096 (16 heads per group against
-    // all 96 interleaved) the scan went from 0.533 to 0.459 ms; at
-    // B1 H12 L32768 the group is all 12 heads, the order as before.
+    // balance the CTAs' ends), in groups of equal size (a small last group
+    // balanced badly: B2 H12 L4096 in groups of 16 and 8 heads was 13%
+    // slower than one group).  B8 H12 L4096 (6 groups of 16 heads against
+    // all 96 interleaved): 0.533 -> 0.459 ms; B16: 1.39 -> 0.93 ms; up to
+    // 24 heads, and B1 H12 L32768, one group, the order as before.
     FlashTcArgs ag = a;
     {
         long long g = (grid + 9) / 10;
         const long long gb = (5ll * grid + 2ll * a.nloc - 1) / (2ll * a.nloc);
         if (gb > g) g = gb;
-        if (g > a.BH) g = a.BH;
-        if (g < 1) g = 1;
-        ag.tile_group = (int)g;
+        long long groups = a.BH / g;
+        if (groups < 1) groups = 1;
+        ag.tile_group = (int)((a.BH + groups - 1) / groups);
     }
     if (!after_prep) {
         if (a.tile_ctr) {
