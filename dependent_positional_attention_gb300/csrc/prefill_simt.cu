@@ -116,27 +116,70 @@ __global__ void __launch_bounds__(kThreads) prep_simt_kernel(PrepSimtArgs a) {
 
 // ------------------------------------------------------------------ FoX prefix
 
-// F[bh][i] = sum_{s<=i} log_f[bh][s] (fp64 running sum, stored fp32); padded
-// positions repeat the last value.  One warp per head.
-__global__ void fox_prefix_kernel(const float *log_f, float *F, int L, int Lp, int BH) {
-    const int bh = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    const int lane = threadIdx.x & 31;
+// F[bh][i] = sum_{s<=i} log_f[bh][s] (fp64 sums, stored fp32); padded
+// positions repeat the last value.  One block of kPrefixThreads per head,
+// over tiles of kPrefixThreads * 16 positions: each thread sums its 16
+// consecutive values, a block-wide exclusive scan of those sums (warp
+// shuffles, then the warp totals) gives each thread its offset, and a second
+// pass over the values held in registers writes the prefixes.  (One warp per
+// head with a serial fp64 chain per lane took tens of microseconds at
+// B8 H12 L4096, on the path of every PaTH-FoX call.)
+constexpr int kPrefixThreads = 256;
+__global__ void __launch_bounds__(kPrefixThreads)
+    fox_prefix_kernel(const float *log_f, float *F, int L, int Lp, int BH) {
+    constexpr int kPer = 16, kWarps = kPrefixThreads / 32;
+    __shared__ double wtot[kWarps];
+    const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (bh >= BH) return;
     const float *lf = log_f + (size_t)bh * L;
     float *out = F + (size_t)bh * Lp;
-    const int seg = (Lp + 31) / 32;
-    const int s0 = lane * seg, s1 = min(Lp, s0 + seg);
-    double tot = 0.0;
-    for (int i = s0; i < s1; ++i) tot += (i < L) ? (double)lf[i] : 0.0;
-    double incl = tot;
-    for (int o = 1; o < 32; o <<= 1) {
-        double v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    double run = incl - tot;
-    for (int i = s0; i < s1; ++i) {
-        run += (i < L) ? (double)lf[i] : 0.0;
-        out[i] = (float)run;
+    double base = 0.0;
+    for (int t0 = 0; t0 < Lp; t0 += kPrefixThreads * kPer) {
+        const int i0 = t0 + tid * kPer;
+        float x[kPer];
+        double part = 0.0;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            x[e] = (i0 + e < L) ? lf[i0 + e] : 0.f;
+            part += (double)x[e];
+        }
+        // exclusive scan of the threads' sums: within the warp, then over warps
+        double incl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) wtot[warp] = incl;
+        __syncthreads();
+        double before = 0.0, total = 0.0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const double t = wtot[w];
+            if (w < warp) before += t;
+            total += t;
+        }
+        __syncthreads();  // wtot is rewritten by the next tile
+        double run = base + before + (incl - part);
+        if (i0 < Lp) {
+            float y[kPer];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                run += (double)x[e];
+                y[e] = (float)run;
+            }
+            if (i0 + kPer <= Lp && (reinterpret_cast<uintptr_t>(out + i0) & 15) == 0) {
+#pragma unroll
+                for (int e = 0; e < kPer; e += 4)
+                    *reinterpret_cast<float4 *>(out + i0 + e) =
+                        make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kPer; ++e)
+                    if (i0 + e < Lp) out[i0 + e] = y[e];
+            }
+        }
+        base += total;
     }
 }
 
@@ -276,8 +319,8 @@ cudaError_t launch_prep_simt(const PrepSimtArgs &a, bool bf16_in, bool bf16_out,
 
 cudaError_t launch_fox_prefix(const float *log_f, float *F, int L, int Lp, int BH,
                               cudaStream_t st) {
-    const int warps = 4;
-    fox_prefix_kernel<<<(BH + warps - 1) / warps, 32 * warps, 0, st>>>(log_f, F, L, Lp, BH);
+    if (BH <= 0) return cudaSuccess;
+    fox_prefix_kernel<<<BH, kPrefixThreads, 0, st>>>(log_f, F, L, Lp, BH);
     return cudaGetLastError();
 }
 
