@@ -479,6 +479,18 @@ def autotune_block(wlk):
             "ms_library_default": times[0], "speedup_vs_default": times[0] / times[best]}
 
 
+def scan_group_block(wlk):
+    """Tensor-core route: the scan's head-group size (the one tensor-core
+    launch parameter; the chunk is 128 there) swept on the one-call forward,
+    against the library's automatic size (key "0")."""
+    from dependent_positional_attention_gb300 import autotune
+    best, times = autotune.autotune_scan_group(wlk.batch, wlk.heads, wlk.seq_len,
+                                               wlk.head_dim, wlk.dtype)
+    return {"workload": wlk.name, "best_scan_group": best,
+            "ms_by_scan_group": {str(g): t for g, t in sorted(times.items())},
+            "ms_library_default": times[0], "speedup_vs_default": times[0] / times[best]}
+
+
 class OracleSampler:
     """fp64 oracle on uniformly sampled query rows of a few heads of a
     workload (inputs drawn once, with the workload's seeded generator)."""
@@ -621,6 +633,7 @@ def main():
         extra["backward_fox_4k"] = backward_block(wl.FOX_4K, max(3, steps // 2), 3, ws, peaks)
         extra["backward_4k_ws1gb"] = backward_block(head, max(3, steps // 2), 3, ws, peaks,
                                                     workspace_bytes=10 ** 9)
+        extra["scan_group_autotune_4k"] = scan_group_block(head)
         extra["chunk_autotune_f32_tiny"] = autotune_block(wl.TINY_F32)
         extra["chunk_autotune_bf16_d64"] = autotune_block(
             wl.PrefillWorkload("PaTH prefill fwd B8 H12 L4096 d64 bf16 (chunks 16-64 on the CUDA "

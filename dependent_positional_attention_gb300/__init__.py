@@ -60,7 +60,7 @@ class PrefillDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
                 ("seq_len", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("chunk", ctypes.c_int32)]
+                ("chunk", ctypes.c_int32), ("scan_group", ctypes.c_int32)]
 
 
 class DecodeDesc(ctypes.Structure):
@@ -174,11 +174,11 @@ def _need(t, name, shape=None, dtype=None):
                             % (name, t.dtype, dtype))
 
 
-def _prefill_desc(q, scale, chunk):
+def _prefill_desc(q, scale, chunk, scan_group=0):
     B, H, L, d = q.shape
     if scale is None:
         scale = d ** -0.5
-    return PrefillDesc(B, H, L, d, _dtype_code(q), float(scale), int(chunk))
+    return PrefillDesc(B, H, L, d, _dtype_code(q), float(scale), int(chunk), int(scan_group))
 
 
 def path_attn_prefill_workspace_size(desc: PrefillDesc) -> int:
@@ -186,10 +186,12 @@ def path_attn_prefill_workspace_size(desc: PrefillDesc) -> int:
 
 
 def path_attn_prefill_fwd(q, k, v, w, beta, log_f=None, out=None, lse=None, scale=None,
-                          chunk=0, workspace=None, stream=None, want_lse=True):
+                          chunk=0, workspace=None, stream=None, want_lse=True, scan_group=0):
     """Causal PaTH / PaTH-FoX attention forward (see path_attn_prefill_fwd in
     include/path_attn.h).  q, k, v, w: [B, H, L, d] CUDA tensors (float32 or
-    bfloat16); beta, log_f: float32 [B, H, L].  Returns (out, lse)."""
+    bfloat16); beta, log_f: float32 [B, H, L].  scan_group: heads per group
+    of the tensor-core scan's tile order (0 = automatic; speed only).
+    Returns (out, lse)."""
     import torch
     lib = load_library()
     B, H, L, d = q.shape
@@ -198,7 +200,7 @@ def path_attn_prefill_fwd(q, k, v, w, beta, log_f=None, out=None, lse=None, scal
     _need(beta, "beta", (B, H, L), torch.float32)
     if log_f is not None:
         _need(log_f, "log_f", (B, H, L), torch.float32)
-    desc = _prefill_desc(q, scale, chunk)
+    desc = _prefill_desc(q, scale, chunk, scan_group)
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", (B, H, L, d), q.dtype)
@@ -235,12 +237,12 @@ def path_attn_prefill_prep(q, k, v, w, beta, log_f=None, scale=None, chunk=0, wo
 
 
 def path_attn_prefill_scan(q, w, v, workspace, log_f=None, out=None, lse=None, scale=None,
-                          chunk=0, stream=None):
+                          chunk=0, stream=None, scan_group=0):
     """Stage 2 of the prefill (see path_attn_prefill_scan in include/path_attn.h);
     q is used for its shape and dtype only.  Returns (out, lse)."""
     import torch
     lib = load_library()
-    desc = _prefill_desc(q, scale, chunk)
+    desc = _prefill_desc(q, scale, chunk, scan_group)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:

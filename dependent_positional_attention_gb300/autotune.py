@@ -1,5 +1,5 @@
-"""Chunk-size autotune for the prefill (per batch, heads, seq_len, head_dim,
-dtype).
+"""Prefill autotune (per batch, heads, seq_len, head_dim, dtype): the chunk
+size on the CUDA-core route, and the tensor-core scan's head-group size.
 
 The chunk size C is a free parameter of the blockwise algorithm (the PaTH
 lecture notes, hands-on item 3, sweep it against wallclock).  The
@@ -10,6 +10,14 @@ choice: 16, 32, 64 or 128.  Each candidate, and the library's own default
 through path_attn_prefill_fwd, and the fastest candidate is cached for the
 process.  This module only chooses a parameter; the computation is the
 library's.
+
+On the tensor-core route the chunk stays 128, and what there is to choose is
+the order of the scan's query tiles: the heads per group
+(path_prefill_desc_t.scan_group).  The tiles of one group of heads go out,
+heaviest first, before the next group's, so that the CTAs on a head read key
+chunks another CTA has just brought into L2; the library's automatic size
+is about SM count / 10 heads.  autotune_scan_group times it against a few
+fixed sizes; every size gives identical results.
 """
 from __future__ import annotations
 
@@ -59,4 +67,42 @@ def autotune_chunk(batch: int, heads: int, seq_len: int, head_dim: int, dtype: s
             x["q"], x["k"], x["v"], x["w"], x["beta"], chunk=c, want_lse=False), reps)
     best = min((c for c in times if c), key=times.get)
     _cache[key] = (best, times)
+    return best, times
+
+
+_group_cache: dict = {}
+
+
+def scan_group_candidates(batch: int, heads: int):
+    """0 (the library's automatic size), powers of two below batch*heads,
+    and batch*heads (one group: every head interleaved)."""
+    bh = batch * heads
+    c = [0]
+    g = 4
+    while g < bh:
+        c.append(g)
+        g *= 2
+    c.append(bh)
+    return tuple(c)
+
+
+def autotune_scan_group(batch: int, heads: int, seq_len: int, head_dim: int = 128,
+                        dtype: str = "bf16", reps: int = 5, device: str = "cuda"):
+    """Returns (best_group, {group: median milliseconds}) of the one-call
+    forward on the tensor-core route for this shape; key 0 is the automatic
+    size.  Cached per process."""
+    key = (batch, heads, seq_len, head_dim, dtype)
+    if key in _group_cache:
+        return _group_cache[key]
+    import torch
+
+    x = wl.prefill_inputs(batch, heads, seq_len, head_dim, dtype, seed=0, device=device)
+    out = torch.empty_like(x["q"])
+    times = {}
+    for g in scan_group_candidates(batch, heads):
+        times[g] = _median_ms(lambda: path_attn_prefill_fwd(
+            x["q"], x["k"], x["v"], x["w"], x["beta"], out=out, want_lse=False,
+            scan_group=g), reps)
+    best = min(times, key=times.get)
+    _group_cache[key] = (best, times)
     return best, times

@@ -87,6 +87,7 @@ path_status_t check_prefill_desc(const path_prefill_desc_t *desc) {
         return fail(PATH_ERR_INVALID_ARG, "scale must be finite");
     if ((long long)desc->batch * desc->heads > 65535)
         return fail(PATH_ERR_UNSUPPORTED, "batch*heads must be <= 65535");
+    if (desc->scan_group < 0) return fail(PATH_ERR_INVALID_ARG, "scan_group must be >= 0");
     return ok();
 }
 
@@ -840,6 +841,7 @@ path_status_t prefill_scan(const path_prefill_desc_t *desc, const void *w, const
         ta.cm = ChunkMap{1, 0, p.N};
         ta.nloc = p.N; ta.Lq = p.Lp; ta.Lout = p.L; ta.zs = p.BH; ta.d = ds;
         ta.tile_ctr = at<int>(workspace, p.off_tile);
+        ta.tile_group = desc->scan_group;
         ta.ready = overlap ? at<int>(workspace, p.off_tile + kReadyOff) : nullptr;
         ta.err = error_flag_ptr();
         const int sms = num_sms();
@@ -1257,6 +1259,7 @@ path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, 
     ta.BH = p.BH; ta.L = p.L; ta.Lp = p.Lp; ta.N = p.N;
     ta.cm = p.cm; ta.nloc = p.nloc; ta.Lq = p.Lq; ta.Lout = p.Lr; ta.zs = 3 * p.BH; ta.d = 128;
     ta.tile_ctr = at<int>(workspace, p.off_tile);
+    ta.tile_group = desc->scan_group;
     ta.ready = nullptr;
     ta.err = error_flag_ptr();
     const int sms = num_sms();

@@ -224,7 +224,7 @@ struct FlashTcArgs {
     const int *ready;         // [BH] chunks of each head the prep has finished (the prep's
                               // PrepTcArgs::ready), when the scan overlaps the prep: a tile
                               // starts once its head counts nloc.  Null: the prep is complete
-    int tile_group;           // heads per group of the tile order (set by launch_flash_tc)
+    int tile_group;           // heads per group of the tile order; 0: launch_flash_tc chooses
     uint32_t *err;
 };
 

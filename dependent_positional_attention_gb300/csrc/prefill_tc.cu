@@ -788,7 +788,9 @@ cudaError_t launch_flash_tc(const FlashTcMaps &maps, const FlashTcArgs &a, int n
     // all 96 interleaved): 0.533 -> 0.459 ms; B16: 1.39 -> 0.93 ms; up to
     // 24 heads, and B1 H12 L32768, one group, the order as before.
     FlashTcArgs ag = a;
-    {
+    if (a.tile_group > 0) {
+        ag.tile_group = a.tile_group < a.BH ? a.tile_group : a.BH;  // the caller's choice
+    } else {
         long long g = (grid + 9) / 10;
         const long long gb = (5ll * grid + 2ll * a.nloc - 1) / (2ll * a.nloc);
         if (gb > g) g = gb;

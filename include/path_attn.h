@@ -64,6 +64,14 @@ typedef struct {
                        Otherwise 16, 32, 64 or 128; the default is 64
                        when batch*heads*seq_len <= 8192 and head_dim <= 64,
                        else 128. */
+    int32_t scan_group; /* tensor-core scan only: heads per group of its
+                           tile order (the query tiles of one group of heads
+                           are handed out, heaviest first, before the next
+                           group's).  0 = automatic: about SM count / 10 heads
+                           (at least 2.5 grids of tiles per group), groups of
+                           equal size.  Values above batch*heads mean one
+                           group.  It changes only the speed, never a result.
+                           Negative: PATH_ERR_INVALID_ARG. */
 } path_prefill_desc_t;
 
 /*

@@ -65,6 +65,11 @@ def test_prefill_rejects_bad_descriptors(lib):
     assert prefill(lib, D(1, 1, 16, 128, 1, 0.1, 64)) == pa.PATH_ERR_UNSUPPORTED
     assert lib.path_attn_prefill_workspace_size(ctypes.byref(D(0, 1, 16, 64, 0, 0.1, 0))) == 0
     assert b"batch" in lib.path_attn_last_error()
+    # the tensor-core scan's head-group size: >= 0 (0 = automatic)
+    assert lib.path_attn_prefill_workspace_size(ctypes.byref(D(1, 1, 16, 128, 1, 0.1, 0, -1))) == 0
+    assert b"scan_group" in lib.path_attn_last_error()
+    assert (lib.path_attn_prefill_workspace_size(ctypes.byref(D(1, 1, 16, 128, 1, 0.1, 0, 7))) ==
+            lib.path_attn_prefill_workspace_size(ctypes.byref(D(1, 1, 16, 128, 1, 0.1, 0, 0))))
 
 
 def test_prefill_rejects_bad_pointers_and_workspace(lib):
