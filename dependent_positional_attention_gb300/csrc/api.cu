@@ -1315,17 +1315,24 @@ int32_t path_attn_version(void) { return 100; }
 
 namespace path {
 namespace {
-// One thread waits on an mbarrier that expects an arrival nobody makes.
+// A global counter nothing raises (the form of the scan's wait for the
+// prep's chunks in the one-call forward).
+__device__ int g_selftest_counter = 0;
+
+// Lane 0 waits on an mbarrier that expects an arrival nobody makes; lane 1
+// waits for the counter above to reach 1.  Each has its own abort word, so
+// that each wait runs out on its own limit.
 __global__ void selftest_wait_kernel(uint32_t *err_flag, uint64_t limit_ns) {
     __shared__ uint64_t bar;
-    __shared__ int abort_word;
+    __shared__ int abort_word[2];
     if (threadIdx.x == 0) {
-        abort_word = 0;
+        abort_word[0] = abort_word[1] = 0;
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) mbar_wait(&bar, 0, err_flag, &abort_word, limit_ns);
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err_flag, &abort_word[0], limit_ns);
+    if (threadIdx.x == 1) counter_wait(&g_selftest_counter, 1, err_flag, &abort_word[1], limit_ns);
 }
 }  // namespace
 

@@ -371,7 +371,9 @@ path_status_t path_attn_cp_scan(const path_prefill_desc_t *desc, int32_t world, 
 path_status_t path_attn_device_status(int32_t clear);
 
 /*
- * Launches one tiny kernel whose mbarrier wait can never complete, bounded by
+ * Launches one tiny kernel whose two waits can never complete: one on an
+ * mbarrier, one on a global counter (the form in which the scan of
+ * path_attn_prefill_fwd waits for the prep's chunks).  Each is bounded by
  * limit_us microseconds of device time; the kernel then sets the device
  * error flag and exits cleanly.  Exists so tests can check the bounded-wait
  * path without hanging a GPU.
