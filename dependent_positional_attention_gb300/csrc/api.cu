@@ -13,8 +13,9 @@
 namespace path {
 
 // Device-resident state of the library: this error flag, set by kernels
-// whose bounded waits ran out, and the fixed split-KV scratch of the
-// allocation-free decode step (decode_noalloc.cu).
+// whose bounded waits ran out, the fixed split-KV scratch of the
+// allocation-free decode step (decode_noalloc.cu), and a counter that stays
+// zero for the bounded-wait self-test (end of this file).
 __device__ uint32_t g_error_flag;
 
 namespace {
